@@ -1,0 +1,338 @@
+/*
+ * oracle.c -- plain fp64 CPU reference (test infrastructure only; see
+ * oracle.h). Written from the definitions in the pages, step by step, with
+ * no blocking, fusion or reordering beyond what the definition states.
+ *
+ * ORACLE_MUTANT: when the test suite compiles this file with
+ * -DORACLE_MUTANT=<k>, one deliberate mistake is planted so that the tests
+ * can show that their pins catch it. The normal build never defines it.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Tangram, Sec. "Deterministic Budget Allocation": a static budget per head;
+ * a head never keeps more tokens than its sequence has. */
+int oracle_resolve_budget(int B, int Hkv, const int32_t *budget,
+                          const int32_t *seq_len, int32_t *n) {
+  if (B < 0 || Hkv <= 0 || !budget || !seq_len || !n) return -1;
+  for (int b = 0; b < B; ++b) {
+    if (seq_len[b] < 1) return -1;
+    for (int h = 0; h < Hkv; ++h)
+      if (budget[b * Hkv + h] < 1) return -1;
+  }
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < Hkv; ++h) {
+      int32_t c = budget[b * Hkv + h];
+      int32_t L = seq_len[b];
+#if ORACLE_MUTANT == 15
+      n[b * Hkv + h] = c > L ? c : L;
+#else
+      n[b * Hkv + h] = c < L ? c : L;
+#endif
+    }
+  return 0;
+}
+
+/* Softmax attention over the kept set of one KV head, for its g query
+ * heads (Tangram, Fig. 2: attention output over each head's critical tokens;
+ * plain scaled dot-product softmax attention). */
+int oracle_attn_head(int D, int g, int L, const double *q, const double *k,
+                     const double *v, int n, const int32_t *idx, double scale,
+                     double *out, double *w) {
+  if (D <= 0 || g <= 0 || L <= 0 || n <= 0 || n > L || !q || !k || !v ||
+      !idx || !out)
+    return -1;
+  for (int t = 0; t < n; ++t) {
+    if (idx[t] < 0 || idx[t] >= L) return -1;
+    if (t > 0 && idx[t] <= idx[t - 1]) return -1;
+  }
+  double *s = (double *)malloc(sizeof(double) * (size_t)n);
+  if (!s) return -1;
+  for (int j = 0; j < g; ++j) {
+    const double *qj = q + (size_t)j * D;
+    /* scores s_t = scale * <q_j, k_t> over the kept positions */
+    for (int t = 0; t < n; ++t) {
+#if ORACLE_MUTANT == 5
+      const double *kt = k + (size_t)t * D;
+#else
+      const double *kt = k + (size_t)idx[t] * D;
+#endif
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qj[d] * kt[d];
+#if ORACLE_MUTANT == 2
+      s[t] = dot;
+#elif ORACLE_MUTANT == 8
+      s[t] = -scale * dot;
+#else
+      s[t] = scale * dot;
+#endif
+    }
+    /* softmax: subtract the maximum, exponentiate, normalise */
+    double m = s[0];
+    for (int t = 1; t < n; ++t)
+      if (s[t] > m) m = s[t];
+#if ORACLE_MUTANT == 3
+    m = 0.0;
+#endif
+    double z = 0.0;
+    for (int t = 0; t < n; ++t) {
+      s[t] = exp(s[t] - m);
+      z += s[t];
+    }
+#if ORACLE_MUTANT == 4
+    z = 1.0;
+#endif
+    for (int t = 0; t < n; ++t) s[t] = s[t] / z;
+    if (w)
+      for (int t = 0; t < n; ++t) w[(size_t)j * n + t] = s[t];
+    /* out_j = sum_t w_t v_t */
+    double *oj = out + (size_t)j * D;
+    for (int d = 0; d < D; ++d) {
+      double acc = 0.0;
+#if ORACLE_MUTANT == 6
+      int nt = n > 1 ? n - 1 : n;
+#else
+      int nt = n;
+#endif
+      for (int t = 0; t < nt; ++t) {
+#if ORACLE_MUTANT == 7
+        acc += s[t] * v[(size_t)d * L + idx[t]];
+#else
+        acc += s[t] * v[(size_t)idx[t] * D + d];
+#endif
+      }
+      oj[d] = acc;
+    }
+  }
+  free(s);
+  return 0;
+}
+
+int oracle_decode_attn(int B, int Hq, int Hkv, int D, int Lmax,
+                       const int32_t *seq_len, const double *q,
+                       const double *k, const double *v,
+                       const int64_t *kept_off, const int32_t *kept_idx,
+                       double scale, double *out) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Lmax <= 0 || Hq % Hkv != 0 ||
+      !seq_len || !q || !k || !v || !kept_off || !kept_idx || !out)
+    return -1;
+  const int g = Hq / Hkv;
+  for (int b = 0; b < B; ++b)
+    if (seq_len[b] < 1 || seq_len[b] > Lmax) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int bh = 0; bh < B * Hkv; ++bh) {
+    int b = bh / Hkv, h = bh % Hkv;
+    int64_t n64 = kept_off[bh + 1] - kept_off[bh];
+    if (n64 < 1 || n64 > seq_len[b]) {
+      bad |= 1;
+      continue;
+    }
+    /* query heads of KV head h: j = h*g .. h*g+g-1 */
+    for (int jj = 0; jj < g; ++jj) {
+      int j = h * g + jj;
+#if ORACLE_MUTANT == 1
+      int hk = j % Hkv;
+#else
+      int hk = j / g;
+#endif
+      const double *kh = k + ((size_t)b * Hkv + hk) * (size_t)Lmax * D;
+      const double *vh = v + ((size_t)b * Hkv + hk) * (size_t)Lmax * D;
+      const int32_t *ix = kept_idx + kept_off[b * Hkv + hk];
+      int nn = (int)(kept_off[b * Hkv + hk + 1] - kept_off[b * Hkv + hk]);
+      if (oracle_attn_head(D, 1, seq_len[b], q + ((size_t)b * Hq + j) * D, kh,
+                           vh, nn, ix, scale, out + ((size_t)b * Hq + j) * D,
+                           NULL) != 0)
+        bad |= 1;
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/* Tangram, Fig. 8(b)/(c): a head group has its own page table; all heads of
+ * the group walk the same pages, so the group needs as many pages as its
+ * longest head. */
+int oracle_group_pages(int B, int Hkv, const int32_t *n,
+                       const int32_t *head_group, int G, int P,
+                       int32_t *pages) {
+  if (B < 0 || Hkv <= 0 || G <= 0 || P <= 0 || !n || !head_group || !pages)
+    return -1;
+  for (int h = 0; h < Hkv; ++h)
+    if (head_group[h] < 0 || head_group[h] >= G) return -1;
+  for (int gi = 0; gi < G; ++gi)
+    for (int b = 0; b < B; ++b) {
+      int32_t mx = 0;
+#if ORACLE_MUTANT == 10
+      mx = 0x7fffffff;
+#endif
+      for (int h = 0; h < Hkv; ++h) {
+        if (head_group[h] != gi) continue;
+        int32_t c = n[b * Hkv + h];
+#if ORACLE_MUTANT == 10
+        if (c < mx) mx = c;
+#else
+        if (c > mx) mx = c;
+#endif
+      }
+#if ORACLE_MUTANT == 10
+      if (mx == 0x7fffffff) mx = 0;
+#endif
+#if ORACLE_MUTANT == 9
+      pages[gi * B + b] = mx / P;
+#else
+      pages[gi * B + b] = (mx + P - 1) / P;
+#endif
+    }
+  return 0;
+}
+
+int oracle_footprint_bytes(int B, int Hkv, const int32_t *n,
+                           const int32_t *head_group, int G, int P, int D,
+                           int dtype_bytes, int64_t *bytes) {
+  if (D <= 0 || dtype_bytes <= 0 || !bytes || G <= 0 || B < 0) return -1;
+  int32_t *pages = (int32_t *)malloc(sizeof(int32_t) * (size_t)(G * B + 1));
+  if (!pages) return -1;
+  if (oracle_group_pages(B, Hkv, n, head_group, G, P, pages) != 0) {
+    free(pages);
+    return -1;
+  }
+  for (int b = 0; b < B; ++b) {
+    int64_t tot = 0;
+    for (int gi = 0; gi < G; ++gi) {
+      int64_t size = 0;
+      for (int h = 0; h < Hkv; ++h) size += (head_group[h] == gi);
+      tot += (int64_t)pages[gi * B + b] * size * P * 2 * D * dtype_bytes;
+    }
+    bytes[b] = tot;
+  }
+  free(pages);
+  return 0;
+}
+
+int64_t oracle_plan_coverage(int nheads, const int32_t *n, int maxn,
+                             int nitems, const int32_t *items,
+                             int32_t *count) {
+  if (nheads < 0 || maxn < 0 || nitems < 0 || !n || !count ||
+      (nitems > 0 && !items))
+    return -1;
+  for (int bh = 0; bh < nheads; ++bh)
+    if (n[bh] < 0 || n[bh] > maxn) return -1;
+  memset(count, 0, sizeof(int32_t) * (size_t)nheads * (size_t)maxn);
+  int64_t bad = 0;
+  for (int i = 0; i < nitems; ++i) {
+    int32_t bh = items[4 * i + 0], b0 = items[4 * i + 1],
+            e0 = items[4 * i + 2];
+    if (bh < 0 || bh >= nheads || b0 < 0 || e0 <= b0 || e0 > maxn) {
+      ++bad;
+      continue;
+    }
+    for (int t = b0; t < e0; ++t) count[(size_t)bh * maxn + t] += 1;
+  }
+  for (int bh = 0; bh < nheads; ++bh)
+    for (int t = 0; t < maxn; ++t) {
+      int32_t c = count[(size_t)bh * maxn + t];
+#if ORACLE_MUTANT == 14
+      if (t < n[bh] && c != 1) ++bad;
+#else
+      if (t < n[bh] ? c != 1 : c != 0) ++bad;
+#endif
+    }
+  return bad;
+}
+
+/* KV-RM, Fig. 3: descriptor merging. A run continues while both the logical
+ * block index and the physical block id advance by one. */
+int64_t oracle_runs(int S, int max_blocks, const int32_t *bt,
+                    const int32_t *nb, int32_t *run_count, int32_t *runs) {
+  if (S < 0 || max_blocks < 0 || !bt || !nb || !run_count || !runs) return -1;
+  for (int s = 0; s < S; ++s)
+    if (nb[s] < 0 || nb[s] > max_blocks) return -1;
+  int64_t total = 0;
+  for (int s = 0; s < S; ++s) {
+    const int32_t *row = bt + (size_t)s * max_blocks;
+    int32_t *out = runs + (size_t)s * max_blocks * 3;
+    int r = -1;
+    for (int j = 0; j < nb[s]; ++j) {
+#if ORACLE_MUTANT == 11
+      int cont = (j > 0) && (row[j] == row[j - 1]);
+#else
+      int cont = (j > 0) && (row[j] == row[j - 1] + 1);
+#endif
+      if (!cont) {
+        ++r;
+        out[3 * r + 0] = row[j];
+        out[3 * r + 1] = j;
+        out[3 * r + 2] = 1;
+      } else {
+        out[3 * r + 2] += 1;
+      }
+    }
+    run_count[s] = r + 1;
+    total += r + 1;
+  }
+  return total;
+}
+
+/* KV-RM, abstract and Fig. 2: every live block of a sequence lands in its
+ * logical position of the fixed-shape staging row. */
+int oracle_gather(int S, int max_blocks, const int32_t *bt, const int32_t *nb,
+                  const uint8_t *pool, int64_t num_phys, int64_t block_bytes,
+                  uint8_t *staging, int64_t row_bytes, int zero_tail) {
+  if (S < 0 || max_blocks < 0 || !bt || !nb || !pool || !staging ||
+      num_phys <= 0 || block_bytes <= 0 || row_bytes < 0)
+    return -1;
+  for (int s = 0; s < S; ++s) {
+    if (nb[s] < 0 || nb[s] > max_blocks) return -1;
+    if ((int64_t)nb[s] * block_bytes > row_bytes) return -1;
+    for (int j = 0; j < nb[s]; ++j) {
+      int32_t p = bt[(size_t)s * max_blocks + j];
+      if (p < 0 || p >= num_phys) return -1;
+    }
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int s = 0; s < S; ++s) {
+    uint8_t *row = staging + (size_t)s * row_bytes;
+#if ORACLE_MUTANT == 13
+    int last = nb[s] + 1 <= max_blocks &&
+                       (int64_t)(nb[s] + 1) * block_bytes <= row_bytes
+                   ? nb[s] + 1
+                   : nb[s];
+#else
+    int last = nb[s];
+#endif
+    for (int j = 0; j < last; ++j) {
+      int32_t p = bt[(size_t)s * max_blocks + j];
+      if (p < 0 || p >= num_phys) continue;
+#if ORACLE_MUTANT == 12
+      int64_t dst = (int64_t)(p % (last > 0 ? last : 1)) * block_bytes;
+#else
+      int64_t dst = (int64_t)j * block_bytes;
+#endif
+      memcpy(row + dst, pool + (size_t)p * (size_t)block_bytes,
+             (size_t)block_bytes);
+    }
+    if (zero_tail) {
+      int64_t used = (int64_t)nb[s] * block_bytes;
+      memset(row + used, 0, (size_t)(row_bytes - used));
+    }
+  }
+  return 0;
+}

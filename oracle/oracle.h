@@ -1,0 +1,116 @@
+/*
+ * oracle.h -- plain, slow, obviously correct CPU reference for the
+ * non-uniform paged decode-attention path and the coalesced KV gather.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product (the kvx library and its
+ * Python binding) may include, link, load or call this code. Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg use it.
+ * It shares no source, header, table or helper with the CUDA path.
+ *
+ * All floating point is IEEE double. The oracle never sees pages, head groups
+ * or a work plan: attention is computed from dense, unpaged K/V plus the
+ * explicit set of token positions each head keeps, which is the definition
+ * the paged form must reproduce ("Tangram: Unlocking Non-Uniform KV Cache for
+ * Efficient Multi-turn LLM Serving", Fig. 2 caption: each head keeps its most
+ * critical tokens, which carry most of the attention output; abstract: the
+ * accuracy of the serving system is unchanged by its memory layout).
+ *
+ * Return codes: 0 on success, -1 on invalid arguments (nothing is written).
+ */
+#ifndef KV_ORACLE_H
+#define KV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Number of tokens head (b,h) keeps: n = min(seq_len[b], budget[b*Hkv+h]).
+ * A budget below 1 is invalid (a decode query always sees its own token).
+ * Tangram, abstract and Sec. "Deterministic Budget Allocation": every head
+ * has a static token budget. Writes n[B*Hkv]. */
+int oracle_resolve_budget(int B, int Hkv, const int32_t *budget,
+                          const int32_t *seq_len, int32_t *n);
+
+/* Softmax attention of the g query heads that share one KV head, over the
+ * n kept positions idx[0..n) (strictly increasing, each in [0, L)).
+ *   s_t = scale * <q_j, k_{idx_t}>,  w_t = exp(s_t - max s) / sum_u exp(s_u - max s),
+ *   out_j = sum_t w_t v_{idx_t}.
+ * q: [g][D]; k, v: [L][D] dense rows (rows outside idx are never read);
+ * out: [g][D]; w (optional, may be NULL): [g][n] softmax weights. */
+int oracle_attn_head(int D, int g, int L, const double *q, const double *k,
+                     const double *v, int n, const int32_t *idx, double scale,
+                     double *out, double *w);
+
+/* Decode attention for a whole batch. Query head j of sequence b reads KV
+ * head floor(j / (Hq/Hkv)) (contiguous grouped-query mapping).
+ * q: [B][Hq][D]; k, v: [B][Hkv][Lmax][D]; kept_off: [B*Hkv+1] offsets into
+ * kept_idx (positions of head (b,h) are kept_idx[kept_off[bh] .. kept_off[bh+1]));
+ * each kept position must be < seq_len[b] <= Lmax. out: [B][Hq][D].
+ * Parallel over (b, h) with OpenMP when available; every head is computed
+ * exactly as oracle_attn_head computes it. */
+int oracle_decode_attn(int B, int Hq, int Hkv, int D, int Lmax,
+                       const int32_t *seq_len, const double *q,
+                       const double *k, const double *v,
+                       const int64_t *kept_off, const int32_t *kept_idx,
+                       double scale, double *out);
+
+/* Pages each head group needs per sequence: the group's page table for
+ * sequence b holds ceil(max_{h in group} n[b*Hkv+h] / P) pages, because a
+ * group page has one slot row per head of the group and every head of the
+ * group advances through the same pages (Tangram, Fig. 8(b): each head group
+ * keeps its own page table). head_group[h] in [0, G). pages: [G][B]. */
+int oracle_group_pages(int B, int Hkv, const int32_t *n,
+                       const int32_t *head_group, int G, int P,
+                       int32_t *pages);
+
+/* Guaranteed KV footprint, in bytes, of sequence b for one layer: the sum
+ * over groups of pages * |group| * P * 2 (K and V) * D * dtype_bytes
+ * (Tangram, Fig. 7 caption: the footprint M(r) in terms of the head
+ * dimension and the data-type size; the printed formula is lost, this is the
+ * exact page count times page bytes). bytes: [B]. */
+int oracle_footprint_bytes(int B, int Hkv, const int32_t *n,
+                           const int32_t *head_group, int G, int P, int D,
+                           int dtype_bytes, int64_t *bytes);
+
+/* Token coverage of a work plan. items: [nitems][4] = {bh, tok_begin,
+ * tok_end, slot}. count: [nheads][maxn] is filled with the number of items
+ * that cover each token of each head. Returns the number of violations
+ * (a token of [0, n) covered other than exactly once, any token >= n
+ * covered, an empty or out-of-range item), or -1 on invalid arguments.
+ * Tangram, Fig. 13 and abstract: the ahead-of-time plan splits each head's
+ * kept tokens across thread blocks; splitting must not change what is read. */
+int64_t oracle_plan_coverage(int nheads, const int32_t *n, int maxn,
+                             int nitems, const int32_t *items,
+                             int32_t *count);
+
+/* Runs of a block table: maximal stretches of logically consecutive blocks
+ * j, j+1, ... of one sequence whose physical ids are p, p+1, ...
+ * ("KV-RM: Regularizing KV-Cache Movement for Static-Graph LLM Serving",
+ * Fig. 3: descriptor merging turns fragmented page descriptors into a few
+ * large transfers). bt: [S][max_blocks]; nb: [S].
+ * run_count: [S]; runs: [S][max_blocks][3] = {first physical block,
+ * first logical block, length in blocks}, in logical order.
+ * Returns the total number of runs, or -1. */
+int64_t oracle_runs(int S, int max_blocks, const int32_t *bt,
+                    const int32_t *nb, int32_t *run_count, int32_t *runs);
+
+/* Brute-force gather into a fixed-shape staging buffer (KV-RM, abstract and
+ * Fig. 2: non-contiguous mappings are materialised into the buffer a
+ * fixed-shape attention kernel reads). For every sequence s and logical
+ * block j < nb[s]: bytes [j*block_bytes, (j+1)*block_bytes) of staging row s
+ * are a copy of physical block bt[s][j] of pool. Bytes of a row past
+ * nb[s]*block_bytes are left as they are, or set to zero if zero_tail != 0.
+ * pool: [num_phys][block_bytes]; staging: [S][row_bytes]. */
+int oracle_gather(int S, int max_blocks, const int32_t *bt, const int32_t *nb,
+                  const uint8_t *pool, int64_t num_phys, int64_t block_bytes,
+                  uint8_t *staging, int64_t row_bytes, int zero_tail);
+
+/* Number of OpenMP threads the oracle uses (1 without OpenMP). */
+int oracle_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
