@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark of the kvx hot path on one GB300 (or N replicas under torchrun).
+
+One step = one decode step of the Qwen3-4B-shaped workload: for each of its 36
+layers, split decode attention over that layer's head-group paged KV cache
+(plus the log-sum-exp merge of split heads). The KV-RM gather (256 sequences,
+fragmented 40 GB pool, fixed-shape staging) is timed in its own loop and
+reported in the same line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0. `--impl reference` times the fp64 CPU oracle
+on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode-attn KV GB/s and % of GB300 HBM roofline; gather GB/s"
+FALLBACK_HBM = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_4b",
+                    choices=["qwen3_4b", "qwen3_4b_32k", "qwen25_32b", "llama3_sparse"])
+    ap.add_argument("--no-gather", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM, "fallback"
+
+
+def describe(cfg) -> str:
+    return (f"{cfg.name} decode: {cfg.layers} layers, batch {cfg.B}, {cfg.Hq} q / {cfg.Hkv} KV "
+            f"heads, head_dim {cfg.D}, {cfg.dtype}, page {cfg.P}, {cfg.num_groups} head groups, "
+            f"seq_len {int(cfg.seq_len.min())}..{int(cfg.seq_len.max())}, "
+            f"kept tokens/step {int(cfg.n.sum())}")
+
+
+# ------------------------------------------------------------ CPU oracle
+def host_sequences(cfg, table_seed=11):
+    """Yields, sequence by sequence and layer by layer, the oracle's inputs for
+    all KV heads of one sequence: (q [1][Hq][D], k, v [1][Hkv][nmax][D],
+    [nmax], kept sets, KV bytes), rebuilt on the host from the seeded value
+    table and page tables the GPU arm uses."""
+    from synth.device import page_tables_for, rows_in_group
+    table_rows = 1 << 19
+    vals = synth.bf16_bits_to_f32(synth.value_table(table_seed, table_rows * cfg.D, "bf16"))
+    vals = vals.reshape(table_rows, cfg.D)
+    gpf = host_group_pages(cfg)
+    for layer in range(cfg.layers):
+        tables, _ = page_tables_for(gpf(layer), 0 * 131 + layer, 0)
+        hg = cfg.head_group[layer]
+        rows, gsize = rows_in_group(hg), np.bincount(hg, minlength=cfg.num_groups)
+        gen = synth.rng(0 * 1009 + layer)
+        sh = gen.integers(0, table_rows, size=(cfg.num_groups, 2)).astype(np.int64)
+        q = synth.normal(gen, (cfg.B, cfg.Hq, cfg.D), cfg.dtype)
+        for b in range(cfg.B):
+            n = cfg.n[layer][b]
+            nmax = int(n.max())
+            k = np.zeros((1, cfg.Hkv, nmax, cfg.D))
+            v = np.zeros((1, cfg.Hkv, nmax, cfg.D))
+            for h in range(cfg.Hkv):
+                gi = int(hg[h])
+                t = np.arange(int(n[h]), dtype=np.int64)
+                ids = (tables[gi][b, t // cfg.P].astype(np.int64) * int(gsize[gi]) +
+                       int(rows[h])) * cfg.P + t % cfg.P
+                k[0, h, :n[h]] = vals[(sh[gi, 0] + ids) % table_rows]
+                v[0, h, :n[h]] = vals[(sh[gi, 1] + ids) % table_rows]
+            kept = [np.arange(int(n[h]), dtype=np.int32) for h in range(cfg.Hkv)]
+            qb = np.ascontiguousarray(q[b:b + 1], dtype=np.float64)
+            yield qb, k, v, np.array([nmax], np.int32), kept, int(n.sum()) * 2 * cfg.D * 2
+
+
+def oracle_sample(cfg, seconds):
+    """Times the fp64 oracle (OpenMP over the KV heads of one sequence per
+    call) on the workload's sequences in order until `seconds` of oracle time
+    have been spent. Returns (kv bytes, seconds, heads, threads)."""
+    import oracle
+    orc = oracle.load()
+    scale = 1.0 / math.sqrt(cfg.D)
+    spent, nbytes, heads = 0.0, 0, 0
+    for item in host_sequences(cfg):
+        t0 = time.perf_counter()
+        orc.decode_attn(*item[:5], scale)
+        spent += time.perf_counter() - t0
+        nbytes += item[5]
+        heads += cfg.Hkv
+        if spent >= seconds:
+            break
+    return nbytes, spent, heads, min(orc.num_threads(), cfg.Hkv)
+
+
+def cpu_baseline(cfg, seconds):
+    nbytes, secs, heads, cores = oracle_sample(cfg, seconds)
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} (sequence, KV head) pairs of {cfg.name}, from layer 0 on "
+                      f"({nbytes / 1e9:.3f} GB of bf16 KV, {secs:.1f} s of fp64 oracle time; "
+                      f"one sequence per call, OpenMP over its KV heads)"}
+
+
+def host_group_pages(cfg):
+    """Pages each group needs (for the oracle-only arm, computed like the
+    page tables the GPU arm builds: ceil of the group's longest head / P)."""
+    def fn(layer):
+        hg = cfg.head_group[layer]
+        gp = np.zeros((cfg.num_groups, cfg.B), dtype=np.int64)
+        for h in range(cfg.Hkv):
+            gp[hg[h]] = np.maximum(gp[hg[h]], (cfg.n[layer][:, h] + cfg.P - 1) // cfg.P)
+        return gp
+    return fn
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores: each step runs it over the
+    same bounded sample of the workload (the first sequences of layer 0),
+    sized so that warm-up plus timed steps take about a minute."""
+    import oracle
+    cfg = synth.decode_config(args.workload, seed=0)
+    if rank != 0:
+        return
+    orc = oracle.load()
+    total_steps = max(args.steps + args.warmup, 1)
+    target = max(0.02, 60.0 / total_steps)
+    sample = []  # (q, k, v, L, kept, bytes) per sequence
+    scale = 1.0 / math.sqrt(cfg.D)
+    spent, held = 0.0, 0
+    for item in host_sequences(cfg):
+        t0 = time.perf_counter()
+        orc.decode_attn(*item[:5], scale)
+        spent += time.perf_counter() - t0
+        sample.append(item)
+        held += item[1].nbytes + item[2].nbytes
+        if spent >= target or held >= (4 << 30):
+            break
+    secs = []
+    for i in range(total_steps):
+        t0 = time.perf_counter()
+        for it in sample:
+            orc.decode_attn(*it[:5], scale)
+        if i >= args.warmup:
+            secs.append(time.perf_counter() - t0)
+    nbytes = sum(it[5] for it in sample)
+    sec = sum(secs)
+    value = nbytes * len(secs) / sec / 1e9
+    cores = min(orc.num_threads(), cfg.Hkv)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sec / max(len(secs), 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(cfg)},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step: the fp64 oracle over the first {len(sample)} "
+                                       f"sequences of the step in layer order "
+                                       f"({nbytes / 1e9:.3f} GB of bf16 KV), "
+                                       f"OpenMP over each sequence's KV heads"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ clocks
+class Clocks:
+    def __init__(self):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+            dev = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0] or "0"
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", dev, f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world):
+    import torch
+    from paged_non_uniform_gb300 import build
+    build.build()
+    from paged_non_uniform_gb300 import kvx
+    from synth.device import TableLayer, ValueTable
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+
+    cfg = synth.decode_config(args.workload, seed=rank)  # each rank serves its own batch
+    table = ValueTable(seed=11 + rank, rows=1 << 19, D=cfg.D, dtype=cfg.dtype)
+    sms = kvx.kvx_device_sm_count()
+    plans, layers = [], []
+    plan_us = []
+    for l in range(cfg.layers):
+        p = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                                kvx.KVX_BF16, cfg.budget[l], cfg.seq_len, cfg.head_group[l], 0)
+        kvx.kvx_plan_upload(p)
+        plan_us.append(p.stats()["plan_us"])
+        plans.append(p)
+        layers.append(TableLayer(cfg, l, table, p.group_pages(), seed=0))
+    ws_bytes = max(p.workspace_bytes() for p in plans)
+    ws = torch.zeros(ws_bytes // 4 + 64, dtype=torch.int32, device=dev)
+    outs = torch.empty((cfg.layers, cfg.B, cfg.Hq, cfg.D), dtype=torch.float32, device=dev)
+    launches_per_step = sum(1 + (p.stats()["num_split_heads"] > 0) for p in plans)
+    bytes_layer = [cfg.kv_bytes_layer(l) for l in range(cfg.layers)]
+    bytes_step = sum(bytes_layer)
+
+    def call(l, q=None, out=None):
+        lay = layers[l]
+        kvx.kvx_decode_attn(plans[l], lay.q if q is None else q, lay.k_pools, lay.v_pools,
+                            lay.pool_pages, lay.pt, lay.strides, lay.budget, lay.seq_len, 0.0,
+                            outs[l] if out is None else out, ws, stream=stream)
+
+    def step():
+        for l in range(cfg.layers):
+            call(l)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == 0, "device status set during warm-up"
+
+    # ---- timed region: whole steps, per-call events for the roofline
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(cfg.layers + 1)]
+          for _ in range(args.steps)]
+    clocks = Clocks()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        for l in range(cfg.layers):
+            call(l)
+            ev[s][l + 1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    call_ms = [[ev[s][l].elapsed_time(ev[s][l + 1]) for l in range(cfg.layers)]
+               for s in range(args.steps)]
+    assert kvx.kvx_workspace_status(ws) == 0, "device status set during the timed region"
+    ms_step = ms_total / args.steps
+    if dist:
+        t = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+
+    # roofline of the attention call (split kernel + merge): algorithmic KV
+    # bytes of each layer over that call's event time, averaged over calls
+    mean_call_ms = float(np.mean(call_ms))
+    achieved = float(np.mean([bytes_layer[l] / (call_ms[s][l] * 1e-3)
+                              for s in range(args.steps) for l in range(cfg.layers)])) / 1e9
+    peak, peak_kind = peaks()
+
+    # ---- end to end through the public API with host buffers
+    g = cfg.Hq // cfg.Hkv
+    q_host = torch.empty((cfg.layers, cfg.B, cfg.Hq, cfg.D), dtype=torch.bfloat16,
+                         pin_memory=True)
+    for l in range(cfg.layers):
+        q_host[l].copy_(layers[l].q.cpu())
+    out_host = torch.empty((cfg.layers, cfg.B, cfg.Hq, cfg.D), dtype=torch.float32,
+                           pin_memory=True)
+    q_dev = torch.empty_like(q_host, device=dev)
+    e2e_steps = max(3, args.steps // 2)
+
+    def e2e_step():
+        q_dev.copy_(q_host, non_blocking=True)
+        for l in range(cfg.layers):
+            call(l, q=q_dev[l])
+        out_host.copy_(outs, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    h0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+
+    # ---- gather (KV-RM movement workload)
+    gather = None
+    if not args.no_gather:
+        del layers, plans
+        torch.cuda.empty_cache()
+        gather = bench_gather(args, dev, stream, peak, dist, world, rank)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(cfg, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 K/V, fragmented page tables)",
+            "config": {"workload": describe(cfg),
+                       "l2": "inputs larger than L2: each step streams "
+                             f"{bytes_step / 1e9:.1f} GB of distinct KV pages",
+                       "plan": "balanced ahead-of-time split, one persistent block per SM",
+                       "sms": sms},
+            "frac_of_hbm": value / world / peak,
+            "seq_heads_per_s": world * cfg.B * cfg.Hq * cfg.layers / (ms_step * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "attn_mma_kernel<128> + combine_kernel (one decode call)",
+                         "peak_source": f"{peak_kind} hbm_gbs", "mean_call_us": 1e3 * mean_call_ms},
+            "e2e": {"value": e2e_value, "unit": "GB/s",
+                    "h2d_bytes_per_step": int(q_host.numel() * 2),
+                    "d2h_bytes_per_step": int(out_host.numel() * 4)},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "plan_host_us_per_layer": float(np.mean(plan_us)),
+            "gather": gather,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_gather(args, dev, stream, peak, dist, world, rank):
+    import torch
+    from paged_non_uniform_gb300 import kvx
+    from synth.device import ValueTable
+    cfg = synth.gather_config(seed=rank)
+    table = ValueTable(seed=21 + rank, rows=1 << 18, D=128, dtype="bf16")
+    pools, stagings = [], []
+    for t in range(2):
+        p = torch.empty((cfg.num_phys, cfg.block_bytes // 2), dtype=torch.bfloat16, device=dev)
+        table.fill(p, 1000 * t + 7)
+        pools.append(p)
+        stagings.append(torch.zeros((cfg.S, cfg.row_bytes // 2), dtype=torch.bfloat16,
+                                    device=dev))
+    bt = torch.from_numpy(cfg.bt).to(dev)
+    nb = torch.from_numpy(cfg.nb).to(dev)
+    ws = torch.zeros(kvx.kvx_gather_workspace_bytes(cfg.S, cfg.max_blocks) // 4 + 64,
+                     dtype=torch.int32, device=dev)
+
+    def call():
+        kvx.kvx_gather_coalesce(bt, nb, cfg.S, cfg.max_blocks, pools, cfg.num_phys,
+                                cfg.block_bytes, stagings, cfg.row_bytes, 0, ws, stream=stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    steps = max(5, args.steps // 2)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    a.record(stream)
+    for _ in range(steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert kvx.kvx_workspace_status(ws) == 0
+    live = 2 * cfg.live_bytes()  # K and V
+    moved = 2 * live             # read + write
+    return {"workload": f"KV-RM movement: {cfg.S} seqs, {int(cfg.seq_tokens.min())}.."
+                        f"{int(cfg.seq_tokens.max())} tokens, 32 KB blocks (16 tok x 8 heads x 128 "
+                        f"bf16), K+V pools {2 * cfg.num_phys * cfg.block_bytes / 2**30:.0f} GiB "
+                        f"randomly permuted, staging [{cfg.S}][16384] per tensor",
+            "value": world * moved / (ms * 1e-3) / 1e9, "unit": "GB/s (read+write)",
+            "payload_gbs": world * live / (ms * 1e-3) / 1e9, "ms_per_call": ms,
+            "frac": moved / (ms * 1e-3) / 1e9 / peak, "launches_per_call": 4}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,283 @@
+/*
+ * kvx.h -- C ABI of the kvx library: decode-step attention over a paged KV
+ * cache with non-uniform per-head budgets, and the coalesced KV gather.
+ *
+ * Sources of the operations:
+ *  - "Tangram: Unlocking Non-Uniform KV Cache for Efficient Multi-turn LLM
+ *    Serving": static per-head budgets (Deterministic Budget Allocation),
+ *    head-group page tables (Head Group Page, Fig. 8), and a work split
+ *    computed ahead of time from the static budgets (AOT Load Balancing,
+ *    Figs. 4(c), 5 and 13).
+ *  - "KV-RM: Regularizing KV-Cache Movement for Static-Graph LLM Serving":
+ *    descriptor merging of fragmented block mappings into a few large
+ *    transfers that fill a fixed-shape staging buffer (Figs. 2 and 3).
+ *
+ * Conventions for every entry point:
+ *  - Every function returns an int status: KVX_OK (0) or a negative code
+ *    (kvx_status_string() names it). Nothing throws across the ABI.
+ *  - The caller owns all device memory (inputs, outputs, workspaces) and all
+ *    host arrays passed in. The library owns only the opaque plan (host
+ *    arrays plus a device copy made by kvx_plan_upload), freed by
+ *    kvx_plan_destroy.
+ *  - Device calls are asynchronous on the stream passed as `void *stream`
+ *    (a cudaStream_t; NULL = the legacy default stream). They never
+ *    synchronise and never allocate device memory. Argument errors are
+ *    found on the host, before anything is launched.
+ *  - Errors found on the device (a page id outside its pool, a budget that
+ *    disagrees with the plan, a block id outside the pool, a wait that ran
+ *    out) set bits in a status word at the start of the caller's workspace
+ *    (KVX_DEV_* below); the affected reads are replaced by zeros and the
+ *    kernel still terminates. The word is sticky: kvx_workspace_status reads
+ *    it, kvx_workspace_clear resets it. A fresh workspace must be cleared
+ *    (or zero-filled) once before first use.
+ *  - All layouts are dense row-major C arrays, outermost index first.
+ */
+#ifndef KVX_H
+#define KVX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define KVX_OK 0
+#define KVX_EINVAL (-1)       /* a null pointer, bad size or inconsistent argument */
+#define KVX_ERANGE (-2)       /* an index or length outside its declared range */
+#define KVX_ENOMEM (-3)       /* host allocation failed */
+#define KVX_ECUDA (-4)        /* a CUDA runtime call failed; see kvx_last_cuda_error */
+#define KVX_EUNSUPPORTED (-5) /* head_dim / page size / dtype / GQA combination */
+#define KVX_ESTATE (-6)       /* plan used before kvx_plan_upload */
+
+/* ---- device status bits (workspace status word) ---------------------- */
+#define KVX_DEV_BAD_PAGE 1u    /* a page-table entry outside [0, pool_pages) */
+#define KVX_DEV_BAD_BUDGET 2u  /* min(seq_len, head_budget) differs from the plan */
+#define KVX_DEV_TIMEOUT 4u     /* a pipeline wait gave up after its time limit */
+#define KVX_DEV_BAD_BLOCK 8u   /* a block-table entry outside [0, num_phys_blocks) */
+#define KVX_DEV_BAD_LENGTH 16u /* num_blocks[s] outside [0, max_blocks] or the row */
+
+/* ---- element types --------------------------------------------------- */
+#define KVX_F32 0
+#define KVX_BF16 1
+
+/* ---- work-split policies (kvx_plan_create) ---------------------------- */
+/* Ahead-of-time balanced split (Tangram, AOT Load Balancing): the kept tokens
+ * of all heads are laid end to end and cut into num_ctas spans of equal cost;
+ * a head cut across spans is split into partials merged by log-sum-exp. */
+#define KVX_PLAN_BALANCED 0
+/* One thread block per (sequence, KV head); no split (naive baseline). */
+#define KVX_PLAN_PER_HEAD 1
+/* Every head split into the same number of equal pieces, sized so the grid
+ * covers the GPU twice; one block per piece (the uniform split of Tangram
+ * Fig. 4(c), whose stragglers the balanced plan removes). */
+#define KVX_PLAN_UNIFORM 2
+
+/* ---- kernel choice ----------------------------------------------------- */
+#define KVX_KERNEL_AUTO 0 /* tensor-core kernel for bf16, CUDA-core kernel for fp32 */
+#define KVX_KERNEL_MMA 1  /* bf16 only: bulk-tensor loads + warp-level MMA */
+#define KVX_KERNEL_SIMT 2 /* CUDA-core kernel, fp32 or bf16 */
+
+/* ---- gather flags ------------------------------------------------------ */
+#define KVX_ZERO_TAIL 1 /* zero each staging row past its live blocks */
+
+/* ---- limits ------------------------------------------------------------ */
+#define KVX_MAX_GROUPS 16
+#define KVX_MAX_KV_HEADS 64
+#define KVX_MAX_GQA 8
+#define KVX_MAX_GATHER_TENSORS 4
+#define KVX_WS_HEADER_BYTES 256
+
+typedef struct kvx_shape {
+  int32_t B;          /* sequences in the batch */
+  int32_t Hq;         /* query heads; Hq = g * Hkv, 1 <= g <= KVX_MAX_GQA */
+  int32_t Hkv;        /* KV heads, <= KVX_MAX_KV_HEADS */
+  int32_t D;          /* head dimension: 64 or 128 */
+  int32_t page_size;  /* P, tokens per page: 8, 16, 32, 64 or 128 */
+  int32_t num_groups; /* head groups, <= KVX_MAX_GROUPS */
+  int32_t dtype;      /* KVX_F32 or KVX_BF16 (q, K and V share it) */
+} kvx_shape;
+
+typedef struct kvx_plan kvx_plan;
+
+typedef struct kvx_plan_stats {
+  int32_t num_ctas;          /* thread blocks the attention kernel launches */
+  int32_t num_items;         /* work items (head, token range) */
+  int32_t num_slots;         /* partial results written for split heads */
+  int32_t num_split_heads;   /* heads cut into more than one item */
+  int32_t kernel;            /* KVX_KERNEL_MMA or KVX_KERNEL_SIMT (resolved) */
+  int32_t policy;            /* KVX_PLAN_* */
+  int64_t total_tokens;      /* sum of kept tokens over all heads */
+  int64_t max_cta_tokens;    /* largest token load of one thread block */
+  double mean_cta_tokens;    /* mean token load per thread block */
+  int64_t slots_allocated;   /* token slots in allocated group pages (all heads) */
+  int64_t slots_used;        /* token slots holding kept tokens (= total_tokens) */
+  double plan_us;            /* host time spent building the plan */
+} kvx_plan_stats;
+
+/* Text for a status code. Never NULL. */
+const char *kvx_status_string(int status);
+
+/* The cudaError_t of the last failed CUDA call in this thread (0 if none). */
+int kvx_last_cuda_error(void);
+
+/* Streaming multiprocessors of the current device (queries the driver). */
+int kvx_device_sm_count(int32_t *sms);
+
+/* ---------------------------------------------------------------------------
+ * kvx_plan_create -- host only, no device work.
+ *
+ * Resolves the kept-token count of every head (Tangram, Deterministic Budget
+ * Allocation: a static budget per head):
+ *     n[b][h] = min(seq_len[b], head_budget[b*Hkv + h]),  head_budget >= 1,
+ * groups the KV heads (Tangram, Fig. 8: heads with similar budgets share one
+ * head-group page table) and builds the ahead-of-time work split.
+ *
+ *   shape        problem shape (host).
+ *   head_budget  int32 [B*Hkv], tokens each (sequence, KV head) keeps (host).
+ *   seq_len      int32 [B], tokens in each sequence, >= 1 (host).
+ *   head_group   int32 [Hkv], group of each KV head, in [0, num_groups); every
+ *                group non-empty (host). Within a group, heads take page-slot
+ *                rows 0, 1, ... in ascending head order.
+ *   num_ctas     thread blocks for KVX_PLAN_BALANCED; 0 = one per SM of the
+ *                current device (ignored by the other policies).
+ *   policy       KVX_PLAN_*.   kernel  KVX_KERNEL_*.
+ *   out          receives the plan (owned by the caller; kvx_plan_destroy).
+ * Errors: KVX_EINVAL, KVX_EUNSUPPORTED, KVX_ENOMEM; *out is NULL on error.
+ * ------------------------------------------------------------------------- */
+int kvx_plan_create(const kvx_shape *shape, const int32_t *head_budget,
+                    const int32_t *seq_len, const int32_t *head_group,
+                    int32_t num_ctas, int32_t policy, int32_t kernel,
+                    kvx_plan **out);
+
+/* Copies the plan's work list to the device (allocates plan-owned device
+ * memory; call once, outside any hot loop). Stream-ordered on `stream`. */
+int kvx_plan_upload(kvx_plan *plan, void *stream);
+
+/* Bytes of device workspace kvx_decode_attn needs with this plan:
+ * a KVX_WS_HEADER_BYTES header (status word) plus the split partials. */
+int kvx_plan_workspace_bytes(const kvx_plan *plan, size_t *bytes);
+
+int kvx_plan_get_stats(const kvx_plan *plan, kvx_plan_stats *stats);
+
+/* Kept-token counts n, int32 [B*Hkv] (host). */
+int kvx_plan_kept(const kvx_plan *plan, int32_t *n);
+
+/* Pages each head group needs per sequence: int32 [num_groups][B] (host),
+ * pages[g][b] = ceil(max_{h in g} n[b][h] / P). A group's page table row for
+ * sequence b must hold at least that many valid page ids. */
+int kvx_plan_group_pages(const kvx_plan *plan, int32_t *pages);
+
+/* The work list (host copies): items int32 [num_items][4] =
+ * {b*Hkv + h, first token, end token, partial slot or -1}, and cta_off
+ * int32 [num_ctas + 1]: thread block c runs items cta_off[c] .. cta_off[c+1]-1.
+ * Token t of head (b,h) is the head's t-th kept token in ascending position. */
+int kvx_plan_items(const kvx_plan *plan, int32_t *items, int32_t *cta_off);
+
+/* Per-block token loads, int64 [num_ctas] (host). */
+int kvx_plan_cta_tokens(const kvx_plan *plan, int64_t *tokens);
+
+/* Optional per-block timing trace: dev_trace is a device buffer of int64
+ * [num_ctas][4] = {SM id, start ns, end ns, tokens}, written by every
+ * subsequent kvx_decode_attn with this plan; NULL turns it off. */
+int kvx_plan_set_trace(kvx_plan *plan, int64_t *dev_trace);
+
+void kvx_plan_destroy(kvx_plan *plan);
+
+/* ---------------------------------------------------------------------------
+ * kvx_decode_attn -- one decode step of attention for one layer.
+ *
+ * For sequence b, query head j, KV head h = floor(j / g) (g = Hq / Hkv), over
+ * the n[b][h] kept tokens t of head h:
+ *     s_t = scale * <q[b][j], k_t>,   out[b][j] = sum_t softmax(s)_t * v_t.
+ * (Tangram, Fig. 2: attention over each head's kept tokens; the split-K
+ * partials of a cut head are merged by log-sum-exp, which leaves the result
+ * unchanged up to rounding.)
+ *
+ * Head-group page addressing (Tangram, Fig. 8(b)): head h belongs to group
+ * G = head_group[h] and has row r = its rank within G. Its t-th kept token is
+ * in physical page p = page_tables[G][b * page_table_stride[G] + t / P],
+ * at k_pools[G] + ((p * |G| + r) * P + t % P) * D elements (same for V).
+ *
+ *   plan              an uploaded plan built for these shapes and budgets.
+ *   q                 [B][Hq][D] of the plan's dtype (device).
+ *   k_pools, v_pools  host arrays [num_groups] of device pointers, each a
+ *                     pool [pool_pages[G]][|G|][P][D] of the plan's dtype,
+ *                     16-byte aligned.
+ *   pool_pages        host int64 [num_groups], pages in each pool.
+ *   page_tables       host array [num_groups] of device int32 pointers, each
+ *                     [B][page_table_stride[G]].
+ *   page_table_stride host int32 [num_groups]; must be >= the pages the plan
+ *                     says the group needs (kvx_plan_group_pages).
+ *   head_budget       device int32 [B*Hkv]; seq_len device int32 [B]: checked
+ *                     on the device against the plan (KVX_DEV_BAD_BUDGET).
+ *   scale             score scale; 0 means 1/sqrt(D).
+ *   out               device fp32 [B][Hq][D].
+ *   workspace         device, >= kvx_plan_workspace_bytes, 256-byte aligned.
+ * Padding slots of partly filled pages are never read into the result.
+ * Errors: KVX_EINVAL, KVX_ERANGE, KVX_ESTATE, KVX_ECUDA (nothing launched on
+ * argument errors).
+ * ------------------------------------------------------------------------- */
+int kvx_decode_attn(const kvx_plan *plan, const void *q,
+                    const void *const *k_pools, const void *const *v_pools,
+                    const int64_t *pool_pages,
+                    const int32_t *const *page_tables,
+                    const int32_t *page_table_stride,
+                    const int32_t *head_budget, const int32_t *seq_len,
+                    float scale, float *out, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/* Reads the workspace status word (synchronous device-to-host copy). */
+int kvx_workspace_status(const void *workspace, uint32_t *status);
+
+/* Zeroes the workspace status word (stream-ordered). */
+int kvx_workspace_clear(void *workspace, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * kvx_gather_coalesce -- KV-RM movement step.
+ *
+ * (1) Descriptor merging (KV-RM, Fig. 3): the block table of each sequence is
+ *     cut into runs, maximal stretches of logically consecutive blocks whose
+ *     physical ids are consecutive; the runs are written to the workspace.
+ * (2) Coalesced gather (KV-RM, abstract and Fig. 2): every run is copied as
+ *     one contiguous transfer into the fixed-shape staging buffer, so that
+ *     for s < S, j < num_blocks[s]:
+ *         staging_t[s*row_bytes + j*block_bytes ...+block_bytes]
+ *           = pools_t[block_table[s*max_blocks + j] * block_bytes ...]
+ *     for every tensor t < num_tensors (e.g. K and V). Staging bytes of a row
+ *     past num_blocks[s]*block_bytes are left untouched, or zeroed with
+ *     KVX_ZERO_TAIL.
+ *
+ *   block_table   device int32 [S][max_blocks]; entries past num_blocks[s]
+ *                 are ignored.
+ *   num_blocks    device int32 [S], each in [0, max_blocks] with
+ *                 num_blocks[s]*block_bytes <= row_bytes (else the row is
+ *                 skipped and KVX_DEV_BAD_LENGTH is set).
+ *   pools         host array [num_tensors] of device pointers, each
+ *                 [num_phys_blocks][block_bytes] bytes, 16-byte aligned.
+ *   stagings      host array [num_tensors] of device pointers, each
+ *                 [S][staging_row_bytes] bytes, 16-byte aligned.
+ *   block_bytes, staging_row_bytes  multiples of 16.
+ *   workspace     device, >= kvx_gather_workspace_bytes(S, max_blocks).
+ * Blocks with an id outside the pool are not copied (KVX_DEV_BAD_BLOCK).
+ * ------------------------------------------------------------------------- */
+int kvx_gather_workspace_bytes(int32_t S, int32_t max_blocks, size_t *bytes);
+
+int kvx_gather_coalesce(const int32_t *block_table, const int32_t *num_blocks,
+                        int32_t S, int32_t max_blocks, int32_t num_tensors,
+                        const void *const *pools, int64_t num_phys_blocks,
+                        int64_t block_bytes, void *const *stagings,
+                        int64_t staging_row_bytes, int32_t flags,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Reads the runs of the last kvx_gather_coalesce on this workspace
+ * (synchronous): run_count int32 [S]; runs int32 [S][max_blocks][3] =
+ * {first physical block, first logical block, length in blocks}. */
+int kvx_gather_read_runs(const void *workspace, int32_t S, int32_t max_blocks,
+                         int32_t *run_count, int32_t *runs);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVX_H */

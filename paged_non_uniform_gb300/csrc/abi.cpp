@@ -1,0 +1,276 @@
+// abi.cpp -- the C ABI entry points of kvx that launch device work:
+// argument validation (everything is checked before anything is launched),
+// bulk-tensor map encoding, kernel launches and workspace helpers.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kvx_internal.h"
+
+namespace kvx {
+
+static thread_local int g_last_cuda_error = 0;
+
+int set_cuda_error(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return KVX_ECUDA;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t,
+                                  void *, const cuuint64_t *, const cuuint64_t *,
+                                  const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)f;
+  });
+  return fn;
+}
+
+// A 2-D bf16 tensor map over a pool viewed as [rows][D], box = 64 elements
+// (128 bytes, the swizzle span) x box_rows rows, 128-byte swizzle, zero fill
+// out of bounds.
+static bool encode_pool_map(CUtensorMap *tm, const void *base, int64_t rows,
+                            int D, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace kvx
+
+using namespace kvx;
+
+extern "C" const char *kvx_status_string(int s) {
+  switch (s) {
+    case KVX_OK: return "ok";
+    case KVX_EINVAL: return "invalid argument";
+    case KVX_ERANGE: return "index or length out of range";
+    case KVX_ENOMEM: return "out of host memory";
+    case KVX_ECUDA: return "CUDA runtime error";
+    case KVX_EUNSUPPORTED: return "unsupported shape, page size, dtype or GQA factor";
+    case KVX_ESTATE: return "plan not uploaded";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int kvx_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
+                               const void *const *k_pools,
+                               const void *const *v_pools,
+                               const int64_t *pool_pages,
+                               const int32_t *const *page_tables,
+                               const int32_t *page_table_stride,
+                               const int32_t *head_budget,
+                               const int32_t *seq_len, float scale, float *out,
+                               void *workspace, size_t workspace_bytes,
+                               void *stream) {
+  if (!plan || !q || !k_pools || !v_pools || !pool_pages || !page_tables ||
+      !page_table_stride || !head_budget || !seq_len || !out || !workspace)
+    return KVX_EINVAL;
+  if (!plan->d_buf) return KVX_ESTATE;
+  const kvx_shape &s = plan->shape;
+  const int G = s.num_groups, B = s.B, P = s.page_size, D = s.D;
+  size_t need = 0;
+  kvx_plan_workspace_bytes(plan, &need);
+  if (workspace_bytes < need || !aligned(workspace, 256)) return KVX_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.f) return KVX_EINVAL;
+  const size_t es = s.dtype == KVX_BF16 ? 2 : 4;
+  if (!aligned(q, 4) || !aligned(out, 16)) return KVX_EINVAL;
+
+  AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int gi = 0; gi < G; ++gi) {
+    if (!k_pools[gi] || !v_pools[gi] || !page_tables[gi]) return KVX_EINVAL;
+    if (!aligned(k_pools[gi], 16) || !aligned(v_pools[gi], 16)) return KVX_EINVAL;
+    if (pool_pages[gi] < 1) return KVX_EINVAL;
+    const int64_t rows = pool_pages[gi] * plan->group_size[gi] * (int64_t)P;
+    if (rows >= ((int64_t)1 << 31) - 128) return KVX_ERANGE;
+    int32_t mx = 0;
+    for (int b = 0; b < B; ++b) mx = std::max(mx, plan->group_pages[(size_t)gi * B + b]);
+    if (page_table_stride[gi] < std::max(mx, 1)) return KVX_ERANGE;
+    GroupDesc &gd = p.grp[gi];
+    gd.page_table = page_tables[gi];
+    gd.k_pool = k_pools[gi];
+    gd.v_pool = v_pools[gi];
+    gd.num_pages = pool_pages[gi];
+    gd.stride = page_table_stride[gi];
+    gd.size = plan->group_size[gi];
+    if (plan->kernel == KVX_KERNEL_MMA) {
+      const int box = std::min(P, kStageTokens);
+      if (!encode_pool_map(&p.tmK[gi], k_pools[gi], rows, D, box) ||
+          !encode_pool_map(&p.tmV[gi], v_pools[gi], rows, D, box))
+        return set_cuda_error(cudaErrorInvalidValue);
+    }
+  }
+  (void)es;
+  for (int h = 0; h < s.Hkv; ++h) {
+    p.head_grp[h] = (int8_t)plan->head_group[h];
+    p.head_row[h] = (int8_t)plan->head_row[h];
+  }
+  const int g = s.Hq / s.Hkv;
+  char *ws = (char *)workspace;
+  const size_t ml_bytes =
+      ((size_t)plan->num_slots * g * sizeof(float2) + 255) & ~size_t(255);
+  p.items = plan->d_items;
+  p.cta_off = plan->d_cta_off;
+  p.n_plan = plan->d_n;
+  p.head_budget = head_budget;
+  p.seq_len = seq_len;
+  p.q = q;
+  p.out = out;
+  p.status = (uint32_t *)ws;
+  p.part_ml = (float2 *)(ws + KVX_WS_HEADER_BYTES);
+  p.part_o = (float *)(ws + KVX_WS_HEADER_BYTES + ml_bytes);
+  p.trace = plan->d_trace;
+  p.B = B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.D = D;
+  p.g = g;
+  p.P = P;
+  const float sc = scale == 0.f ? 1.0f / std::sqrt((float)D) : scale;
+  p.scale_log2 = (float)((double)sc * 1.4426950408889634);
+
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = plan->kernel == KVX_KERNEL_MMA
+                      ? launch_attn_mma(p, plan->num_ctas, st)
+                      : launch_attn_simt(p, s.dtype, plan->num_ctas, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (!plan->split_heads.empty()) {
+    CombineParams cp;
+    cp.heads = plan->d_split;
+    cp.part_o = p.part_o;
+    cp.part_ml = p.part_ml;
+    cp.out = out;
+    cp.num_heads = (int32_t)plan->split_heads.size();
+    cp.Hkv = s.Hkv;
+    cp.Hq = s.Hq;
+    cp.g = g;
+    cp.D = D;
+    e = launch_combine(cp, st);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  return KVX_OK;
+}
+
+extern "C" int kvx_workspace_status(const void *workspace, uint32_t *status) {
+  if (!workspace || !status) return KVX_EINVAL;
+  cudaError_t e = cudaMemcpy(status, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return KVX_OK;
+}
+
+extern "C" int kvx_workspace_clear(void *workspace, void *stream) {
+  if (!workspace) return KVX_EINVAL;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, KVX_WS_HEADER_BYTES, (cudaStream_t)stream);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return KVX_OK;
+}
+
+extern "C" int kvx_gather_workspace_bytes(int32_t S, int32_t max_blocks, size_t *bytes) {
+  if (!bytes || S < 0 || max_blocks < 0) return KVX_EINVAL;
+  *bytes = gather_ws_layout(S, max_blocks).total;
+  return KVX_OK;
+}
+
+extern "C" int kvx_gather_coalesce(const int32_t *block_table,
+                                   const int32_t *num_blocks, int32_t S,
+                                   int32_t max_blocks, int32_t num_tensors,
+                                   const void *const *pools,
+                                   int64_t num_phys_blocks, int64_t block_bytes,
+                                   void *const *stagings,
+                                   int64_t staging_row_bytes, int32_t flags,
+                                   void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+  if (!block_table || !num_blocks || !pools || !stagings || !workspace) return KVX_EINVAL;
+  if (S < 0 || max_blocks < 0 || num_tensors < 1 || num_tensors > KVX_MAX_GATHER_TENSORS)
+    return KVX_EINVAL;
+  if (num_phys_blocks < 1 || block_bytes < 16 || block_bytes % 16 != 0 ||
+      staging_row_bytes < 0 || staging_row_bytes % 16 != 0)
+    return KVX_EINVAL;
+  if (flags & ~KVX_ZERO_TAIL) return KVX_EINVAL;
+  const GatherWs w = gather_ws_layout(S, max_blocks);
+  if (workspace_bytes < w.total || !aligned(workspace, 256)) return KVX_EINVAL;
+  GatherParams p;
+  std::memset(&p, 0, sizeof(p));
+  for (int t = 0; t < num_tensors; ++t) {
+    if (!pools[t] || !stagings[t] || !aligned(pools[t], 16) || !aligned(stagings[t], 16))
+      return KVX_EINVAL;
+    p.pools[t] = pools[t];
+    p.stagings[t] = stagings[t];
+  }
+  char *ws = (char *)workspace;
+  p.block_table = block_table;
+  p.num_blocks = num_blocks;
+  p.status = (uint32_t *)ws;
+  p.totals = (int64_t *)(ws + 16);
+  p.run_count = (int32_t *)(ws + w.run_count);
+  p.row_blocks = (int32_t *)(ws + w.row_blocks);
+  p.run_off = (int32_t *)(ws + w.run_off);
+  p.row_bstart = (int64_t *)(ws + w.row_bstart);
+  p.runs = (int4 *)(ws + w.runs);
+  p.run_bstart = (int64_t *)(ws + w.run_bstart);
+  p.num_phys = num_phys_blocks;
+  p.block_bytes = block_bytes;
+  p.row_bytes = staging_row_bytes;
+  p.S = S;
+  p.max_blocks = max_blocks;
+  p.num_tensors = num_tensors;
+  p.flags = flags;
+  cudaError_t e = launch_gather(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return KVX_OK;
+}
+
+extern "C" int kvx_gather_read_runs(const void *workspace, int32_t S,
+                                    int32_t max_blocks, int32_t *run_count,
+                                    int32_t *runs) {
+  if (!workspace || !run_count || !runs || S < 0 || max_blocks < 0) return KVX_EINVAL;
+  const GatherWs w = gather_ws_layout(S, max_blocks);
+  const char *ws = (const char *)workspace;
+  std::vector<int32_t> off((size_t)S + 1);
+  cudaError_t e = cudaMemcpy(run_count, ws + w.run_count, 4 * (size_t)S, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(off.data(), ws + w.run_off, 4 * ((size_t)S + 1), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  const int64_t total = off[S];
+  std::vector<int4> all((size_t)std::max<int64_t>(total, 1));
+  if (total > 0) {
+    e = cudaMemcpy(all.data(), ws + w.runs, 16 * (size_t)total, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  std::memset(runs, 0, sizeof(int32_t) * 3 * (size_t)S * (size_t)max_blocks);
+  for (int s = 0; s < S; ++s) {
+    for (int r = 0; r < run_count[s]; ++r) {
+      const int4 &d = all[(size_t)off[s] + r];
+      int32_t *o = runs + ((size_t)s * max_blocks + r) * 3;
+      o[0] = d.x;
+      o[1] = d.z;
+      o[2] = d.w;
+    }
+  }
+  return KVX_OK;
+}

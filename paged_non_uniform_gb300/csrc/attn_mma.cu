@@ -1,0 +1,403 @@
+// attn_mma.cu -- split decode attention over head-group pages, bf16 K/V,
+// tensor-core (warp MMA) path for sm_103a.
+//
+// Computes, for every work item {head (b,h), kept tokens [begin,end)} of the
+// ahead-of-time plan ("Tangram: Unlocking Non-Uniform KV Cache for Efficient
+// Multi-turn LLM Serving", AOT Load Balancing, Fig. 13), the softmax
+// attention of the g query heads of KV head h over those tokens, either as
+// the final output (item covers the head) or as a log-sum-exp partial
+// (max, sum, un-normalised output) merged later by the combine kernel.
+//
+// Data path, per thread block (one per SM, persistent over its items):
+//  * one producer warp walks the items' pages through the head group's page
+//    table (Fig. 8(b)) and issues bulk-tensor loads of each page slot's K and
+//    V rows (token-major, 128-byte swizzled, two 64-element halves of a row)
+//    into a ring of 32-token stages, completing on per-stage mbarriers;
+//  * kCons consumer warps take the stages round-robin. Per stage a warp
+//    computes S^T = K Q^T on m16n8k16 bf16 MMAs (16 tokens x 8 query columns;
+//    GQA query heads of one KV head are the columns), runs the online softmax
+//    on the accumulator fragments (column max by three shuffles), transposes
+//    P into the B operand with movmatrix, and accumulates O^T += V^T P^T with
+//    V^T fragments read by ldmatrix.trans. P is split into a bf16 high part
+//    and a bf16 residual, so the product keeps ~16 bits of P;
+//  * at the end of an item the consumer warps merge their (m, l, O) in shared
+//    memory and write the output or the partial.
+// No spin-wait is unbounded: every mbarrier wait gives up after kWaitNs and
+// sets KVX_DEV_TIMEOUT. Pages outside the pool are loaded as zeros (the box
+// is placed past the tensor's end) and set KVX_DEV_BAD_PAGE.
+#include <math.h>
+
+#include "kvx_internal.h"
+#include "ptx.cuh"
+
+namespace kvx {
+namespace {
+
+constexpr int kCons = 4;       // consumer warps
+constexpr int kStages = 10;    // ring depth (32-token stages)
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTile = kHalves * kStageTokens * 128;  // K (or V) bytes/stage
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kMS = D + 4;                   // merge row stride (floats)
+  static constexpr int kMW = 8 * kMS + 16;            // floats per warp record
+  static constexpr int kSmem =
+      1024 + kStages * kStage + 2 * kCons * kMW * 4 + 2 * kStages * 8 + 16;
+};
+
+// Byte offset, inside a stage's K or V tile, of 16-byte chunk `gc` (0..D/8-1)
+// of token row `tok` (0..31): halves are [32 tokens][128 B] blocks and the
+// chunk index is XOR-swizzled with the token's low 3 bits (128B swizzle).
+__device__ __forceinline__ uint32_t tile_off(int tok, int gc) {
+  return (uint32_t)((gc >> 3) * (kStageTokens * 128) + tok * 128 +
+                    (((gc & 7) ^ (tok & 7)) << 4));
+}
+
+template <int D>
+__device__ __forceinline__ void consume_stage(
+    uint32_t kbase, uint32_t vbase, int valid, const uint32_t (&qf)[D / 16][2],
+    float (&o)[D / 16][4], float &m0, float &m1, float &l0, float &l1,
+    float sl2, int lane) {
+  constexpr int NK = D / 16;
+  const int r = lane >> 2, c = lane & 3, mi = lane >> 3, lr = lane & 7;
+  float s[2][4];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+    const int tok = mt * 16 + (mi & 1) * 8 + lr;
+#pragma unroll
+    for (int j = 0; j < NK; ++j) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kbase + tile_off(tok, 2 * j + (mi >> 1)), a0, a1, a2, a3);
+      mma_bf16(s[mt], a0, a1, a2, a3, qf[j][0], qf[j][1]);
+    }
+  }
+  // s[mt][e]: token mt*16 + r (+8 for e >= 2), query column 2c + (e & 1).
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float x = s[mt][e] * sl2;
+      const int tok = mt * 16 + r + ((e >> 1) << 3);
+      x = tok < valid ? x : -INFINITY;
+      s[mt][e] = x;
+      if (e & 1)
+        mx1 = fmaxf(mx1, x);
+      else
+        mx0 = fmaxf(mx0, x);
+    }
+#pragma unroll
+  for (int sh = 4; sh < 32; sh <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
+  }
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+  m0 = mn0;
+  m1 = mn1;
+  float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float pv = ex2(s[mt][e] - ((e & 1) ? mn1 : mn0));
+      s[mt][e] = pv;
+      if (e & 1)
+        ps1 += pv;
+      else
+        ps0 += pv;
+    }
+  l0 = l0 * al0 + ps0;
+  l1 = l1 * al1 + ps1;
+#pragma unroll
+  for (int dm = 0; dm < NK; ++dm) {
+    o[dm][0] *= al0;
+    o[dm][1] *= al1;
+    o[dm][2] *= al0;
+    o[dm][3] *= al1;
+  }
+  // P^T as the B operand (k = tokens, n = query columns), high and residual.
+  uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const uint32_t h01 = pack_bf16(s[mt][0], s[mt][1]);
+    const uint32_t h23 = pack_bf16(s[mt][2], s[mt][3]);
+    const float2 f01 = unpack_bf16(h01), f23 = unpack_bf16(h23);
+    const uint32_t r01 = pack_bf16(s[mt][0] - f01.x, s[mt][1] - f01.y);
+    const uint32_t r23 = pack_bf16(s[mt][2] - f23.x, s[mt][3] - f23.y);
+    bh[mt][0] = movmatrix_t(h01);
+    bh[mt][1] = movmatrix_t(h23);
+    bl[mt][0] = movmatrix_t(r01);
+    bl[mt][1] = movmatrix_t(r23);
+  }
+  const bool tail = valid < kStageTokens;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    const int tok = mt * 16 + (mi >> 1) * 8 + lr;
+    // tokens held by this lane in the V^T fragment (for tail masking)
+    const int t0 = mt * 16 + 2 * c;
+    const uint32_t k01 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+    const uint32_t k89 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int dm = 0; dm < NK; ++dm) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vbase + tile_off(tok, 2 * dm + (mi & 1)), a0, a1, a2, a3);
+      if (tail) {  // rows past the valid tokens may hold stale or padding data
+        a0 &= k01;
+        a1 &= k01;
+        a2 &= k89;
+        a3 &= k89;
+      }
+      mma_bf16(o[dm], a0, a1, a2, a3, bh[mt][0], bh[mt][1]);
+      mma_bf16(o[dm], a0, a1, a2, a3, bl[mt][0], bl[mt][1]);
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__((kCons + 1) * 32, 1)
+    attn_mma_kernel(const __grid_constant__ AttnParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem =
+      (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  float *merge = (float *)(smem + kStages * C::kStage);
+  uint64_t *bars = (uint64_t *)(merge + 2 * kCons * C::kMW);
+  volatile int *abort_flag = (volatile int *)(bars + 2 * kStages);
+  const uint32_t stage0 = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int it0 = p.cta_off[blockIdx.x], it1 = p.cta_off[blockIdx.x + 1];
+  const int P = p.P, g = p.g;
+  uint64_t t_start = 0;
+  if (threadIdx.x == 0) {
+    if (p.trace) t_start = globaltimer_ns();
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kCons) {
+    // ------------------------------------------------------------ producer
+    const uint64_t pol = policy_evict_first();
+    const int box_h = P < kStageTokens ? P : kStageTokens;
+    const uint32_t box_bytes = (uint32_t)box_h * 128u;
+    int gs = 0;
+    bool dead = false;
+    for (int it = it0; it < it1 && !dead; ++it) {
+      const Item item = p.items[it];
+      const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
+      const int gi = p.head_grp[h], row = p.head_row[h];
+      const GroupDesc &gd = p.grp[gi];
+      const int32_t *pt = gd.page_table + (size_t)b * gd.stride;
+      const void *tmk = &p.tmK[gi];
+      const void *tmv = &p.tmV[gi];
+      const int rows_ext = (int)(gd.num_pages * gd.size * P);
+      const int maxpg = (item.end - 1) / P;
+      int win = -1;
+      int32_t my_page = 0;
+      for (int t0 = item.begin; t0 < item.end; t0 += kStageTokens, ++gs) {
+        const int slot = gs % kStages;
+        const int valid = min(kStageTokens, item.end - t0);
+        const int nbox = (valid + box_h - 1) / box_h;
+        const int pg_last = (t0 + valid - 1) / P;
+        if (win < 0 || pg_last >= win + 32) {
+          win = t0 / P;
+          const int idx = win + lane;
+          my_page = idx <= maxpg ? __ldg(pt + idx) : 0;
+        }
+        if (gs >= kStages) {
+          bool ok = true;
+          if (lane == 0)
+            ok = !*abort_flag &&
+                 mbar_wait(empty0 + 8 * slot, ((gs / kStages) - 1) & 1, kWaitNs);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) {
+            if (lane == 0) {
+              atomicOr(p.status, KVX_DEV_TIMEOUT);
+              *abort_flag = 1;
+            }
+            dead = true;
+            break;
+          }
+        }
+        const uint32_t full = full0 + 8 * slot;
+        if (lane == 0)
+          mbar_arrive_expect_tx(full, (uint32_t)nbox * box_bytes * C::kHalves * 2u);
+        const uint32_t kdst = stage0 + slot * C::kStage;
+        for (int i = 0; i < nbox; ++i) {
+          const int tb = t0 + i * box_h;
+          const int32_t page = __shfl_sync(0xffffffffu, my_page, tb / P - win);
+          int y;
+          if (page < 0 || (int64_t)page >= gd.num_pages) {
+            if (lane == 0) atomicOr(p.status, KVX_DEV_BAD_PAGE);
+            y = rows_ext;  // whole box past the end: loads zeros
+          } else {
+            y = (page * gd.size + row) * P + (tb & (P - 1));
+          }
+          if (lane == 0) {
+            const uint32_t d = kdst + (uint32_t)(i * box_h) * 128u;
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf) {
+              tma_load_2d(d + hf * kStageTokens * 128, tmk, hf * 64, y, full, pol);
+              tma_load_2d(d + C::kTile + hf * kStageTokens * 128, tmv, hf * 64, y,
+                          full, pol);
+            }
+          }
+        }
+      }
+    }
+    // Do not leave while a load of ours may still be landing.
+    if (lane == 0) {
+      const int issued = gs;
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / kStages) * kStages;
+        if (!mbar_wait(full0 + 8 * s, (last / kStages) & 1, kWaitNs))
+          atomicOr(p.status, KVX_DEV_TIMEOUT);
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- consumers
+    constexpr int NK = D / 16;
+    const int r = lane >> 2, c = lane & 3;
+    const float sl2 = p.scale_log2;
+    int gs = 0;
+    bool dead = false;
+    for (int it = it0; it < it1; ++it) {
+      const Item item = p.items[it];
+      const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
+      if (warp == 0 && lane == 0) {
+        const int L = __ldg(p.seq_len + b), bud = __ldg(p.head_budget + item.bh);
+        if (min(L, bud) != __ldg(p.n_plan + item.bh))
+          atomicOr(p.status, KVX_DEV_BAD_BUDGET);
+      }
+      uint32_t qf[NK][2];
+      {
+        const __nv_bfloat16 *qb = (const __nv_bfloat16 *)p.q +
+                                  ((size_t)b * p.Hq + (size_t)h * g + r) * D;
+#pragma unroll
+        for (int j = 0; j < NK; ++j) {
+          if (r < g) {
+            qf[j][0] = __ldg((const uint32_t *)(qb + 16 * j + 2 * c));
+            qf[j][1] = __ldg((const uint32_t *)(qb + 16 * j + 2 * c + 8));
+          } else {
+            qf[j][0] = qf[j][1] = 0u;
+          }
+        }
+      }
+      float o[NK][4];
+#pragma unroll
+      for (int dm = 0; dm < NK; ++dm) o[dm][0] = o[dm][1] = o[dm][2] = o[dm][3] = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      const int nst = (item.end - item.begin + kStageTokens - 1) / kStageTokens;
+      for (int st = 0; st < nst; ++st, ++gs) {
+        if (gs % kCons != warp || dead) continue;
+        const int slot = gs % kStages;
+        bool ok = !*abort_flag;
+        if (ok) ok = mbar_wait(full0 + 8 * slot, (gs / kStages) & 1, kWaitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) {
+            atomicOr(p.status, KVX_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+          dead = true;
+          continue;
+        }
+        const int valid = min(kStageTokens, item.end - (item.begin + st * kStageTokens));
+        const uint32_t kb = stage0 + slot * C::kStage;
+        consume_stage<D>(kb, kb + C::kTile, valid, qf, o, m0, m1, l0, l1, sl2, lane);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      }
+      // ---- merge the consumer warps' partial states of this item
+#pragma unroll
+      for (int sh = 4; sh < 32; sh <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
+      }
+      float *buf = merge + ((it - it0) & 1) * kCons * C::kMW;
+      float *mw = buf + warp * C::kMW;
+#pragma unroll
+      for (int dm = 0; dm < NK; ++dm) {
+        mw[(2 * c) * C::kMS + 16 * dm + r] = o[dm][0];
+        mw[(2 * c + 1) * C::kMS + 16 * dm + r] = o[dm][1];
+        mw[(2 * c) * C::kMS + 16 * dm + r + 8] = o[dm][2];
+        mw[(2 * c + 1) * C::kMS + 16 * dm + r + 8] = o[dm][3];
+      }
+      if (r == 0) {
+        mw[8 * C::kMS + 2 * c] = m0;
+        mw[8 * C::kMS + 2 * c + 1] = m1;
+        mw[8 * C::kMS + 8 + 2 * c] = l0;
+        mw[8 * C::kMS + 8 + 2 * c + 1] = l1;
+      }
+      consumer_sync(kCons * 32);
+      const int tid = threadIdx.x;
+      for (int idx = tid; idx < g * D; idx += kCons * 32) {
+        const int qi = idx / D, d = idx - qi * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) M = fmaxf(M, buf[w * C::kMW + 8 * C::kMS + qi]);
+        float Ls = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) {
+          const float f = ex2(buf[w * C::kMW + 8 * C::kMS + qi] - M);
+          Ls += f * buf[w * C::kMW + 8 * C::kMS + 8 + qi];
+          O += f * buf[w * C::kMW + qi * C::kMS + d];
+        }
+        if (item.slot < 0) {
+          p.out[((size_t)b * p.Hq + (size_t)h * g + qi) * D + d] = O / Ls;
+        } else {
+          p.part_o[((size_t)item.slot * g + qi) * D + d] = O;
+          if (d == 0) p.part_ml[(size_t)item.slot * g + qi] = make_float2(M, Ls);
+        }
+      }
+    }
+  }
+  if (p.trace) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int64_t tok = 0;
+      for (int it = it0; it < it1; ++it) tok += p.items[it].end - p.items[it].begin;
+      int64_t *tr = p.trace + 4 * (size_t)blockIdx.x;
+      tr[0] = smid();
+      tr[1] = (int64_t)t_start;
+      tr[2] = (int64_t)globaltimer_ns();
+      tr[3] = tok;
+    }
+  }
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams &p, int num_ctas, cudaStream_t st) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  attn_mma_kernel<D><<<num_ctas, (kCons + 1) * 32, Cfg<D>::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_mma(const AttnParams &p, int num_ctas, cudaStream_t st) {
+  if (num_ctas <= 0) return cudaSuccess;
+  return p.D == 128 ? launch_d<128>(p, num_ctas, st) : launch_d<64>(p, num_ctas, st);
+}
+
+}  // namespace kvx

@@ -1,0 +1,167 @@
+// attn_simt.cu -- split decode attention over head-group pages on the CUDA
+// cores (fp32 or bf16 K/V, fp32 arithmetic).
+//
+// Same work items, partial format and output as the tensor-core kernel
+// ("Tangram: Unlocking Non-Uniform KV Cache for Efficient Multi-turn LLM
+// Serving", Fig. 8(b) page addressing, Fig. 13 ahead-of-time split): four
+// warps per block; warp w takes tokens begin+w, begin+w+4, ... of an item;
+// the 32 lanes of a warp split the head dimension, reduce the g dot products
+// with shuffles and run the online softmax per query head. The warps' states
+// are merged in shared memory at the end of each item. Page ids outside the
+// pool read as zero rows and set KVX_DEV_BAD_PAGE.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "kvx_internal.h"
+#include "ptx.cuh"
+
+namespace kvx {
+namespace {
+
+constexpr int kWarps = 4;
+
+template <typename T>
+__device__ __forceinline__ float to_f(T x);
+template <>
+__device__ __forceinline__ float to_f<float>(float x) {
+  return x;
+}
+template <>
+__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+  return __bfloat162float(x);
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+    attn_simt_kernel(const __grid_constant__ AttnParams p) {
+  constexpr int DL = D / 32;
+  constexpr int MW = 8 * D + 16;  // floats per warp record
+  __shared__ float merge[2][kWarps][MW];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int it0 = p.cta_off[blockIdx.x], it1 = p.cta_off[blockIdx.x + 1];
+  const int g = p.g, P = p.P;
+  uint64_t t_start = p.trace ? globaltimer_ns() : 0;
+  for (int it = it0; it < it1; ++it) {
+    const Item item = p.items[it];
+    const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
+    const int gi = p.head_grp[h], row = p.head_row[h];
+    const GroupDesc &gd = p.grp[gi];
+    const int32_t *pt = gd.page_table + (size_t)b * gd.stride;
+    const T *kp = (const T *)gd.k_pool;
+    const T *vp = (const T *)gd.v_pool;
+    if (warp == 0 && lane == 0) {
+      const int L = __ldg(p.seq_len + b), bud = __ldg(p.head_budget + item.bh);
+      if (min(L, bud) != __ldg(p.n_plan + item.bh)) atomicOr(p.status, KVX_DEV_BAD_BUDGET);
+    }
+    float qv[KVX_MAX_GQA][DL], o[KVX_MAX_GQA][DL], m[KVX_MAX_GQA], l[KVX_MAX_GQA];
+    const T *qb = (const T *)p.q + ((size_t)b * p.Hq + (size_t)h * g) * D;
+#pragma unroll
+    for (int j = 0; j < KVX_MAX_GQA; ++j) {
+      m[j] = -INFINITY;
+      l[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < DL; ++i) {
+        qv[j][i] = j < g ? to_f(qb[(size_t)j * D + lane + 32 * i]) : 0.f;
+        o[j][i] = 0.f;
+      }
+    }
+    for (int t = item.begin + warp; t < item.end; t += kWarps) {
+      const int32_t page = __ldg(pt + t / P);
+      float kv[DL], vv[DL];
+      if (page < 0 || (int64_t)page >= gd.num_pages) {
+        if (lane == 0) atomicOr(p.status, KVX_DEV_BAD_PAGE);
+#pragma unroll
+        for (int i = 0; i < DL; ++i) kv[i] = vv[i] = 0.f;
+      } else {
+        const size_t rr = ((size_t)page * gd.size + row) * P + (t & (P - 1));
+#pragma unroll
+        for (int i = 0; i < DL; ++i) {
+          kv[i] = to_f(kp[rr * D + lane + 32 * i]);
+          vv[i] = to_f(vp[rr * D + lane + 32 * i]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < KVX_MAX_GQA; ++j) {
+        if (j >= g) break;
+        float dot = 0.f;
+#pragma unroll
+        for (int i = 0; i < DL; ++i) dot = fmaf(qv[j][i], kv[i], dot);
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+        const float x = dot * p.scale_log2;
+        const float mn = fmaxf(m[j], x);
+        const float al = ex2(m[j] - mn), pw = ex2(x - mn);
+        l[j] = l[j] * al + pw;
+#pragma unroll
+        for (int i = 0; i < DL; ++i) o[j][i] = fmaf(o[j][i], al, pw * vv[i]);
+        m[j] = mn;
+      }
+    }
+    float *buf = &merge[(it - it0) & 1][0][0];
+    float *mw = buf + warp * MW;
+#pragma unroll
+    for (int j = 0; j < KVX_MAX_GQA; ++j) {
+      if (j >= g) break;
+#pragma unroll
+      for (int i = 0; i < DL; ++i) mw[j * D + lane + 32 * i] = o[j][i];
+      if (lane == 0) {
+        mw[8 * D + j] = m[j];
+        mw[8 * D + 8 + j] = l[j];
+      }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < g * D; idx += kWarps * 32) {
+      const int qi = idx / D, d = idx - qi * D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, buf[w * MW + 8 * D + qi]);
+      float Ls = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = ex2(buf[w * MW + 8 * D + qi] - M);
+        Ls += f * buf[w * MW + 8 * D + 8 + qi];
+        O += f * buf[w * MW + qi * D + d];
+      }
+      if (item.slot < 0) {
+        p.out[((size_t)b * p.Hq + (size_t)h * g + qi) * D + d] = O / Ls;
+      } else {
+        p.part_o[((size_t)item.slot * g + qi) * D + d] = O;
+        if (d == 0) p.part_ml[(size_t)item.slot * g + qi] = make_float2(M, Ls);
+      }
+    }
+  }
+  if (p.trace) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int64_t tok = 0;
+      for (int it = it0; it < it1; ++it) tok += p.items[it].end - p.items[it].begin;
+      int64_t *tr = p.trace + 4 * (size_t)blockIdx.x;
+      tr[0] = smid();
+      tr[1] = (int64_t)t_start;
+      tr[2] = (int64_t)globaltimer_ns();
+      tr[3] = tok;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_simt(const AttnParams &p, int dtype, int num_ctas,
+                             cudaStream_t st) {
+  if (num_ctas <= 0) return cudaSuccess;
+  const dim3 grid(num_ctas), block(kWarps * 32);
+  if (dtype == KVX_F32) {
+    if (p.D == 128)
+      attn_simt_kernel<float, 128><<<grid, block, 0, st>>>(p);
+    else
+      attn_simt_kernel<float, 64><<<grid, block, 0, st>>>(p);
+  } else {
+    if (p.D == 128)
+      attn_simt_kernel<__nv_bfloat16, 128><<<grid, block, 0, st>>>(p);
+    else
+      attn_simt_kernel<__nv_bfloat16, 64><<<grid, block, 0, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvx

@@ -1,0 +1,127 @@
+// kvx_internal.h -- structures shared by the host planner, the C ABI and the
+// kernels of the kvx library. Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/kvx.h"
+
+namespace kvx {
+
+// Tokens one pipeline stage of the attention kernels covers (a multiple of
+// every supported page size up to 32, and two 16-row MMA tiles).
+constexpr int kStageTokens = 32;
+
+// One work item: tokens [begin, end) of head bh = b*Hkv + h. slot >= 0 names
+// the partial-result slot of a split head; slot < 0 means the item covers the
+// whole head and writes the final output.
+struct Item {
+  int32_t bh, begin, end, slot;
+};
+
+// A split head: its partials occupy slots [slot_begin, slot_begin + count).
+struct SplitHead {
+  int32_t bh, slot_begin, count, pad;
+};
+
+struct GroupDesc {
+  const int32_t *page_table;  // [B][stride]
+  const void *k_pool;         // [num_pages][size][P][D]
+  const void *v_pool;
+  int64_t num_pages;
+  int32_t stride;
+  int32_t size;
+};
+
+// Kernel parameters of the attention kernels (passed by value as a
+// __grid_constant__ argument; the tensor maps keep their 128-byte alignment).
+struct alignas(128) AttnParams {
+  CUtensorMap tmK[KVX_MAX_GROUPS];
+  CUtensorMap tmV[KVX_MAX_GROUPS];
+  GroupDesc grp[KVX_MAX_GROUPS];
+  const Item *items;
+  const int32_t *cta_off;
+  const int32_t *n_plan;       // [B*Hkv]
+  const int32_t *head_budget;  // [B*Hkv] device, for the plan check
+  const int32_t *seq_len;      // [B] device
+  const void *q;               // [B][Hq][D]
+  float *out;                  // [B][Hq][D]
+  float *part_o;               // [slots][g][D]
+  float2 *part_ml;             // [slots][g] = (max in log2 units, sum)
+  uint32_t *status;
+  int64_t *trace;
+  int32_t B, Hq, Hkv, D, g, P;
+  float scale_log2;            // scale * log2(e)
+  int8_t head_grp[KVX_MAX_KV_HEADS];
+  int8_t head_row[KVX_MAX_KV_HEADS];
+};
+
+struct CombineParams {
+  const SplitHead *heads;
+  const float *part_o;
+  const float2 *part_ml;
+  float *out;
+  int32_t num_heads, Hkv, Hq, g, D;
+};
+
+// Launchers (defined in the .cu files). Return cudaGetLastError().
+cudaError_t launch_attn_mma(const AttnParams &p, int num_ctas, cudaStream_t st);
+cudaError_t launch_attn_simt(const AttnParams &p, int dtype, int num_ctas,
+                             cudaStream_t st);
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);
+
+struct GatherParams {
+  const int32_t *block_table;  // [S][max_blocks]
+  const int32_t *num_blocks;   // [S]
+  const void *pools[KVX_MAX_GATHER_TENSORS];
+  void *stagings[KVX_MAX_GATHER_TENSORS];
+  uint32_t *status;
+  int64_t *totals;       // [0] runs, [1] live blocks
+  int32_t *run_count;    // [S]
+  int32_t *row_blocks;   // [S], -1 for a rejected row
+  int32_t *run_off;      // [S+1] first run of each row in `runs`
+  int64_t *row_bstart;   // [S+1] first live block of each row, all rows laid end to end
+  int4 *runs;            // [total runs] = {first physical block or -1, row, first logical block, length}
+  int64_t *run_bstart;   // [total runs] global index of each run's first block
+  int64_t num_phys, block_bytes, row_bytes;
+  int32_t S, max_blocks, num_tensors, flags;
+};
+
+// Workspace layout of the gather (offsets in bytes from the workspace start).
+struct GatherWs {
+  size_t run_count, row_blocks, run_off, row_bstart, runs, run_bstart, total;
+};
+GatherWs gather_ws_layout(int S, int max_blocks);
+
+cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
+
+
+}  // namespace kvx
+
+// The opaque plan.
+struct kvx_plan {
+  kvx_shape shape;
+  int32_t policy, kernel, num_ctas;
+  std::vector<int32_t> n;            // [B*Hkv]
+  std::vector<int32_t> head_group;   // [Hkv]
+  std::vector<int32_t> head_row;     // [Hkv]
+  std::vector<int32_t> group_size;   // [G]
+  std::vector<int32_t> group_pages;  // [G][B]
+  std::vector<kvx::Item> items;
+  std::vector<int32_t> cta_off;
+  std::vector<kvx::SplitHead> split_heads;
+  std::vector<int64_t> cta_tokens;
+  int32_t num_slots;
+  double plan_us;
+  // device copies (kvx_plan_upload)
+  void *d_buf;
+  kvx::Item *d_items;
+  int32_t *d_cta_off;
+  int32_t *d_n;
+  kvx::SplitHead *d_split;
+  int64_t *d_trace;
+};

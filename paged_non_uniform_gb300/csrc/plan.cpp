@@ -1,0 +1,367 @@
+// plan.cpp -- host planner of the kvx library (no device code).
+//
+// Builds, ahead of time and from static budgets only, the work split of the
+// decode-attention kernels ("Tangram: Unlocking Non-Uniform KV Cache for
+// Efficient Multi-turn LLM Serving", AOT Load Balancing, Figs. 4(c), 5, 13):
+// each head's kept tokens are cut into items and the items are packed onto
+// thread blocks so that every block streams about the same number of KV
+// bytes. Also reports the head-group page counts (Fig. 8) and the footprint
+// they imply (Fig. 7, M(r)).
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "kvx_internal.h"
+
+namespace kvx {
+int set_cuda_error(cudaError_t e);  // abi.cpp
+
+// Cost, in tokens, charged per work item on top of its tokens: the query
+// load, the cross-warp merge and the partial write of an item take about as
+// long as streaming this many tokens.
+static int item_overhead_tokens() { return 64; }
+
+static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+static void finish_splits(kvx_plan *p) {
+  const int H = p->shape.B * p->shape.Hkv;
+  std::vector<int32_t> count(H, 0);
+  for (const Item &it : p->items) count[it.bh]++;
+  std::vector<int32_t> first(H, -1);
+  int32_t slots = 0;
+  for (int bh = 0; bh < H; ++bh) {
+    if (count[bh] > 1) {
+      first[bh] = slots;
+      p->split_heads.push_back(SplitHead{bh, slots, count[bh], 0});
+      slots += count[bh];
+    }
+  }
+  // Slots of a split head follow its items' token order.
+  std::vector<int32_t> next(first);
+  std::vector<size_t> order(p->items.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+    const Item &x = p->items[a], &y = p->items[b];
+    return x.bh != y.bh ? x.bh < y.bh : x.begin < y.begin;
+  });
+  for (size_t i : order) {
+    Item &it = p->items[i];
+    it.slot = count[it.bh] > 1 ? next[it.bh]++ : -1;
+  }
+  p->num_slots = slots;
+  p->cta_tokens.assign(p->num_ctas, 0);
+  for (int c = 0; c < p->num_ctas; ++c)
+    for (int i = p->cta_off[c]; i < p->cta_off[c + 1]; ++i)
+      p->cta_tokens[c] += p->items[i].end - p->items[i].begin;
+}
+
+// Balanced: lay the heads' kept tokens end to end, charge each item its
+// tokens plus a fixed overhead, and cut the stream into num_ctas spans of
+// equal cost at stage boundaries.
+static void plan_balanced(kvx_plan *p, int num_ctas) {
+  const int H = p->shape.B * p->shape.Hkv;
+  const int T = kStageTokens;
+  const double c0 = item_overhead_tokens();
+  // Every block boundary can cut one head, adding one item (and its overhead).
+  double total = c0 * (num_ctas - 1);
+  for (int bh = 0; bh < H; ++bh) total += p->n[bh] + c0;
+  const double per = std::max(total / num_ctas, c0 + T);
+  p->num_ctas = num_ctas;
+  p->cta_off.assign(1, 0);
+  int cta = 0;
+  double used = 0;
+  auto close_cta = [&]() {
+    p->cta_off.push_back((int32_t)p->items.size());
+    ++cta;
+  };
+  for (int bh = 0; bh < H; ++bh) {
+    const int n = p->n[bh];
+    int pos = 0;
+    while (pos < n) {
+      const int rem = n - pos;
+      const double cap = (cta + 1) * per - used;
+      if (cta == num_ctas - 1 || cap >= rem + c0) {
+        p->items.push_back(Item{bh, pos, n, -1});
+        used += rem + c0;
+        pos = n;
+        continue;
+      }
+      int k = (int)std::floor((cap - c0) / T) * T;
+      if (k >= T) {
+        if (rem - k < T) k = rem;  // never leave a sliver behind
+        p->items.push_back(Item{bh, pos, pos + k, -1});
+        used += k + c0;
+        pos += k;
+        if (pos < n) close_cta();
+      } else {
+        close_cta();
+      }
+    }
+  }
+  while ((int)p->cta_off.size() < num_ctas + 1)
+    p->cta_off.push_back((int32_t)p->items.size());
+}
+
+// One block per head, no split.
+static void plan_per_head(kvx_plan *p) {
+  const int H = p->shape.B * p->shape.Hkv;
+  p->cta_off.assign(1, 0);
+  for (int bh = 0; bh < H; ++bh) {
+    p->items.push_back(Item{bh, 0, p->n[bh], -1});
+    p->cta_off.push_back((int32_t)p->items.size());
+  }
+  p->num_ctas = H;
+}
+
+// Every head cut into the same number of equal pieces, one block per piece.
+static void plan_uniform(kvx_plan *p, int sms) {
+  const int H = p->shape.B * p->shape.Hkv;
+  const int T = kStageTokens;
+  const int splits = std::max(1, (2 * sms + H - 1) / H);
+  p->cta_off.assign(1, 0);
+  for (int bh = 0; bh < H; ++bh) {
+    const int n = p->n[bh];
+    int chunk = (n + splits - 1) / splits;
+    chunk = ((chunk + T - 1) / T) * T;
+    for (int b0 = 0; b0 < n; b0 += chunk) {
+      p->items.push_back(Item{bh, b0, std::min(n, b0 + chunk), -1});
+      p->cta_off.push_back((int32_t)p->items.size());
+    }
+  }
+  p->num_ctas = (int32_t)p->items.size();
+}
+
+}  // namespace kvx
+
+using namespace kvx;
+
+extern "C" int kvx_device_sm_count(int32_t *sms) {
+  if (!sms) return KVX_EINVAL;
+  int dev = 0, v = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  *sms = v;
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
+                               const int32_t *seq_len,
+                               const int32_t *head_group, int32_t num_ctas,
+                               int32_t policy, int32_t kernel,
+                               kvx_plan **out) {
+  if (!out) return KVX_EINVAL;
+  *out = nullptr;
+  if (!s || !head_budget || !seq_len || !head_group) return KVX_EINVAL;
+  const auto t0 = std::chrono::steady_clock::now();
+  if (s->B < 1 || s->Hkv < 1 || s->Hq < 1 || s->num_groups < 1)
+    return KVX_EINVAL;
+  if (s->Hkv > KVX_MAX_KV_HEADS || s->num_groups > KVX_MAX_GROUPS ||
+      s->num_groups > s->Hkv)
+    return KVX_EUNSUPPORTED;
+  if (s->Hq % s->Hkv != 0) return KVX_EINVAL;
+  const int g = s->Hq / s->Hkv;
+  if (g > KVX_MAX_GQA) return KVX_EUNSUPPORTED;
+  if (s->D != 64 && s->D != 128) return KVX_EUNSUPPORTED;
+  if (!is_pow2(s->page_size) || s->page_size < 8 || s->page_size > 128)
+    return KVX_EUNSUPPORTED;
+  if (s->dtype != KVX_F32 && s->dtype != KVX_BF16) return KVX_EUNSUPPORTED;
+  if (policy < KVX_PLAN_BALANCED || policy > KVX_PLAN_UNIFORM)
+    return KVX_EINVAL;
+  if (kernel < KVX_KERNEL_AUTO || kernel > KVX_KERNEL_SIMT) return KVX_EINVAL;
+  int resolved = kernel;
+  if (resolved == KVX_KERNEL_AUTO)
+    resolved = s->dtype == KVX_BF16 ? KVX_KERNEL_MMA : KVX_KERNEL_SIMT;
+  if (resolved == KVX_KERNEL_MMA && s->dtype != KVX_BF16)
+    return KVX_EUNSUPPORTED;
+  if (num_ctas < 0) return KVX_EINVAL;
+
+  const int B = s->B, Hkv = s->Hkv, G = s->num_groups, P = s->page_size;
+  for (int h = 0; h < Hkv; ++h)
+    if (head_group[h] < 0 || head_group[h] >= G) return KVX_EINVAL;
+  for (int b = 0; b < B; ++b)
+    if (seq_len[b] < 1) return KVX_EINVAL;
+  for (int i = 0; i < B * Hkv; ++i)
+    if (head_budget[i] < 1) return KVX_EINVAL;
+
+  int sms = 0;
+  if ((policy == KVX_PLAN_BALANCED && num_ctas == 0) ||
+      policy == KVX_PLAN_UNIFORM) {
+    if (num_ctas > 0) {
+      sms = num_ctas;
+    } else {
+      int rc = kvx_device_sm_count(&sms);
+      if (rc != KVX_OK) return rc;
+    }
+  }
+
+  kvx_plan *p = new (std::nothrow) kvx_plan();
+  if (!p) return KVX_ENOMEM;
+  try {
+    p->shape = *s;
+    p->policy = policy;
+    p->kernel = resolved;
+    p->num_ctas = 0;
+    p->num_slots = 0;
+    p->d_buf = nullptr;
+    p->d_items = nullptr;
+    p->d_cta_off = nullptr;
+    p->d_n = nullptr;
+    p->d_split = nullptr;
+    p->d_trace = nullptr;
+    // Deterministic Budget Allocation: n = min(L, budget).
+    p->n.resize((size_t)B * Hkv);
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < Hkv; ++h)
+        p->n[(size_t)b * Hkv + h] =
+            std::min(seq_len[b], head_budget[(size_t)b * Hkv + h]);
+    // Head groups: rows within a group in ascending head order.
+    p->head_group.assign(head_group, head_group + Hkv);
+    p->head_row.assign(Hkv, 0);
+    p->group_size.assign(G, 0);
+    for (int h = 0; h < Hkv; ++h) p->head_row[h] = p->group_size[head_group[h]]++;
+    for (int gi = 0; gi < G; ++gi)
+      if (p->group_size[gi] == 0) {
+        delete p;
+        return KVX_EINVAL;
+      }
+    p->group_pages.assign((size_t)G * B, 0);
+    for (int b = 0; b < B; ++b)
+      for (int h = 0; h < Hkv; ++h) {
+        int32_t &pg = p->group_pages[(size_t)head_group[h] * B + b];
+        pg = std::max(pg, (p->n[(size_t)b * Hkv + h] + P - 1) / P);
+      }
+    if (policy == KVX_PLAN_BALANCED)
+      plan_balanced(p, num_ctas > 0 ? num_ctas : sms);
+    else if (policy == KVX_PLAN_PER_HEAD)
+      plan_per_head(p);
+    else
+      plan_uniform(p, sms);
+    finish_splits(p);
+  } catch (const std::bad_alloc &) {
+    delete p;
+    return KVX_ENOMEM;
+  }
+  p->plan_us = std::chrono::duration<double, std::micro>(
+                   std::chrono::steady_clock::now() - t0)
+                   .count();
+  *out = p;
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_upload(kvx_plan *p, void *stream) {
+  if (!p) return KVX_EINVAL;
+  if (p->d_buf) return KVX_OK;
+  const size_t ni = p->items.size(), nc = p->cta_off.size(), nn = p->n.size(),
+               ns = p->split_heads.size();
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t o_items = 0, o_cta = al(o_items + ni * sizeof(Item)),
+               o_n = al(o_cta + nc * sizeof(int32_t)),
+               o_split = al(o_n + nn * sizeof(int32_t)),
+               total = al(o_split + std::max<size_t>(ns, 1) * sizeof(SplitHead));
+  void *buf = nullptr;
+  cudaError_t e = cudaMalloc(&buf, total);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  char *b = (char *)buf;
+  cudaStream_t st = (cudaStream_t)stream;
+  e = cudaMemcpyAsync(b + o_items, p->items.data(), ni * sizeof(Item),
+                      cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b + o_cta, p->cta_off.data(), nc * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(b + o_n, p->n.data(), nn * sizeof(int32_t),
+                        cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && ns)
+    e = cudaMemcpyAsync(b + o_split, p->split_heads.data(),
+                        ns * sizeof(SplitHead), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cudaFree(buf);
+    return set_cuda_error(e);
+  }
+  p->d_buf = buf;
+  p->d_items = (Item *)(b + o_items);
+  p->d_cta_off = (int32_t *)(b + o_cta);
+  p->d_n = (int32_t *)(b + o_n);
+  p->d_split = (SplitHead *)(b + o_split);
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_workspace_bytes(const kvx_plan *p, size_t *bytes) {
+  if (!p || !bytes) return KVX_EINVAL;
+  const size_t g = (size_t)(p->shape.Hq / p->shape.Hkv);
+  const size_t slots = (size_t)p->num_slots;
+  size_t ml = (slots * g * sizeof(float2) + 255) & ~size_t(255);
+  *bytes = KVX_WS_HEADER_BYTES + ml + slots * g * p->shape.D * sizeof(float);
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_get_stats(const kvx_plan *p, kvx_plan_stats *st) {
+  if (!p || !st) return KVX_EINVAL;
+  std::memset(st, 0, sizeof(*st));
+  st->num_ctas = p->num_ctas;
+  st->num_items = (int32_t)p->items.size();
+  st->num_slots = p->num_slots;
+  st->num_split_heads = (int32_t)p->split_heads.size();
+  st->kernel = p->kernel;
+  st->policy = p->policy;
+  int64_t tot = 0, mx = 0;
+  for (int32_t v : p->n) tot += v;
+  for (int64_t v : p->cta_tokens) mx = std::max(mx, v);
+  st->total_tokens = tot;
+  st->max_cta_tokens = mx;
+  st->mean_cta_tokens = p->num_ctas ? (double)tot / p->num_ctas : 0.0;
+  const int B = p->shape.B, G = p->shape.num_groups, P = p->shape.page_size;
+  int64_t alloc = 0;
+  for (int gi = 0; gi < G; ++gi)
+    for (int b = 0; b < B; ++b)
+      alloc += (int64_t)p->group_pages[(size_t)gi * B + b] * p->group_size[gi] * P;
+  st->slots_allocated = alloc;
+  st->slots_used = tot;
+  st->plan_us = p->plan_us;
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_kept(const kvx_plan *p, int32_t *n) {
+  if (!p || !n) return KVX_EINVAL;
+  std::memcpy(n, p->n.data(), p->n.size() * sizeof(int32_t));
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_group_pages(const kvx_plan *p, int32_t *pages) {
+  if (!p || !pages) return KVX_EINVAL;
+  std::memcpy(pages, p->group_pages.data(),
+              p->group_pages.size() * sizeof(int32_t));
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_items(const kvx_plan *p, int32_t *items,
+                              int32_t *cta_off) {
+  if (!p || !items || !cta_off) return KVX_EINVAL;
+  std::memcpy(items, p->items.data(), p->items.size() * sizeof(Item));
+  std::memcpy(cta_off, p->cta_off.data(), p->cta_off.size() * sizeof(int32_t));
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_cta_tokens(const kvx_plan *p, int64_t *tokens) {
+  if (!p || !tokens) return KVX_EINVAL;
+  std::memcpy(tokens, p->cta_tokens.data(),
+              p->cta_tokens.size() * sizeof(int64_t));
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_set_trace(kvx_plan *p, int64_t *dev_trace) {
+  if (!p) return KVX_EINVAL;
+  p->d_trace = dev_trace;
+  return KVX_OK;
+}
+
+extern "C" void kvx_plan_destroy(kvx_plan *p) {
+  if (!p) return;
+  if (p->d_buf) cudaFree(p->d_buf);
+  delete p;
+}

@@ -351,3 +351,16 @@ def block_stamp_pool(num_phys: int, block_bytes: int, seed: int = 0) -> np.ndarr
     ids = np.arange(num_phys, dtype=np.int64).view(np.uint8).reshape(num_phys, 8)
     pool[:, :8] = ids
     return pool
+
+
+def select_top_recent(q_heads: np.ndarray, k: np.ndarray, top: int = 2048,
+                      recent: int = 128) -> np.ndarray:
+    """Kept set of one KV head for the sparse long-context workload: the last
+    `recent` positions plus the `top` positions of [0, L - recent) with the
+    largest score sum_j <q_j, k_t> over the head's query heads (float64; ties
+    go to the lower position). Returns ascending positions."""
+    L = k.shape[0]
+    cut = max(0, L - recent)
+    score = k[:cut].astype(np.float64) @ q_heads.astype(np.float64).sum(0)
+    order = np.lexsort((np.arange(cut), -score))[:min(top, cut)]
+    return np.sort(np.concatenate([order, np.arange(cut, L)])).astype(np.int32)

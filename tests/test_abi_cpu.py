@@ -1,0 +1,174 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and its host-only planner agrees with the oracle."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvx():
+    from paged_non_uniform_gb300 import build
+    build.build()
+    from paged_non_uniform_gb300 import kvx as k
+    return k
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvx.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvx_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("kvx_plan_create", "kvx_decode_attn", "kvx_gather_coalesce",
+                 "kvx_plan_destroy", "kvx_plan_upload", "kvx_plan_workspace_bytes"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(kvx):
+    missing = [n for n in declared_functions() if not hasattr(kvx.lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(kvx):
+    for code in (0, -1, -2, -3, -4, -5, -6, -99):
+        assert isinstance(kvx.kvx_status_string(code), str)
+
+
+def _plan(kvx, case, num_ctas=0, policy=0, kernel=0):
+    dtype = kvx.KVX_BF16 if case.dtype == "bf16" else kvx.KVX_F32
+    G = int(case.head_group.max()) + 1
+    return kvx.kvx_plan_create(case.B, case.Hq, case.Hkv, case.D, case.P, G, dtype,
+                               case.budget, case.seq_len, case.head_group, num_ctas, policy,
+                               kernel)
+
+
+CASES = {
+    "tiny_per_head": lambda: synth.tiny(0, "per_head"),
+    "tiny_one_group": lambda: synth.tiny(0, "one"),
+    "mixed": lambda: synth.dense_case(3, 12, 4, 64, [40, 300, 1000],
+                                      [[40, 5, 17, 33], [300, 100, 1, 64], [900, 1000, 31, 32]],
+                                      "f32", seed=2, head_group=[0, 1, 1, 2]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("policy", [0, 1, 2])
+@pytest.mark.parametrize("num_ctas", [1, 3, 7, 152])
+def test_plan_coverage_matches_oracle(kvx, orc, name, policy, num_ctas):
+    case = CASES[name]()
+    plan = _plan(kvx, case, num_ctas=num_ctas, policy=policy)
+    n_oracle = orc.resolve_budget(case.budget, case.seq_len)
+    assert np.array_equal(plan.kept(), n_oracle)
+    assert np.array_equal(plan.kept(), case.n)
+    items, off = plan.items()
+    bad, count = orc.plan_coverage(n_oracle.reshape(-1), items)
+    assert bad == 0
+    st = plan.stats()
+    assert off[0] == 0 and off[-1] == len(items) and np.all(np.diff(off) >= 0)
+    assert st["total_tokens"] == int(n_oracle.sum())
+    # partial slots: every item of a split head has a distinct slot, others -1
+    per_head = np.bincount(items[:, 0], minlength=case.B * case.Hkv)
+    split = per_head[items[:, 0]] > 1
+    assert np.all(items[~split, 3] == -1)
+    slots = items[split, 3]
+    assert sorted(slots.tolist()) == list(range(st["num_slots"]))
+    # items start on stage boundaries (32 tokens)
+    assert np.all(items[:, 1] % 32 == 0)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_group_pages_and_footprint_match_oracle(kvx, orc, name):
+    case = CASES[name]()
+    plan = _plan(kvx, case, num_ctas=4)
+    pages = orc.group_pages(case.n, case.head_group, case.P)
+    assert np.array_equal(plan.group_pages(), pages)
+    st = plan.stats()
+    fp = orc.footprint_bytes(case.n, case.head_group, case.P, case.D, 4)
+    # footprint = allocated token slots x 2 (K, V) x D x bytes
+    assert st["slots_allocated"] * 2 * case.D * 4 == int(fp.sum())
+    assert st["slots_used"] == int(case.n.sum())
+
+
+def test_balanced_plan_is_balanced(kvx):
+    cfg = synth.decode_config("qwen3_4b", seed=0, layers=2)
+    for layer in range(cfg.layers):
+        plan = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                                   kvx.KVX_BF16, cfg.budget[layer], cfg.seq_len,
+                                   cfg.head_group[layer], 152)
+        t = plan.cta_tokens()
+        st = plan.stats()
+        assert t.sum() == cfg.n[layer].sum()
+        # max load within one item overhead + one stage of the mean
+        assert t.max() <= t.mean() + 64 + 32 + 1, (t.max(), t.mean())
+        naive = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                                    kvx.KVX_BF16, cfg.budget[layer], cfg.seq_len,
+                                    cfg.head_group[layer], 152, kvx.KVX_PLAN_PER_HEAD)
+        assert naive.stats()["max_cta_tokens"] > 2 * st["max_cta_tokens"]
+
+
+@pytest.mark.parametrize("bad", ["budget0", "seq0", "group_range", "empty_group", "gqa",
+                                 "head_dim", "page", "mma_f32", "policy"])
+def test_plan_rejects_bad_arguments(kvx, bad):
+    B, Hq, Hkv, D, P, G = 2, 8, 2, 64, 16, 2
+    budget, seq, hg = np.array([[4, 5], [6, 7]]), np.array([10, 20]), np.array([0, 1])
+    dtype, kernel, policy = kvx.KVX_BF16, 0, 0
+    if bad == "budget0":
+        budget = np.array([[0, 5], [6, 7]])
+    elif bad == "seq0":
+        seq = np.array([0, 20])
+    elif bad == "group_range":
+        hg = np.array([0, 2])
+    elif bad == "empty_group":
+        hg = np.array([0, 0])
+    elif bad == "gqa":
+        Hq = 7
+    elif bad == "head_dim":
+        D = 96
+    elif bad == "page":
+        P = 12
+    elif bad == "mma_f32":
+        dtype, kernel = kvx.KVX_F32, kvx.KVX_KERNEL_MMA
+    elif bad == "policy":
+        policy = 9
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_plan_create(B, Hq, Hkv, D, P, G, dtype, budget, seq, hg, 4, policy, kernel)
+    assert e.value.status in (kvx.KVX_EINVAL, kvx.KVX_EUNSUPPORTED)
+
+
+def test_decode_rejects_before_upload(kvx):
+    case = synth.tiny(0)
+    plan = _plan(kvx, case, num_ctas=2)
+    rc = kvx.lib.kvx_decode_attn(plan.handle, 16, (kvx._vp * 2)(16, 16), (kvx._vp * 2)(16, 16),
+                                 np.array([1, 1], np.int64).ctypes.data,
+                                 (kvx._vp * 2)(16, 16), np.array([8, 8], np.int32).ctypes.data,
+                                 16, 16, 0.0, 16, 256, 1 << 20, None)
+    assert rc == kvx.KVX_ESTATE
+
+
+def test_gather_rejects_bad_arguments(kvx):
+    p = (kvx._vp * 1)(4096)
+    ws = kvx.kvx_gather_workspace_bytes(2, 4)
+    assert ws > kvx.KVX_WS_HEADER_BYTES
+    # block_bytes not a multiple of 16
+    rc = kvx.lib.kvx_gather_coalesce(256, 256, 2, 4, 1, p, 8, 40, p, 160, 0, 256, ws, None)
+    assert rc == kvx.KVX_EINVAL
+    # workspace too small
+    rc = kvx.lib.kvx_gather_coalesce(256, 256, 2, 4, 1, p, 8, 32, p, 128, 0, 256, 16, None)
+    assert rc == kvx.KVX_EINVAL
+    # unknown flag
+    rc = kvx.lib.kvx_gather_coalesce(256, 256, 2, 4, 1, p, 8, 32, p, 128, 8, 256, ws, None)
+    assert rc == kvx.KVX_EINVAL

@@ -1,0 +1,189 @@
+"""Parity of the CUDA decode-attention path against the fp64 oracle.
+
+Tolerances: bf16 K/V with fp32 accumulation must stay within max-abs 2e-3 of
+the oracle (the accuracy target of the method's GPU path). fp32 K/V: the
+kernel's only approximations are fp32 rounding and the hardware exp2
+(relative error ~2^-22), so 2e-5 is a safe bound for |o| <= ~4.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from harness import DeviceCase, make_plan, max_abs, oracle_out
+from paged_non_uniform_gb300 import kvx
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-3
+TOL_F32 = 2e-5
+
+
+def qwen3_like(seed=0):
+    L = [700, 2000, 3100]
+    g = synth.rng(seed)
+    rate = g.uniform(0.1, 0.5, size=8)
+    rate[[1, 6]] = 1.0
+    n = [[L[b] if rate[h] >= 1 else max(1, int(math.ceil(rate[h] * L[b]))) for h in range(8)]
+         for b in range(3)]
+    return synth.dense_case(3, 32, 8, 128, L, n, "bf16", seed=seed, P=16,
+                            head_group=synth.groups_by_budget(rate, [2, 3, 3]))
+
+
+def qwen25_like(seed=0):
+    L = [2500, 90, 1000, 377]
+    full = [0, 3, 4, 7]
+    n = [[L[b] if h in full else max(1, int(math.ceil(0.125 * L[b]))) for h in range(8)]
+         for b in range(4)]
+    rate = np.array([1.0 if h in full else 0.125 for h in range(8)])
+    return synth.dense_case(4, 40, 8, 128, L, n, "bf16", seed=seed, P=32,
+                            head_group=synth.groups_by_budget(rate, [2, 2, 2, 2]))
+
+
+def sparse_like(seed=0):
+    return synth.dense_case(2, 32, 8, 128, [5000, 4100], [[2176] * 8] * 2, "bf16", seed=seed,
+                            P=16, head_group=np.zeros(8, np.int32))
+
+
+def d64_bf16(seed=0):
+    return synth.dense_case(2, 4, 2, 64, [37, 100], [[37, 20], [100, 20]], "bf16", seed=seed,
+                            P=16, head_group=[0, 1])
+
+
+def g8_p8(seed=0):
+    return synth.dense_case(2, 16, 2, 128, [300, 77], [[300, 40], [3, 77]], "bf16", seed=seed,
+                            P=8, head_group=[0, 0])
+
+
+def p64(seed=0):
+    return synth.dense_case(2, 8, 4, 128, [600, 130], [[600, 1, 64, 65], [130, 2, 33, 129]],
+                            "bf16", seed=seed, P=64, head_group=[0, 1, 1, 0])
+
+
+BF16_CASES = {"qwen3_like": qwen3_like, "qwen25_like": qwen25_like, "sparse_like": sparse_like,
+              "d64": d64_bf16, "g8_p8": g8_p8, "p64": p64}
+
+
+@pytest.mark.parametrize("grouping", ["per_head", "one"])
+@pytest.mark.parametrize("policy,num_ctas", [(0, 0), (0, 1), (0, 2), (0, 3), (0, 5),
+                                             (1, 0), (2, 4)])
+def test_tiny_fp32(grouping, policy, num_ctas):
+    case = synth.tiny(0, grouping)
+    plan = make_plan(case, num_ctas=num_ctas, policy=policy)
+    dev = DeviceCase(case, plan)
+    got = dev.run()
+    ref = oracle_out(case)
+    assert np.all(np.isfinite(got))
+    err = max_abs(got, ref)
+    assert err <= TOL_F32, err
+    assert dev.status() == 0
+
+
+@pytest.mark.parametrize("name", sorted(BF16_CASES))
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+@pytest.mark.parametrize("num_ctas", [0, 7])
+def test_bf16_parity(name, kernel, num_ctas):
+    case = BF16_CASES[name]()
+    plan = make_plan(case, num_ctas=num_ctas, kernel=kernel)
+    dev = DeviceCase(case, plan)
+    got = dev.run()
+    ref = oracle_out(case)
+    assert np.all(np.isfinite(got))
+    err = max_abs(got, ref)
+    assert err <= TOL_BF16, err
+    assert dev.status() == 0
+
+
+@pytest.mark.parametrize("policy", [kvx.KVX_PLAN_PER_HEAD, kvx.KVX_PLAN_UNIFORM])
+def test_naive_plans_match_oracle(policy):
+    case = qwen3_like(1)
+    dev = DeviceCase(case, make_plan(case, policy=policy))
+    assert max_abs(dev.run(), oracle_out(case)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+def test_page_permutation_is_bit_exact(kernel):
+    """Same plan and page size, different physical page order: identical bits."""
+    case = qwen3_like(2)
+    plan = make_plan(case, num_ctas=11, kernel=kernel)
+    a = DeviceCase(case, plan, perm_seed=1).run()
+    b = DeviceCase(case, plan, perm_seed=2, spare_pages=17).run()
+    assert np.array_equal(a, b)
+
+
+def test_page_size_and_grouping_invariance():
+    """P = 16 vs 32 and three group assignments: all within tolerance of the oracle."""
+    base = qwen3_like(3)
+    ref = oracle_out(base)
+    for P in (16, 32):
+        for hg in ([0, 1, 2, 3, 4, 5, 6, 7], [0] * 8, list(base.head_group)):
+            case = synth.dense_case(base.B, base.Hq, base.Hkv, base.D, base.seq_len, base.n,
+                                    "bf16", seed=3, P=P, head_group=hg)
+            got = DeviceCase(case, make_plan(case)).run()
+            assert max_abs(got, ref) <= TOL_BF16, (P, hg)
+
+
+def test_tokens_outside_kept_set_do_not_matter():
+    """Dense rows a head does not keep, set to NaN, change nothing (bitwise);
+    padding slots of partial pages hold NaN in every run here."""
+    case = qwen25_like(4)
+    plan = make_plan(case)
+    a = DeviceCase(case, plan).run()
+    k, v = case.k.copy(), case.v.copy()
+    for b in range(case.B):
+        for h in range(case.Hkv):
+            mask = np.ones(k.shape[2], bool)
+            mask[case.kept[b * case.Hkv + h]] = False
+            k[b, h, mask] = np.nan
+            v[b, h, mask] = np.nan
+    b_ = DeviceCase(case, plan, dense_override=(k, v)).run()
+    assert np.array_equal(a, b_)
+    assert np.all(np.isfinite(a))
+
+
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+def test_single_token_heads_return_value_row(kernel):
+    case = synth.dense_case(2, 16, 4, 128, [50, 70], [[1, 1, 50, 1], [1, 70, 1, 5]], "bf16",
+                            seed=5, head_group=[0, 0, 1, 0])
+    got = DeviceCase(case, make_plan(case, num_ctas=3, kernel=kernel)).run()
+    g = case.Hq // case.Hkv
+    for b in range(case.B):
+        for h in range(case.Hkv):
+            if case.n[b, h] == 1:
+                t = case.kept[b * case.Hkv + h][0]
+                for j in range(h * g, (h + 1) * g):
+                    assert np.array_equal(got[b, j], case.v[b, h, t].astype(np.float64))
+
+
+def test_device_flags_budget_mismatch():
+    case = qwen3_like(6)
+    dev = DeviceCase(case, make_plan(case))
+    bad = dev.budget.clone()
+    bad[5] = 1
+    dev.run(budget=bad)
+    assert dev.status() & kvx.KVX_DEV_BAD_BUDGET
+    kvx.kvx_workspace_clear(dev.ws)
+    torch.cuda.synchronize()
+    dev.run()
+    assert dev.status() == 0
+
+
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+def test_device_flags_page_outside_pool(kernel):
+    """A page id past the pool is read as zeros and flagged; nothing faults."""
+    case = qwen3_like(7)
+    dev = DeviceCase(case, make_plan(case, kernel=kernel))
+    pt = dev.pt[0]
+    pt[0, 0] = dev.pool_pages[0] + 7
+    got = dev.run()
+    assert dev.status() & kvx.KVX_DEV_BAD_PAGE
+    assert np.all(np.isfinite(got))
+
+
+def test_custom_scale():
+    case = d64_bf16(8)
+    dev = DeviceCase(case, make_plan(case))
+    got = dev.run(scale=0.05)
+    assert max_abs(got, oracle_out(case, scale=0.05)) <= TOL_BF16

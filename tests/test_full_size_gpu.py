@@ -1,0 +1,96 @@
+"""Full-size workloads in the launch configuration the benchmark times
+(balanced plan, one persistent block per SM, tensor-core kernel), checked on
+sampled heads against the fp64 oracle one head at a time."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from synth.device import TableLayer, ValueTable
+from paged_non_uniform_gb300 import kvx
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-3
+
+
+@pytest.fixture(scope="module")
+def table():
+    return ValueTable(seed=11, rows=1 << 19, D=128, dtype="bf16")
+
+
+def _plan(cfg, layer):
+    plan = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                               kvx.KVX_BF16, cfg.budget[layer], cfg.seq_len,
+                               cfg.head_group[layer])
+    kvx.kvx_plan_upload(plan)
+    return plan
+
+
+def _run(plan, lay, cfg):
+    out = torch.full((cfg.B, cfg.Hq, cfg.D), float("nan"), device="cuda")
+    ws = torch.zeros(plan.workspace_bytes() // 4 + 64, dtype=torch.int32, device="cuda")
+    kvx.kvx_decode_attn(plan, lay.q, lay.k_pools, lay.v_pools, lay.pool_pages, lay.pt,
+                        lay.strides, lay.budget, lay.seq_len, 0.0, out, ws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == 0
+    return out.cpu().numpy().astype(np.float64)
+
+
+def _sample_heads(cfg, layer, k, seed):
+    g = synth.rng(seed)
+    heads = {tuple(int(x) for x in np.unravel_index(np.argmax(cfg.n[layer]), cfg.n[layer].shape)),
+             tuple(int(x) for x in np.unravel_index(np.argmin(cfg.n[layer]), cfg.n[layer].shape))}
+    while len(heads) < k:
+        heads.add((int(g.integers(cfg.B)), int(g.integers(cfg.Hkv))))
+    return sorted(heads)
+
+
+@pytest.mark.parametrize("name", ["qwen3_4b", "qwen3_4b_32k", "qwen25_32b"])
+def test_full_size_sampled_heads(name, table):
+    cfg = synth.decode_config(name, seed=0, layers=1)
+    plan = _plan(cfg, 0)
+    lay = TableLayer(cfg, 0, table, plan.group_pages(), seed=0)
+    got = _run(plan, lay, cfg)
+    assert np.all(np.isfinite(got))
+    orc = oracle.load()
+    g = cfg.Hq // cfg.Hkv
+    for b, h in _sample_heads(cfg, 0, 6, seed=1):
+        k, v = lay.host_kv(b, h)
+        ref = orc.attn_head(lay.q_host[b, h * g:(h + 1) * g], k, v,
+                            np.arange(k.shape[0], dtype=np.int32), 1.0 / math.sqrt(cfg.D))
+        err = float(np.abs(got[b, h * g:(h + 1) * g] - ref).max())
+        assert err <= TOL, (b, h, err)
+
+
+def test_full_size_sparse_with_selected_tokens(table):
+    """Llama-3-8B shapes, batch 8 x 122k: sampled heads keep the top 2048
+    tokens by score plus the 128 most recent, selected from dense keys."""
+    cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
+    plan = _plan(cfg, 0)
+    lay = TableLayer(cfg, 0, table, plan.group_pages(), seed=0)
+    g = cfg.Hq // cfg.Hkv
+    L = int(cfg.seq_len[0])
+    dense = {}
+    for b, h in [(0, 0), (3, 5), (7, 7)]:
+        gen = synth.rng(5000 + b * cfg.Hkv + h)
+        K = synth.normal(gen, (L, cfg.D), "bf16")
+        V = synth.normal(gen, (L, cfg.D), "bf16")
+        qh = lay.q_host[b, h * g:(h + 1) * g]
+        kept = synth.select_top_recent(qh, K, 2048, 128)
+        assert kept.size == cfg.n[0][b, h] == 2176
+        ids = torch.from_numpy(lay.pool_row_ids(b, h)).cuda()
+        gi = int(cfg.head_group[0][h])
+        for pool, src in ((lay.k_pools[gi], K), (lay.v_pools[gi], V)):
+            rows = torch.from_numpy(synth.f32_to_bf16_bits(src[kept]).view(np.int16)).view(
+                torch.bfloat16).cuda()
+            pool.view(-1, cfg.D).index_copy_(0, ids, rows)
+        dense[(b, h)] = (qh, K, V, kept)
+    got = _run(plan, lay, cfg)
+    orc = oracle.load()
+    for (b, h), (qh, K, V, kept) in dense.items():
+        ref = orc.attn_head(qh, K, V, kept, 1.0 / math.sqrt(cfg.D))
+        err = float(np.abs(got[b, h * g:(h + 1) * g] - ref).max())
+        assert err <= TOL, (b, h, err)
