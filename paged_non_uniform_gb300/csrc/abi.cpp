@@ -38,18 +38,20 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A 2-D bf16 tensor map over a pool viewed as [rows][D], box = 64 elements
-// (128 bytes, the swizzle span) x box_rows rows, 128-byte swizzle, zero fill
-// out of bounds.
+// A 3-D bf16 tensor map over a pool of rows of D elements, viewed as
+// {64 elements, rows, D/64 halves} with strides {2 B, D*2 B, 128 B}: one box
+// {64, box_rows, D/64} fetches box_rows whole rows and lands in shared memory
+// as [half][row][128 B], 128-byte swizzled, zero-filled out of bounds.
 static bool encode_pool_map(CUtensorMap *tm, const void *base, int64_t rows,
                             int D, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+  const cuuint32_t halves = (cuuint32_t)(D / 64);
+  cuuint64_t dims[3] = {64u, (cuuint64_t)rows, halves};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, halves};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -13,7 +13,9 @@
 //    table (Fig. 8(b)) and issues bulk-tensor loads of each page slot's K and
 //    V rows (token-major, 128-byte swizzled, two 64-element halves of a row)
 //    into a ring of 32-token stages, completing on per-stage mbarriers;
-//  * kCons consumer warps take the stages round-robin. Per stage a warp
+//  * kCons consumer warps take the stages round-robin (ring slot s always
+//    belongs to warp s % kCons, so each warp sees its slots' mbarrier phases
+//    in order). Per stage a warp
 //    computes S^T = K Q^T on m16n8k16 bf16 MMAs (16 tokens x 8 query columns;
 //    GQA query heads of one KV head are the columns), runs the online softmax
 //    on the accumulator fragments (column max by three shuffles), transposes
@@ -33,9 +35,28 @@
 namespace kvx {
 namespace {
 
-constexpr int kCons = 4;       // consumer warps
-constexpr int kStages = 10;    // ring depth (32-token stages)
+// Tuning knobs (compile-time).
+#ifndef KVX_ATTN_CONS
+#define KVX_ATTN_CONS 4          // consumer warps per block
+#endif
+#ifndef KVX_ATTN_STAGES
+#define KVX_ATTN_STAGES 4        // ring depth, in 32-token stages
+#endif
+#ifndef KVX_ATTN_CTAS_PER_SM
+#define KVX_ATTN_CTAS_PER_SM 2   // resident blocks per SM
+#endif
+#ifndef KVX_TMA_LANES
+#define KVX_TMA_LANES 1          // issue a stage's boxes from separate lanes
+#endif
+constexpr int kCons = KVX_ATTN_CONS;
+constexpr int kStages = KVX_ATTN_STAGES;
 constexpr uint64_t kWaitNs = 2000000000ull;
+// Stage gs goes to consumer warp gs % kCons and ring slot gs % kStages. With
+// kStages a multiple of kCons every slot belongs to one warp, which waits on
+// that slot's phases strictly in order. Otherwise a warp could wait for phase
+// k of a slot while another warp's phase k-1 is still loading; a parity wait
+// cannot tell those phases apart and would pass early.
+static_assert(kStages % kCons == 0, "each ring slot must belong to one consumer warp");
 
 template <int D>
 struct Cfg {
@@ -48,30 +69,60 @@ struct Cfg {
       1024 + kStages * kStage + 2 * kCons * kMW * 4 + 2 * kStages * 8 + 16;
 };
 
-// Byte offset, inside a stage's K or V tile, of 16-byte chunk `gc` (0..D/8-1)
-// of token row `tok` (0..31): halves are [32 tokens][128 B] blocks and the
-// chunk index is XOR-swizzled with the token's low 3 bits (128B swizzle).
-__device__ __forceinline__ uint32_t tile_off(int tok, int gc) {
-  return (uint32_t)((gc >> 3) * (kStageTokens * 128) + tok * 128 +
-                    (((gc & 7) ^ (tok & 7)) << 4));
+// Shared-memory layout of a stage's K (or V) tile: the stage's 32 tokens
+// come in boxes of `box_h` tokens (one bulk-tensor load each, box_h = min(P,
+// 32)); box b holds [half][box_h rows][128 B] with the row's 16-byte chunks
+// XOR-swizzled by the token's low 3 bits (128-byte swizzle). Every box and
+// half starts on a 1024-byte boundary, so the swizzle key of a row is tok & 7.
+// Row part of the offset of token `tok`:
+__device__ __forceinline__ uint32_t row_off(int tok, int lb, int halves) {
+  return (uint32_t)(((tok >> lb) << (lb + 7)) * halves + ((tok & ((1 << lb) - 1)) << 7));
+}
+
+// Per-lane ldmatrix addressing of one stage, fixed for the whole kernel.
+struct LaneAddr {
+  uint32_t krow[2], vrow[2];  // row offsets for the two 16-token m-tiles
+  uint32_t half;              // bytes between the two 64-element halves
+  int ksel, vsel, key;        // chunk parity of this lane's matrix, swizzle key
+};
+
+template <int D>
+__device__ __forceinline__ LaneAddr lane_addr(int lane, int lb) {
+  constexpr int H = D / 64;
+  const int mi = lane >> 3, lr = lane & 7;
+  LaneAddr a;
+#pragma unroll
+  for (int mt = 0; mt < 2; ++mt) {
+    a.krow[mt] = row_off(mt * 16 + (mi & 1) * 8 + lr, lb, H);
+    a.vrow[mt] = row_off(mt * 16 + (mi >> 1) * 8 + lr, lb, H);
+  }
+  a.half = 1u << (lb + 7);
+  a.ksel = mi >> 1;
+  a.vsel = mi & 1;
+  a.key = lr;
+  return a;
+}
+
+// Offset of 16-byte chunk pair index `j` (dims 16j .. 16j+15), chunk `sel`.
+__device__ __forceinline__ uint32_t chunk_off(const LaneAddr &a, int j, int sel) {
+  return (uint32_t)(j >> 2) * a.half + ((uint32_t)(((2 * j) & 7) + sel) ^ (uint32_t)a.key) * 16u;
 }
 
 template <int D>
 __device__ __forceinline__ void consume_stage(
-    uint32_t kbase, uint32_t vbase, int valid, const uint32_t (&qf)[D / 16][2],
-    float (&o)[D / 16][4], float &m0, float &m1, float &l0, float &l1,
-    float sl2, int lane) {
+    uint32_t kbase, uint32_t vbase, const LaneAddr &la, int valid,
+    const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4], float &m0, float &m1,
+    float &l0, float &l1, float sl2, int lane) {
   constexpr int NK = D / 16;
-  const int r = lane >> 2, c = lane & 3, mi = lane >> 3, lr = lane & 7;
+  const int r = lane >> 2, c = lane & 3;
   float s[2][4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
     s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
-    const int tok = mt * 16 + (mi & 1) * 8 + lr;
 #pragma unroll
     for (int j = 0; j < NK; ++j) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4(kbase + tile_off(tok, 2 * j + (mi >> 1)), a0, a1, a2, a3);
+      ldsm_x4(kbase + la.krow[mt] + chunk_off(la, j, la.ksel), a0, a1, a2, a3);
       mma_bf16(s[mt], a0, a1, a2, a3, qf[j][0], qf[j][1]);
     }
   }
@@ -137,7 +188,6 @@ __device__ __forceinline__ void consume_stage(
   const bool tail = valid < kStageTokens;
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
-    const int tok = mt * 16 + (mi >> 1) * 8 + lr;
     // tokens held by this lane in the V^T fragment (for tail masking)
     const int t0 = mt * 16 + 2 * c;
     const uint32_t k01 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
@@ -145,7 +195,7 @@ __device__ __forceinline__ void consume_stage(
 #pragma unroll
     for (int dm = 0; dm < NK; ++dm) {
       uint32_t a0, a1, a2, a3;
-      ldsm_x4_t(vbase + tile_off(tok, 2 * dm + (mi & 1)), a0, a1, a2, a3);
+      ldsm_x4_t(vbase + la.vrow[mt] + chunk_off(la, dm, la.vsel), a0, a1, a2, a3);
       if (tail) {  // rows past the valid tokens may hold stale or padding data
         a0 &= k01;
         a1 &= k01;
@@ -159,7 +209,7 @@ __device__ __forceinline__ void consume_stage(
 }
 
 template <int D>
-__global__ void __launch_bounds__((kCons + 1) * 32, 1)
+__global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     attn_mma_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -190,7 +240,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, 1)
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
     const int box_h = P < kStageTokens ? P : kStageTokens;
-    const uint32_t box_bytes = (uint32_t)box_h * 128u;
+    const uint32_t box_bytes = (uint32_t)box_h * 128u * C::kHalves;
     int gs = 0;
     bool dead = false;
     for (int it = it0; it < it1 && !dead; ++it) {
@@ -231,27 +281,32 @@ __global__ void __launch_bounds__((kCons + 1) * 32, 1)
           }
         }
         const uint32_t full = full0 + 8 * slot;
-        if (lane == 0)
-          mbar_arrive_expect_tx(full, (uint32_t)nbox * box_bytes * C::kHalves * 2u);
+        if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nbox * box_bytes * 2u);
+        __syncwarp();
         const uint32_t kdst = stage0 + slot * C::kStage;
+#if KVX_TMA_LANES
+        {
+          const int i = lane < nbox ? lane : 0;
+#else
         for (int i = 0; i < nbox; ++i) {
+#endif
           const int tb = t0 + i * box_h;
           const int32_t page = __shfl_sync(0xffffffffu, my_page, tb / P - win);
-          int y;
-          if (page < 0 || (int64_t)page >= gd.num_pages) {
-            if (lane == 0) atomicOr(p.status, KVX_DEV_BAD_PAGE);
-            y = rows_ext;  // whole box past the end: loads zeros
-          } else {
-            y = (page * gd.size + row) * P + (tb & (P - 1));
-          }
+#if KVX_TMA_LANES
+          if (lane < nbox) {
+#else
           if (lane == 0) {
-            const uint32_t d = kdst + (uint32_t)(i * box_h) * 128u;
-#pragma unroll
-            for (int hf = 0; hf < C::kHalves; ++hf) {
-              tma_load_2d(d + hf * kStageTokens * 128, tmk, hf * 64, y, full, pol);
-              tma_load_2d(d + C::kTile + hf * kStageTokens * 128, tmv, hf * 64, y,
-                          full, pol);
+#endif
+            int y;
+            if (page < 0 || (int64_t)page >= gd.num_pages) {
+              atomicOr(p.status, KVX_DEV_BAD_PAGE);
+              y = rows_ext;  // whole box past the end: loads zeros
+            } else {
+              y = (page * gd.size + row) * P + (tb & (P - 1));
             }
+            const uint32_t d = kdst + (uint32_t)i * box_bytes;
+            tma_load_3d(d, tmk, 0, y, 0, full, pol);
+            tma_load_3d(d + C::kTile, tmv, 0, y, 0, full, pol);
           }
         }
       }
@@ -270,6 +325,8 @@ __global__ void __launch_bounds__((kCons + 1) * 32, 1)
     constexpr int NK = D / 16;
     const int r = lane >> 2, c = lane & 3;
     const float sl2 = p.scale_log2;
+    const int box_h = P < kStageTokens ? P : kStageTokens;
+    const LaneAddr la = lane_addr<D>(lane, 31 - __clz(box_h));
     int gs = 0;
     bool dead = false;
     for (int it = it0; it < it1; ++it) {
@@ -315,7 +372,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, 1)
         }
         const int valid = min(kStageTokens, item.end - (item.begin + st * kStageTokens));
         const uint32_t kb = stage0 + slot * C::kStage;
-        consume_stage<D>(kb, kb + C::kTile, valid, qf, o, m0, m1, l0, l1, sl2, lane);
+        consume_stage<D>(kb, kb + C::kTile, la, valid, qf, o, m0, m1, l0, l1, sl2, lane);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * slot);
       }
@@ -394,6 +451,8 @@ cudaError_t launch_d(const AttnParams &p, int num_ctas, cudaStream_t st) {
 }
 
 }  // namespace
+
+int attn_mma_ctas_per_sm() { return KVX_ATTN_CTAS_PER_SM; }
 
 cudaError_t launch_attn_mma(const AttnParams &p, int num_ctas, cudaStream_t st) {
   if (num_ctas <= 0) return cudaSuccess;

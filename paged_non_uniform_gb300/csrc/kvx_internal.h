@@ -8,7 +8,7 @@
 
 #include <vector>
 
-#include "../../include/kvx.h"
+#include "kvx.h"
 
 namespace kvx {
 
@@ -70,6 +70,7 @@ struct CombineParams {
 
 // Launchers (defined in the .cu files). Return cudaGetLastError().
 cudaError_t launch_attn_mma(const AttnParams &p, int num_ctas, cudaStream_t st);
+int attn_mma_ctas_per_sm();  // resident blocks per SM of the tensor-core kernel
 cudaError_t launch_attn_simt(const AttnParams &p, int dtype, int num_ctas,
                              cudaStream_t st);
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);

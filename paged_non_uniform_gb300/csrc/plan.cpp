@@ -235,7 +235,8 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
         pg = std::max(pg, (p->n[(size_t)b * Hkv + h] + P - 1) / P);
       }
     if (policy == KVX_PLAN_BALANCED)
-      plan_balanced(p, num_ctas > 0 ? num_ctas : sms);
+      plan_balanced(p, num_ctas > 0 ? num_ctas
+                                    : sms * (resolved == KVX_KERNEL_MMA ? attn_mma_ctas_per_sm() : 1));
     else if (policy == KVX_PLAN_PER_HEAD)
       plan_per_head(p);
     else

@@ -89,6 +89,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap,
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap,
+                                            int x, int y, int z, uint32_t bar,
+                                            uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -13,7 +13,8 @@ import os
 
 import numpy as np
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkvx.so")
+_LIB_PATH = os.environ.get("KVX_LIBRARY") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libkvx.so")
 
 KVX_OK = 0
 KVX_EINVAL = -1
