@@ -50,6 +50,7 @@ extern "C" {
 #define KVX_ECUDA (-4)        /* a CUDA runtime call failed; see kvx_last_cuda_error */
 #define KVX_EUNSUPPORTED (-5) /* head_dim / page size / dtype / GQA combination */
 #define KVX_ESTATE (-6)       /* plan used before kvx_plan_upload */
+#define KVX_ESCRATCH (-7)     /* kvx_gather_coalesce_noalloc: problem too large for its static scratch */
 
 /* ---- device status bits (workspace status word) ---------------------- */
 #define KVX_DEV_BAD_PAGE 1u    /* a page-table entry outside [0, pool_pages) */
@@ -276,6 +277,44 @@ int kvx_gather_coalesce(const int32_t *block_table, const int32_t *num_blocks,
  * {first physical block, first logical block, length in blocks}. */
 int kvx_gather_read_runs(const void *workspace, int32_t S, int32_t max_blocks,
                          int32_t *run_count, int32_t *runs);
+
+/* ---------------------------------------------------------------------------
+ * kvx_gather_coalesce_noalloc -- kvx_gather_coalesce without a workspace.
+ *
+ * The pages have no counterpart of this entry point: it exists for callers
+ * that cannot allocate device memory (code running inside host callbacks or
+ * allocator paths, runtimes that only hand out pre-planned memory, processes
+ * that keep a fixed device footprint after start-up). It computes exactly what
+ * kvx_gather_coalesce computes, with the same arguments except the workspace:
+ * its scratch (runs, prefix sums) lives in a static device array of
+ * KVX_GATHER_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the library
+ * holds until the process exits. It allocates nothing.
+ *
+ *  - Size limit: the scratch must hold kvx_gather_workspace_bytes(S,
+ *    max_blocks) bytes, about 24 * S * max_blocks + 32 * S (S = 256,
+ *    max_blocks = 1024 fits); larger problems return KVX_ESCRATCH before
+ *    anything is launched.
+ *  - status: optional device uint32 (may be NULL) into which device-detected
+ *    errors (KVX_DEV_BAD_BLOCK, KVX_DEV_BAD_LENGTH) are OR-ed; the caller
+ *    zeroes it. With NULL they are not reported.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array and clears its header on `stream` first;
+ *    calls whose work overlaps on the GPU (different streams, different
+ *    threads) race on it and must be ordered by the caller.
+ *  - Run lists are not readable afterwards (kvx_gather_read_runs needs a
+ *    caller workspace).
+ * ------------------------------------------------------------------------- */
+#define KVX_GATHER_NOALLOC_SCRATCH_BYTES (8u << 20)
+int kvx_gather_coalesce_noalloc(const int32_t *block_table,
+                                const int32_t *num_blocks, int32_t S,
+                                int32_t max_blocks, int32_t num_tensors,
+                                const void *const *pools,
+                                int64_t num_phys_blocks, int64_t block_bytes,
+                                void *const *stagings,
+                                int64_t staging_row_bytes, int32_t flags,
+                                uint32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

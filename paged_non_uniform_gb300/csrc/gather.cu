@@ -16,6 +16,8 @@
 //   copy   persistent blocks, each owns an equal share of all live blocks,
 //          walks the runs covering it and copies them contiguously;
 //   tail   (KVX_ZERO_TAIL) zero every row past its live blocks.
+#include <mutex>
+
 #include "kvx_internal.h"
 #include "ptx.cuh"
 
@@ -274,3 +276,104 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
 }
 
 }  // namespace kvx
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the gather.
+//
+// Some callers cannot call cudaMalloc: code that runs inside a host callback
+// or a custom allocator's own paths, runtimes that hand out only their own
+// pre-planned device memory, or processes that forbid allocation after
+// start-up so their memory footprint stays fixed. For them the gather's
+// scratch memory (block-table runs, prefix sums, the status word) lives in
+// this file-scope device array instead of a caller workspace. Every GPU that
+// loads the library holds it until the process exits.
+#define KVX_GATHER_STATIC_SCRATCH_BYTES KVX_GATHER_NOALLOC_SCRATCH_BYTES
+
+namespace kvx {
+namespace {
+
+static __device__ __align__(256) unsigned char g_gather_scratch[KVX_GATHER_STATIC_SCRATCH_BYTES];
+
+// Device address of g_gather_scratch on the current device, looked up once
+// per device (the array's host-side name is only a stand-in, not a device
+// address). Returns nullptr and sets *err if the lookup fails.
+void *static_scratch(cudaError_t *err) {
+  static std::mutex mu;
+  static void *addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gather_scratch);
+    if (e != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *err = cudaSuccess;
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace kvx
+
+extern "C" int kvx_gather_coalesce_noalloc(
+    const int32_t *block_table, const int32_t *num_blocks, int32_t S,
+    int32_t max_blocks, int32_t num_tensors, const void *const *pools,
+    int64_t num_phys_blocks, int64_t block_bytes, void *const *stagings,
+    int64_t staging_row_bytes, int32_t flags, uint32_t *status, void *stream) {
+  using namespace kvx;
+  if (!block_table || !num_blocks || !pools || !stagings) return KVX_EINVAL;
+  if (S < 0 || max_blocks < 0 || num_tensors < 1 || num_tensors > KVX_MAX_GATHER_TENSORS)
+    return KVX_EINVAL;
+  if (num_phys_blocks < 1 || block_bytes < 16 || block_bytes % 16 != 0 ||
+      staging_row_bytes < 0 || staging_row_bytes % 16 != 0)
+    return KVX_EINVAL;
+  if (flags & ~KVX_ZERO_TAIL) return KVX_EINVAL;
+  if (status && ((uintptr_t)status % 4) != 0) return KVX_EINVAL;
+  const GatherWs w = gather_ws_layout(S, max_blocks);
+  if (w.total > KVX_GATHER_STATIC_SCRATCH_BYTES) return KVX_ESCRATCH;
+  GatherParams p;
+  memset(&p, 0, sizeof(p));
+  for (int t = 0; t < num_tensors; ++t) {
+    if (!pools[t] || !stagings[t] || ((uintptr_t)pools[t] % 16) != 0 ||
+        ((uintptr_t)stagings[t] % 16) != 0)
+      return KVX_EINVAL;
+    p.pools[t] = pools[t];
+    p.stagings[t] = stagings[t];
+  }
+  cudaError_t e = cudaSuccess;
+  char *ws = (char *)static_scratch(&e);
+  if (!ws) return set_cuda_error(e);
+  cudaStream_t st = (cudaStream_t)stream;
+  // The array keeps the previous call's contents: clear the header (status
+  // word and totals) that the kernels accumulate into.
+  e = cudaMemsetAsync(ws, 0, KVX_WS_HEADER_BYTES, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  p.block_table = block_table;
+  p.num_blocks = num_blocks;
+  p.status = status ? status : (uint32_t *)ws;
+  p.totals = (int64_t *)(ws + 16);
+  p.run_count = (int32_t *)(ws + w.run_count);
+  p.row_blocks = (int32_t *)(ws + w.row_blocks);
+  p.run_off = (int32_t *)(ws + w.run_off);
+  p.row_bstart = (int64_t *)(ws + w.row_bstart);
+  p.runs = (int4 *)(ws + w.runs);
+  p.run_bstart = (int64_t *)(ws + w.run_bstart);
+  p.num_phys = num_phys_blocks;
+  p.block_bytes = block_bytes;
+  p.row_bytes = staging_row_bytes;
+  p.S = S;
+  p.max_blocks = max_blocks;
+  p.num_tensors = num_tensors;
+  p.flags = flags;
+  e = launch_gather(p, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return KVX_OK;
+}

@@ -99,6 +99,7 @@ struct GatherWs {
 GatherWs gather_ws_layout(int S, int max_blocks);
 
 cudaError_t launch_gather(const GatherParams &p, cudaStream_t st);
+int set_cuda_error(cudaError_t e);  // records e for kvx_last_cuda_error
 
 
 }  // namespace kvx

@@ -23,6 +23,7 @@ KVX_ENOMEM = -3
 KVX_ECUDA = -4
 KVX_EUNSUPPORTED = -5
 KVX_ESTATE = -6
+KVX_ESCRATCH = -7
 
 KVX_DEV_BAD_PAGE = 1
 KVX_DEV_BAD_BUDGET = 2
@@ -97,6 +98,9 @@ lib.kvx_gather_coalesce.argtypes = [_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32
                                     _c.c_int64, _c.c_int64, _vp, _c.c_int64, _c.c_int32, _vp,
                                     _c.c_size_t, _vp]
 lib.kvx_gather_read_runs.argtypes = [_vp, _c.c_int32, _c.c_int32, _vp, _vp]
+lib.kvx_gather_coalesce_noalloc.argtypes = [_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _vp,
+                                            _c.c_int64, _c.c_int64, _vp, _c.c_int64,
+                                            _c.c_int32, _vp, _vp]
 
 
 def kvx_status_string(status: int) -> str:
@@ -279,3 +283,18 @@ def kvx_gather_read_runs(workspace, S: int, max_blocks: int):
     _check(lib.kvx_gather_read_runs(_dptr(workspace), int(S), int(max_blocks), cnt.ctypes.data,
                                     runs.ctypes.data), "kvx_gather_read_runs")
     return cnt[:S], runs[:S]
+
+
+def kvx_gather_coalesce_noalloc(block_table, num_blocks, S, max_blocks, pools, num_phys_blocks,
+                                block_bytes, stagings, staging_row_bytes, flags, status=None,
+                                stream=None) -> None:
+    """kvx_gather_coalesce for callers that cannot allocate device memory: no
+    workspace argument; the library's static device scratch is used instead.
+    `status` is an optional device uint32/int32 tensor that collects
+    device-detected error bits."""
+    rc = lib.kvx_gather_coalesce_noalloc(_dptr(block_table), _dptr(num_blocks), int(S),
+                                         int(max_blocks), len(pools), _ptr_array(pools),
+                                         int(num_phys_blocks), int(block_bytes),
+                                         _ptr_array(stagings), int(staging_row_bytes), int(flags),
+                                         _dptr(status), _stream(stream))
+    _check(rc, "kvx_gather_coalesce_noalloc")
