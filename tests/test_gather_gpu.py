@@ -137,3 +137,36 @@ def test_full_size_gather_sampled_rows(extents):
                        np.array([ids.size], np.int32), mini, st)
             got = stagings[t][s].view(torch.uint8).cpu().numpy()
             assert np.array_equal(got, st[0]), (t, s)
+
+
+def test_medium_gather_all_rows():
+    """32 sequences, 32 KB blocks, 1 GiB pool per tensor (K and V): every row
+    bit-exact against the oracle (inputs larger than L2)."""
+    cfg = synth.gather_config(seed=7, S=32, num_phys=32768)
+    orc = oracle.load()
+    table = ValueTable(seed=23, rows=1 << 18, D=128, dtype="bf16")
+    rows_per_block = cfg.block_bytes // 256
+    pools, stagings, shifts = [], [], [5, 99991]
+    for t in range(2):
+        p = torch.empty((cfg.num_phys, cfg.block_bytes // 2), dtype=torch.bfloat16, device="cuda")
+        table.fill(p, shifts[t])
+        p.view(torch.int64)[:, 0] = torch.arange(cfg.num_phys, device="cuda", dtype=torch.int64)
+        pools.append(p)
+        stagings.append(torch.full((cfg.S, cfg.row_bytes // 2), 3.0, dtype=torch.bfloat16,
+                                   device="cuda"))
+    ws = run_gather(cfg, pools, stagings)
+    assert kvx.kvx_workspace_status(ws) == 0
+    for t in range(2):
+        got = stagings[t].view(torch.uint8).cpu().numpy()
+        for s in range(cfg.S):
+            ids = cfg.bt[s, :cfg.nb[s]]
+            blk = table.host_rows(shifts[t], (ids[:, None].astype(np.int64) * rows_per_block
+                                              + np.arange(rows_per_block)).reshape(-1))
+            blk = synth.f32_to_bf16_bits(blk).reshape(ids.size, cfg.block_bytes // 2).copy()
+            blk.view(np.int64)[:, 0] = ids
+            mini = blk.view(np.uint8).reshape(ids.size, cfg.block_bytes)
+            init = np.full((1, cfg.row_bytes // 2), 0x4040, np.uint16)  # bf16 3.0
+            ref = orc.gather(np.arange(ids.size, dtype=np.int32)[None, :],
+                             np.array([ids.size], np.int32), mini,
+                             init.view(np.uint8).reshape(1, -1).copy())
+            assert np.array_equal(got[s], ref[0]), (t, s)
