@@ -28,8 +28,9 @@
  *    out) set bits in a status word at the start of the caller's workspace
  *    (KVX_DEV_* below); the affected reads are replaced by zeros and the
  *    kernel still terminates. The word is sticky: kvx_workspace_status reads
- *    it, kvx_workspace_clear resets it. A fresh workspace must be cleared
- *    (or zero-filled) once before first use.
+ *    it, kvx_workspace_clear resets it. A fresh workspace must be zero-filled
+ *    (kvx_workspace_clear over its whole size) once before first use, and
+ *    again after a call that reported KVX_DEV_TIMEOUT.
  *  - All layouts are dense row-major C arrays, outermost index first.
  */
 #ifndef KVX_H
@@ -156,8 +157,9 @@ int kvx_plan_create(const kvx_shape *shape, const int32_t *head_budget,
  * memory; call once, outside any hot loop). Stream-ordered on `stream`. */
 int kvx_plan_upload(kvx_plan *plan, void *stream);
 
-/* Bytes of device workspace kvx_decode_attn needs with this plan:
- * a KVX_WS_HEADER_BYTES header (status word) plus the split partials. */
+/* Bytes of device workspace kvx_decode_attn needs with this plan: a
+ * KVX_WS_HEADER_BYTES header (status word), one counter per split head and
+ * the split partials. The counters return to zero at the end of every call. */
 int kvx_plan_workspace_bytes(const kvx_plan *plan, size_t *bytes);
 
 int kvx_plan_get_stats(const kvx_plan *plan, kvx_plan_stats *stats);
@@ -194,7 +196,8 @@ void kvx_plan_destroy(kvx_plan *plan);
  *     s_t = scale * <q[b][j], k_t>,   out[b][j] = sum_t softmax(s)_t * v_t.
  * (Tangram, Fig. 2: attention over each head's kept tokens; the split-K
  * partials of a cut head are merged by log-sum-exp, which leaves the result
- * unchanged up to rounding.)
+ * unchanged up to rounding. The merge runs inside the same kernel launch, in
+ * the block that finishes the head's last piece, in a fixed order.)
  *
  * Head-group page addressing (Tangram, Fig. 8(b)): head h belongs to group
  * G = head_group[h] and has row r = its rank within G. Its t-th kept token is
@@ -232,8 +235,10 @@ int kvx_decode_attn(const kvx_plan *plan, const void *q,
 /* Reads the workspace status word (synchronous device-to-host copy). */
 int kvx_workspace_status(const void *workspace, uint32_t *status);
 
-/* Zeroes the workspace status word (stream-ordered). */
-int kvx_workspace_clear(void *workspace, void *stream);
+/* Zeroes the first `bytes` bytes of a workspace (stream-ordered): pass the
+ * whole workspace size before first use; KVX_WS_HEADER_BYTES clears only the
+ * status word. bytes >= KVX_WS_HEADER_BYTES. */
+int kvx_workspace_clear(void *workspace, size_t bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * kvx_gather_coalesce -- KV-RM movement step.

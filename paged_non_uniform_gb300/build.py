@@ -16,8 +16,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libkvx.so")
-SOURCES = ["plan.cpp", "abi.cpp", "attn_mma.cu", "attn_simt.cu", "combine.cu", "gather.cu"]
+SOURCES = ["plan.cpp", "abi.cpp", "attn_mma.cu", "attn_simt.cu", "gather.cu"]
 HEADERS = [os.path.join(CSRC, "kvx_internal.h"), os.path.join(CSRC, "ptx.cuh"),
+           os.path.join(CSRC, "split_merge.cuh"),
            os.path.join(ROOT, "include", "kvx.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

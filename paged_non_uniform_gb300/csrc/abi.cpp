@@ -135,18 +135,19 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   }
   const int g = s.Hq / s.Hkv;
   char *ws = (char *)workspace;
-  const size_t ml_bytes =
-      ((size_t)plan->num_slots * g * sizeof(float2) + 255) & ~size_t(255);
+  const AttnWs lay = attn_ws_layout(plan);
   p.items = plan->d_items;
   p.cta_off = plan->d_cta_off;
+  p.split = plan->d_split;
+  p.counters = (int32_t *)(ws + lay.counters);
   p.n_plan = plan->d_n;
   p.head_budget = head_budget;
   p.seq_len = seq_len;
   p.q = q;
   p.out = out;
   p.status = (uint32_t *)ws;
-  p.part_ml = (float2 *)(ws + KVX_WS_HEADER_BYTES);
-  p.part_o = (float *)(ws + KVX_WS_HEADER_BYTES + ml_bytes);
+  p.part_ml = (float2 *)(ws + lay.part_ml);
+  p.part_o = (float *)(ws + lay.part_o);
   p.trace = plan->d_trace;
   p.B = B;
   p.Hq = s.Hq;
@@ -162,20 +163,6 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
                       ? launch_attn_mma(p, plan->num_ctas, st)
                       : launch_attn_simt(p, s.dtype, plan->num_ctas, st);
   if (e != cudaSuccess) return set_cuda_error(e);
-  if (!plan->split_heads.empty()) {
-    CombineParams cp;
-    cp.heads = plan->d_split;
-    cp.part_o = p.part_o;
-    cp.part_ml = p.part_ml;
-    cp.out = out;
-    cp.num_heads = (int32_t)plan->split_heads.size();
-    cp.Hkv = s.Hkv;
-    cp.Hq = s.Hq;
-    cp.g = g;
-    cp.D = D;
-    e = launch_combine(cp, st);
-    if (e != cudaSuccess) return set_cuda_error(e);
-  }
   return KVX_OK;
 }
 
@@ -186,9 +173,9 @@ extern "C" int kvx_workspace_status(const void *workspace, uint32_t *status) {
   return KVX_OK;
 }
 
-extern "C" int kvx_workspace_clear(void *workspace, void *stream) {
-  if (!workspace) return KVX_EINVAL;
-  cudaError_t e = cudaMemsetAsync(workspace, 0, KVX_WS_HEADER_BYTES, (cudaStream_t)stream);
+extern "C" int kvx_workspace_clear(void *workspace, size_t bytes, void *stream) {
+  if (!workspace || bytes < KVX_WS_HEADER_BYTES) return KVX_EINVAL;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream);
   if (e != cudaSuccess) return set_cuda_error(e);
   return KVX_OK;
 }

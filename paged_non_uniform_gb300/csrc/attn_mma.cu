@@ -23,7 +23,9 @@
 //    V^T fragments read by ldmatrix.trans. P is split into a bf16 high part
 //    and a bf16 residual, so the product keeps ~16 bits of P;
 //  * at the end of an item the consumer warps merge their (m, l, O) in shared
-//    memory and write the output or the partial.
+//    memory and write the output or, for a head cut into pieces, the piece's
+//    partial; the block that completes a head's last piece then merges all its
+//    partials (split_merge.cuh).
 // No spin-wait is unbounded: every mbarrier wait gives up after kWaitNs and
 // sets KVX_DEV_TIMEOUT. Pages outside the pool are loaded as zeros (the box
 // is placed past the tensor's end) and set KVX_DEV_BAD_PAGE.
@@ -31,6 +33,7 @@
 
 #include "kvx_internal.h"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace kvx {
 namespace {
@@ -218,6 +221,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   float *merge = (float *)(smem + kStages * C::kStage);
   uint64_t *bars = (uint64_t *)(merge + 2 * kCons * C::kMW);
   volatile int *abort_flag = (volatile int *)(bars + 2 * kStages);
+  volatile int *last_flag = abort_flag + 1;
   const uint32_t stage0 = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
 
@@ -416,6 +420,20 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
         } else {
           p.part_o[((size_t)item.slot * g + qi) * D + d] = O;
           if (d == 0) p.part_ml[(size_t)item.slot * g + qi] = make_float2(M, Ls);
+        }
+      }
+      if (item.slot >= 0) {
+        // Publish this piece; the block that finishes the head's last piece
+        // merges all of them and rearms the counter for the next call.
+        __threadfence();
+        consumer_sync(kCons * 32);
+        if (tid == 0)
+          *last_flag = atomicAdd(p.counters + item.split, 1) == p.split[item.split].count - 1;
+        consumer_sync(kCons * 32);
+        if (*last_flag) {
+          __threadfence();
+          merge_split<D, kCons * 32>(p, p.split[item.split], tid);
+          if (tid == 0) p.counters[item.split] = 0;
         }
       }
     }

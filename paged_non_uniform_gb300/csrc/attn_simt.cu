@@ -7,13 +7,15 @@
 // warps per block; warp w takes tokens begin+w, begin+w+4, ... of an item;
 // the 32 lanes of a warp split the head dimension, reduce the g dot products
 // with shuffles and run the online softmax per query head. The warps' states
-// are merged in shared memory at the end of each item. Page ids outside the
+// are merged in shared memory at the end of each item; split heads are merged
+// by the block that finishes their last piece. Page ids outside the
 // pool read as zero rows and set KVX_DEV_BAD_PAGE.
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include "kvx_internal.h"
 #include "ptx.cuh"
+#include "split_merge.cuh"
 
 namespace kvx {
 namespace {
@@ -37,6 +39,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr int DL = D / 32;
   constexpr int MW = 8 * D + 16;  // floats per warp record
   __shared__ float merge[2][kWarps][MW];
+  __shared__ int last_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int it0 = p.cta_off[blockIdx.x], it1 = p.cta_off[blockIdx.x + 1];
   const int g = p.g, P = p.P;
@@ -127,6 +130,18 @@ __global__ void __launch_bounds__(kWarps * 32)
       } else {
         p.part_o[((size_t)item.slot * g + qi) * D + d] = O;
         if (d == 0) p.part_ml[(size_t)item.slot * g + qi] = make_float2(M, Ls);
+      }
+    }
+    if (item.slot >= 0) {
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0)
+        last_flag = atomicAdd(p.counters + item.split, 1) == p.split[item.split].count - 1;
+      __syncthreads();
+      if (last_flag) {
+        __threadfence();
+        merge_split<D, kWarps * 32>(p, p.split[item.split], threadIdx.x);
+        if (threadIdx.x == 0) p.counters[item.split] = 0;
       }
     }
   }

@@ -10,6 +10,8 @@
 
 #include "kvx.h"
 
+struct kvx_plan;
+
 namespace kvx {
 
 // Tokens one pipeline stage of the attention kernels covers (a multiple of
@@ -17,10 +19,12 @@ namespace kvx {
 constexpr int kStageTokens = 32;
 
 // One work item: tokens [begin, end) of head bh = b*Hkv + h. slot >= 0 names
-// the partial-result slot of a split head; slot < 0 means the item covers the
-// whole head and writes the final output.
-struct Item {
+// the partial-result slot of a split head and split its index in the plan's
+// split-head list; slot < 0 means the item covers the whole head and writes
+// the final output.
+struct alignas(16) Item {
   int32_t bh, begin, end, slot;
+  int32_t split, pad0, pad1, pad2;
 };
 
 // A split head: its partials occupy slots [slot_begin, slot_begin + count).
@@ -45,6 +49,8 @@ struct alignas(128) AttnParams {
   GroupDesc grp[KVX_MAX_GROUPS];
   const Item *items;
   const int32_t *cta_off;
+  const SplitHead *split;      // [split heads]
+  int32_t *counters;           // [split heads] finished pieces, back to 0 after the merge
   const int32_t *n_plan;       // [B*Hkv]
   const int32_t *head_budget;  // [B*Hkv] device, for the plan check
   const int32_t *seq_len;      // [B] device
@@ -60,20 +66,11 @@ struct alignas(128) AttnParams {
   int8_t head_row[KVX_MAX_KV_HEADS];
 };
 
-struct CombineParams {
-  const SplitHead *heads;
-  const float *part_o;
-  const float2 *part_ml;
-  float *out;
-  int32_t num_heads, Hkv, Hq, g, D;
-};
-
 // Launchers (defined in the .cu files). Return cudaGetLastError().
 cudaError_t launch_attn_mma(const AttnParams &p, int num_ctas, cudaStream_t st);
 int attn_mma_ctas_per_sm();  // resident blocks per SM of the tensor-core kernel
 cudaError_t launch_attn_simt(const AttnParams &p, int dtype, int num_ctas,
                              cudaStream_t st);
-cudaError_t launch_combine(const CombineParams &p, cudaStream_t st);
 
 struct GatherParams {
   const int32_t *block_table;  // [S][max_blocks]
@@ -91,6 +88,13 @@ struct GatherParams {
   int64_t num_phys, block_bytes, row_bytes;
   int32_t S, max_blocks, num_tensors, flags;
 };
+
+// Workspace layout of decode attention (offsets in bytes from its start):
+// header (status word) | split-head counters | partial (m, l) | partial o.
+struct AttnWs {
+  size_t counters, part_ml, part_o, total;
+};
+AttnWs attn_ws_layout(const kvx_plan *plan);
 
 // Workspace layout of the gather (offsets in bytes from the workspace start).
 struct GatherWs {

@@ -29,11 +29,12 @@ static void finish_splits(kvx_plan *p) {
   const int H = p->shape.B * p->shape.Hkv;
   std::vector<int32_t> count(H, 0);
   for (const Item &it : p->items) count[it.bh]++;
-  std::vector<int32_t> first(H, -1);
+  std::vector<int32_t> first(H, -1), split_of(H, -1);
   int32_t slots = 0;
   for (int bh = 0; bh < H; ++bh) {
     if (count[bh] > 1) {
       first[bh] = slots;
+      split_of[bh] = (int32_t)p->split_heads.size();
       p->split_heads.push_back(SplitHead{bh, slots, count[bh], 0});
       slots += count[bh];
     }
@@ -49,8 +50,15 @@ static void finish_splits(kvx_plan *p) {
   for (size_t i : order) {
     Item &it = p->items[i];
     it.slot = count[it.bh] > 1 ? next[it.bh]++ : -1;
+    it.split = split_of[it.bh];
   }
   p->num_slots = slots;
+  // Inside each block, run the pieces of split heads first: the block that
+  // finishes a head's last piece merges its partials, and doing that early
+  // keeps the merges off the end of the kernel, behind ongoing streaming.
+  for (int c = 0; c < p->num_ctas; ++c)
+    std::stable_partition(p->items.begin() + p->cta_off[c], p->items.begin() + p->cta_off[c + 1],
+                          [&](const Item &it) { return count[it.bh] > 1; });
   p->cta_tokens.assign(p->num_ctas, 0);
   for (int c = 0; c < p->num_ctas; ++c)
     for (int i = p->cta_off[c]; i < p->cta_off[c + 1]; ++i)
@@ -83,7 +91,7 @@ static void plan_balanced(kvx_plan *p, int num_ctas) {
       const int rem = n - pos;
       const double cap = (cta + 1) * per - used;
       if (cta == num_ctas - 1 || cap >= rem + c0) {
-        p->items.push_back(Item{bh, pos, n, -1});
+        p->items.push_back(Item{bh, pos, n, -1, -1, 0, 0, 0});
         used += rem + c0;
         pos = n;
         continue;
@@ -91,7 +99,7 @@ static void plan_balanced(kvx_plan *p, int num_ctas) {
       int k = (int)std::floor((cap - c0) / T) * T;
       if (k >= T) {
         if (rem - k < T) k = rem;  // never leave a sliver behind
-        p->items.push_back(Item{bh, pos, pos + k, -1});
+        p->items.push_back(Item{bh, pos, pos + k, -1, -1, 0, 0, 0});
         used += k + c0;
         pos += k;
         if (pos < n) close_cta();
@@ -109,7 +117,7 @@ static void plan_per_head(kvx_plan *p) {
   const int H = p->shape.B * p->shape.Hkv;
   p->cta_off.assign(1, 0);
   for (int bh = 0; bh < H; ++bh) {
-    p->items.push_back(Item{bh, 0, p->n[bh], -1});
+    p->items.push_back(Item{bh, 0, p->n[bh], -1, -1, 0, 0, 0});
     p->cta_off.push_back((int32_t)p->items.size());
   }
   p->num_ctas = H;
@@ -126,7 +134,7 @@ static void plan_uniform(kvx_plan *p, int sms) {
     int chunk = (n + splits - 1) / splits;
     chunk = ((chunk + T - 1) / T) * T;
     for (int b0 = 0; b0 < n; b0 += chunk) {
-      p->items.push_back(Item{bh, b0, std::min(n, b0 + chunk), -1});
+      p->items.push_back(Item{bh, b0, std::min(n, b0 + chunk), -1, -1, 0, 0, 0});
       p->cta_off.push_back((int32_t)p->items.size());
     }
   }
@@ -292,12 +300,21 @@ extern "C" int kvx_plan_upload(kvx_plan *p, void *stream) {
   return KVX_OK;
 }
 
-extern "C" int kvx_plan_workspace_bytes(const kvx_plan *p, size_t *bytes) {
-  if (!p || !bytes) return KVX_EINVAL;
+AttnWs kvx::attn_ws_layout(const kvx_plan *p) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   const size_t g = (size_t)(p->shape.Hq / p->shape.Hkv);
   const size_t slots = (size_t)p->num_slots;
-  size_t ml = (slots * g * sizeof(float2) + 255) & ~size_t(255);
-  *bytes = KVX_WS_HEADER_BYTES + ml + slots * g * p->shape.D * sizeof(float);
+  AttnWs w;
+  w.counters = KVX_WS_HEADER_BYTES;
+  w.part_ml = al(w.counters + 4 * p->split_heads.size());
+  w.part_o = al(w.part_ml + slots * g * sizeof(float2));
+  w.total = w.part_o + slots * g * p->shape.D * sizeof(float);
+  return w;
+}
+
+extern "C" int kvx_plan_workspace_bytes(const kvx_plan *p, size_t *bytes) {
+  if (!p || !bytes) return KVX_EINVAL;
+  *bytes = attn_ws_layout(p).total;
   return KVX_OK;
 }
 
@@ -343,7 +360,12 @@ extern "C" int kvx_plan_group_pages(const kvx_plan *p, int32_t *pages) {
 extern "C" int kvx_plan_items(const kvx_plan *p, int32_t *items,
                               int32_t *cta_off) {
   if (!p || !items || !cta_off) return KVX_EINVAL;
-  std::memcpy(items, p->items.data(), p->items.size() * sizeof(Item));
+  for (size_t i = 0; i < p->items.size(); ++i) {
+    items[4 * i + 0] = p->items[i].bh;
+    items[4 * i + 1] = p->items[i].begin;
+    items[4 * i + 2] = p->items[i].end;
+    items[4 * i + 3] = p->items[i].slot;
+  }
   std::memcpy(cta_off, p->cta_off.data(), p->cta_off.size() * sizeof(int32_t));
   return KVX_OK;
 }

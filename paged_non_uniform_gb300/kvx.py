@@ -92,7 +92,7 @@ lib.kvx_plan_destroy.restype = None
 lib.kvx_decode_attn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c.c_float, _vp,
                                 _vp, _c.c_size_t, _vp]
 lib.kvx_workspace_status.argtypes = [_vp, _c.POINTER(_c.c_uint32)]
-lib.kvx_workspace_clear.argtypes = [_vp, _vp]
+lib.kvx_workspace_clear.argtypes = [_vp, _c.c_size_t, _vp]
 lib.kvx_gather_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.POINTER(_c.c_size_t)]
 lib.kvx_gather_coalesce.argtypes = [_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _vp,
                                     _c.c_int64, _c.c_int64, _vp, _c.c_int64, _c.c_int32, _vp,
@@ -253,8 +253,12 @@ def kvx_workspace_status(workspace) -> int:
     return int(v.value)
 
 
-def kvx_workspace_clear(workspace, stream=None) -> None:
-    _check(lib.kvx_workspace_clear(_dptr(workspace), _stream(stream)), "kvx_workspace_clear")
+def kvx_workspace_clear(workspace, nbytes=None, stream=None) -> None:
+    """Zero the first `nbytes` bytes of a workspace (default: all of a tensor)."""
+    if nbytes is None:
+        nbytes = workspace.numel() * workspace.element_size()
+    _check(lib.kvx_workspace_clear(_dptr(workspace), int(nbytes), _stream(stream)),
+           "kvx_workspace_clear")
 
 
 def kvx_gather_workspace_bytes(S: int, max_blocks: int) -> int:

@@ -187,3 +187,23 @@ def test_custom_scale():
     dev = DeviceCase(case, make_plan(case))
     got = dev.run(scale=0.05)
     assert max_abs(got, oracle_out(case, scale=0.05)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+def test_repeated_calls_and_shared_workspace(kernel):
+    """Split heads are merged in-kernel with per-head counters that return to
+    zero after every call: repeated calls, and two plans taking turns on one
+    workspace, give bit-identical results."""
+    a_case, b_case = qwen3_like(9), qwen25_like(10)
+    a = DeviceCase(a_case, make_plan(a_case, num_ctas=13, kernel=kernel))
+    b = DeviceCase(b_case, make_plan(b_case, num_ctas=29, kernel=kernel))
+    assert a.plan.stats()["num_split_heads"] > 0 and b.plan.stats()["num_split_heads"] > 0
+    ws = torch.zeros(max(a.ws.numel(), b.ws.numel()), dtype=torch.int32, device="cuda")
+    a.ws = b.ws = ws
+    first_a, first_b = a.run(), b.run()
+    for _ in range(3):
+        assert np.array_equal(a.run(), first_a)
+        assert np.array_equal(b.run(), first_b)
+    assert a.status() == 0
+    assert max_abs(first_a, oracle_out(a_case)) <= TOL_BF16
+    assert max_abs(first_b, oracle_out(b_case)) <= TOL_BF16
