@@ -229,6 +229,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   const int it0 = p.cta_off[blockIdx.x], it1 = p.cta_off[blockIdx.x + 1];
   const int P = p.P, g = p.g;
   uint64_t t_start = 0;
+  pdl_launch_dependents();
   if (threadIdx.x == 0) {
     if (p.trace) t_start = globaltimer_ns();
     for (int s = 0; s < kStages; ++s) {
@@ -238,7 +239,14 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     *abort_flag = 0;
     fence_barrier_init();
   }
+  if (warp == kCons && lane < p.num_groups) {
+    prefetch_tensormap(&p.tmK[lane]);
+    prefetch_tensormap(&p.tmV[lane]);
+  }
   __syncthreads();
+  // Everything above touches only this block's shared memory and the kernel
+  // parameters; global inputs may come from the previous kernel in the stream.
+  pdl_wait();
 
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
@@ -464,7 +472,18 @@ cudaError_t launch_d(const AttnParams &p, int num_ctas, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  attn_mma_kernel<D><<<num_ctas, (kCons + 1) * 32, Cfg<D>::kSmem, st>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3((kCons + 1) * 32);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_mma_kernel<D>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -44,6 +44,8 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int it0 = p.cta_off[blockIdx.x], it1 = p.cta_off[blockIdx.x + 1];
   const int g = p.g, P = p.P;
   uint64_t t_start = p.trace ? globaltimer_ns() : 0;
+  pdl_launch_dependents();
+  pdl_wait();  // global inputs may come from the previous kernel in the stream
   for (int it = it0; it < it1; ++it) {
     const Item item = p.items[it];
     const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
@@ -164,18 +166,23 @@ __global__ void __launch_bounds__(kWarps * 32)
 cudaError_t launch_attn_simt(const AttnParams &p, int dtype, int num_ctas,
                              cudaStream_t st) {
   if (num_ctas <= 0) return cudaSuccess;
-  const dim3 grid(num_ctas), block(kWarps * 32);
-  if (dtype == KVX_F32) {
-    if (p.D == 128)
-      attn_simt_kernel<float, 128><<<grid, block, 0, st>>>(p);
-    else
-      attn_simt_kernel<float, 64><<<grid, block, 0, st>>>(p);
-  } else {
-    if (p.D == 128)
-      attn_simt_kernel<__nv_bfloat16, 128><<<grid, block, 0, st>>>(p);
-    else
-      attn_simt_kernel<__nv_bfloat16, 64><<<grid, block, 0, st>>>(p);
-  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_ctas);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (dtype == KVX_F32)
+    e = p.D == 128 ? cudaLaunchKernelEx(&cfg, attn_simt_kernel<float, 128>, p)
+                   : cudaLaunchKernelEx(&cfg, attn_simt_kernel<float, 64>, p);
+  else
+    e = p.D == 128 ? cudaLaunchKernelEx(&cfg, attn_simt_kernel<__nv_bfloat16, 128>, p)
+                   : cudaLaunchKernelEx(&cfg, attn_simt_kernel<__nv_bfloat16, 64>, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -60,7 +60,7 @@ struct alignas(128) AttnParams {
   float2 *part_ml;             // [slots][g] = (max in log2 units, sum)
   uint32_t *status;
   int64_t *trace;
-  int32_t B, Hq, Hkv, D, g, P;
+  int32_t B, Hq, Hkv, D, g, P, num_groups;
   float scale_log2;            // scale * log2(e)
   int8_t head_grp[KVX_MAX_KV_HEADS];
   int8_t head_row[KVX_MAX_KV_HEADS];
