@@ -58,6 +58,37 @@ def peaks():
         return FALLBACK_HBM, "fallback"
 
 
+KERNEL_SOURCES = ["attn_mma.cu", "ptx.cuh", "split_merge.cuh", "kvx_internal.h"]
+PROFILE = os.path.join(ROOT, "profiles", "attn_mma_qwen3_4b.md")
+
+
+def kernel_source_hash() -> str:
+    """sha256 over the attention kernel's source files, to tell whether a
+    committed ncu capture still describes the kernel that runs."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_non_uniform_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic():
+    """(dram bytes per launch, algorithmic bytes of that launch) from the
+    committed ncu summary, or None if the kernel has changed since."""
+    try:
+        kv = {}
+        for line in open(PROFILE):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                kv[k.strip()] = v.strip().strip("`")
+        if kv.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"]), float(kv["algorithmic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def describe(cfg) -> str:
     return (f"{cfg.name} decode: {cfg.layers} layers, batch {cfg.B}, {cfg.Hq} q / {cfg.Hkv} KV "
             f"heads, head_dim {cfg.D}, {cfg.dtype}, page {cfg.P}, {cfg.num_groups} head groups, "
@@ -187,6 +218,37 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- replicas
+def rank_seed(rank: int) -> int:
+    """Seed of the batch a replica serves: every rank decodes its own batch."""
+    return rank
+
+
+def max_over_ranks(ms: float, dist, device=None) -> float:
+    """The slowest rank's time (the whole job finishes when it does)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, dist, device=None) -> float:
+    """Units all ranks processed (each rank's batch differs)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def job_rate(total_bytes: float, ms: float) -> float:
+    """Whole-job GB/s: bytes all ranks processed over the slowest rank's time."""
+    return total_bytes / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 class Clocks:
     def __init__(self):
@@ -252,8 +314,8 @@ def run_ours(args, rank, world):
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.current_stream()
 
-    cfg = synth.decode_config(args.workload, seed=rank)  # each rank serves its own batch
-    table = ValueTable(seed=11 + rank, rows=1 << 19, D=cfg.D, dtype=cfg.dtype)
+    cfg = synth.decode_config(args.workload, seed=rank_seed(rank))
+    table = ValueTable(seed=11 + rank_seed(rank), rows=1 << 19, D=cfg.D, dtype=cfg.dtype)
     sms = kvx.kvx_device_sm_count()
     plans, layers = [], []
     plan_us = []
@@ -305,12 +367,9 @@ def run_ours(args, rank, world):
         dist.barrier()
     ms_total = t0.elapsed_time(t1)
     assert kvx.kvx_workspace_status(ws) == 0, "device status set during the timed region"
-    ms_step = ms_total / args.steps
-    if dist:
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    ms_step = max_over_ranks(ms_total / args.steps, dist, dev)
+    bytes_job = sum_over_ranks(bytes_step, dist, dev)
+    value = job_rate(bytes_job, ms_step)
 
     # ---- roofline of the attention kernel: a second pass of K steps with an
     # event around every call (one kernel launch each); algorithmic KV bytes
@@ -329,6 +388,12 @@ def run_ours(args, rank, world):
     achieved = float(np.mean([bytes_layer[l] / (call_ms[s][l] * 1e-3)
                               for s in range(args.steps) for l in range(cfg.layers)])) / 1e9
     peak, peak_kind = peaks()
+    prof = profiled_traffic()
+    # ncu traffic of the profiled launch (layer 0), scaled to the mean launch
+    traffic = (prof[0] * np.mean(bytes_layer) / prof[1]) if prof else None
+
+    # ---- load balance of layer 0 under the three plans (same kernel)
+    balance = measure_balance(cfg, layers[0], ws, stream, kvx, torch) if rank == 0 else None
 
     # ---- end to end through the public API with host buffers
     g = cfg.Hq // cfg.Hkv
@@ -356,12 +421,8 @@ def run_ours(args, rank, world):
     for _ in range(e2e_steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - h0) * 1e3 / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks((time.perf_counter() - h0) * 1e3 / e2e_steps, dist, dev)
+    e2e_value = job_rate(bytes_job, e2e_ms)
 
     # ---- gather (KV-RM movement workload)
     gather = None
@@ -387,8 +448,12 @@ def run_ours(args, rank, world):
                        "sms": sms},
             "frac_of_hbm": value / world / peak,
             "seq_heads_per_s": world * cfg.B * cfg.Hq * cfg.layers / (ms_step * 1e-3),
+            "kv_bytes_per_step": bytes_job,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak, "traffic": traffic,
+                         "traffic_note": "ncu dram read+write of the profiled layer-0 launch, scaled "
+                                         "to the mean launch by algorithmic bytes" if prof else
+                                         "kernel changed since the committed capture",
                          "kernel": "attn_mma_kernel<128> (one launch per layer call)",
                          "timing": "second pass of K steps, CUDA events around every launch",
                          "peak_source": f"{peak_kind} hbm_gbs", "mean_call_us": 1e3 * mean_call_ms},
@@ -399,6 +464,7 @@ def run_ours(args, rank, world):
             "clocks": clk,
             "plan_host_us_per_layer": float(np.mean(plan_us)),
             "gather": gather,
+            "balance": balance,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -406,12 +472,58 @@ def run_ours(args, rank, world):
         dist.destroy_process_group()
 
 
+def measure_balance(cfg, lay, ws, stream, kvx, torch):
+    """Layer 0 under the balanced ahead-of-time plan and the two naive plans:
+    kernel time (median of 20) and the spread of per-block busy times from
+    the kernel's own trace (SM id, start, end, tokens per block)."""
+    res = {}
+    names = {kvx.KVX_PLAN_BALANCED: "balanced_aot", kvx.KVX_PLAN_PER_HEAD: "one_block_per_head",
+             kvx.KVX_PLAN_UNIFORM: "uniform_split"}
+    out = torch.empty((cfg.B, cfg.Hq, cfg.D), dtype=torch.float32, device=ws.device)
+    for pol, name in names.items():
+        p = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                                kvx.KVX_BF16, cfg.budget[0], cfg.seq_len, cfg.head_group[0], 0,
+                                pol)
+        kvx.kvx_plan_upload(p)
+        w = torch.zeros(p.workspace_bytes() // 4 + 64, dtype=torch.int32, device=ws.device)
+
+        def run():
+            kvx.kvx_decode_attn(p, lay.q, lay.k_pools, lay.v_pools, lay.pool_pages, lay.pt,
+                                lay.strides, lay.budget, lay.seq_len, 0.0, out, w, stream=stream)
+        for _ in range(3):
+            run()
+        ts = []
+        for _ in range(20):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            run()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3)
+        st = p.stats()
+        tr = torch.zeros((st["num_ctas"], 4), dtype=torch.int64, device=ws.device)
+        p.set_trace(tr)
+        run()
+        torch.cuda.synchronize()
+        p.set_trace(None)
+        t = tr.cpu().numpy()
+        busy = (t[:, 2] - t[:, 1]) / 1e3
+        res[name] = {"kernel_us": float(np.median(ts)), "blocks": int(st["num_ctas"]),
+                     "block_busy_us_mean": float(busy.mean()), "block_busy_us_max": float(busy.max()),
+                     "tokens_per_block_mean": float(st["mean_cta_tokens"]),
+                     "tokens_per_block_max": int(st["max_cta_tokens"]),
+                     "plan_host_us": float(st["plan_us"])}
+        p.destroy()
+    return res
+
+
 def bench_gather(args, dev, stream, peak, dist, world, rank):
     import torch
     from paged_non_uniform_gb300 import kvx
     from synth.device import ValueTable
-    cfg = synth.gather_config(seed=rank)
-    table = ValueTable(seed=21 + rank, rows=1 << 18, D=128, dtype="bf16")
+    cfg = synth.gather_config(seed=rank_seed(rank))
+    table = ValueTable(seed=21 + rank_seed(rank), rows=1 << 18, D=128, dtype="bf16")
     pools, stagings = [], []
     for t in range(2):
         p = torch.empty((cfg.num_phys, cfg.block_bytes // 2), dtype=torch.bfloat16, device=dev)
@@ -441,21 +553,17 @@ def bench_gather(args, dev, stream, peak, dist, world, rank):
         call()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(a.elapsed_time(b) / steps, dist, dev)
     assert kvx.kvx_workspace_status(ws) == 0
-    live = 2 * cfg.live_bytes()  # K and V
-    moved = 2 * live             # read + write
+    live = sum_over_ranks(2 * cfg.live_bytes(), dist, dev)  # K and V, all ranks
+    moved = 2 * live                                        # read + write
     return {"workload": f"KV-RM movement: {cfg.S} seqs, {int(cfg.seq_tokens.min())}.."
                         f"{int(cfg.seq_tokens.max())} tokens, 32 KB blocks (16 tok x 8 heads x 128 "
                         f"bf16), K+V pools {2 * cfg.num_phys * cfg.block_bytes / 2**30:.0f} GiB "
                         f"randomly permuted, staging [{cfg.S}][16384] per tensor",
-            "value": world * moved / (ms * 1e-3) / 1e9, "unit": "GB/s (read+write)",
-            "payload_gbs": world * live / (ms * 1e-3) / 1e9, "ms_per_call": ms,
-            "frac": moved / (ms * 1e-3) / 1e9 / peak, "launches_per_call": 4}
+            "value": job_rate(moved, ms), "unit": "GB/s (read+write)",
+            "payload_gbs": job_rate(live, ms), "ms_per_call": ms,
+            "frac": job_rate(moved, ms) / world / peak, "launches_per_call": 4}
 
 
 def main():
