@@ -186,6 +186,16 @@ int kvx_plan_cta_tokens(const kvx_plan *plan, int64_t *tokens);
  * subsequent kvx_decode_attn with this plan; NULL turns it off. */
 int kvx_plan_set_trace(kvx_plan *plan, int64_t *dev_trace);
 
+/* Failure-detection test hook (no effect unless called). The tensor-core
+ * kernel's thread block `block` arms the barrier of its first pipeline stage
+ * but issues none of its loads, so the wait for that stage runs out after
+ * wait_limit_ns (1 ms .. 10 s; every pipeline wait uses this limit, 2 s by
+ * default). The call then finishes with KVX_DEV_TIMEOUT set in the workspace
+ * status word; its output is undefined, the CUDA context stays usable, and the
+ * workspace must be cleared before the next call. block < 0 turns the stall
+ * off (the limit stays as given). Errors: KVX_EINVAL, KVX_ERANGE. */
+int kvx_plan_inject_stall(kvx_plan *plan, int32_t block, uint64_t wait_limit_ns);
+
 void kvx_plan_destroy(kvx_plan *plan);
 
 /* ---------------------------------------------------------------------------

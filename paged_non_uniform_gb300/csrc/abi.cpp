@@ -156,6 +156,8 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   p.g = g;
   p.P = P;
   p.num_groups = G;
+  p.stall_block = plan->stall_block;
+  p.wait_ns = plan->wait_ns;
   const float sc = scale == 0.f ? 1.0f / std::sqrt((float)D) : scale;
   p.scale_log2 = (float)((double)sc * 1.4426950408889634);
 

@@ -26,9 +26,10 @@
 //    memory and write the output or, for a head cut into pieces, the piece's
 //    partial; the block that completes a head's last piece then merges all its
 //    partials (split_merge.cuh).
-// No spin-wait is unbounded: every mbarrier wait gives up after kWaitNs and
-// sets KVX_DEV_TIMEOUT. Pages outside the pool are loaded as zeros (the box
-// is placed past the tensor's end) and set KVX_DEV_BAD_PAGE.
+// No spin-wait is unbounded: every mbarrier wait gives up after p.wait_ns
+// (2 s unless a test shortens it) and sets KVX_DEV_TIMEOUT. Pages outside the
+// pool are loaded as zeros (the box is placed past the tensor's end) and set
+// KVX_DEV_BAD_PAGE.
 #include <math.h>
 
 #include "kvx_internal.h"
@@ -53,7 +54,6 @@ namespace {
 #endif
 constexpr int kCons = KVX_ATTN_CONS;
 constexpr int kStages = KVX_ATTN_STAGES;
-constexpr uint64_t kWaitNs = 2000000000ull;
 // Stage gs goes to consumer warp gs % kCons and ring slot gs % kStages. With
 // kStages a multiple of kCons every slot belongs to one warp, which waits on
 // that slot's phases strictly in order. Otherwise a warp could wait for phase
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
           bool ok = true;
           if (lane == 0)
             ok = !*abort_flag &&
-                 mbar_wait(empty0 + 8 * slot, ((gs / kStages) - 1) & 1, kWaitNs);
+                 mbar_wait(empty0 + 8 * slot, ((gs / kStages) - 1) & 1, p.wait_ns);
           ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!ok) {
             if (lane == 0) {
@@ -317,8 +317,12 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
               y = (page * gd.size + row) * P + (tb & (P - 1));
             }
             const uint32_t d = kdst + (uint32_t)i * box_bytes;
-            tma_load_3d(d, tmk, 0, y, 0, full, pol);
-            tma_load_3d(d + C::kTile, tmv, 0, y, 0, full, pol);
+            // Failure-detection test only: the chosen block arms its first
+            // stage but loads nothing, so that stage's wait runs out.
+            if (!(gs == 0 && (int)blockIdx.x == p.stall_block)) {
+              tma_load_3d(d, tmk, 0, y, 0, full, pol);
+              tma_load_3d(d + C::kTile, tmv, 0, y, 0, full, pol);
+            }
           }
         }
       }
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       const int issued = gs;
       for (int s = 0; s < kStages && s < issued; ++s) {
         const int last = s + ((issued - 1 - s) / kStages) * kStages;
-        if (!mbar_wait(full0 + 8 * s, (last / kStages) & 1, kWaitNs))
+        if (!mbar_wait(full0 + 8 * s, (last / kStages) & 1, p.wait_ns))
           atomicOr(p.status, KVX_DEV_TIMEOUT);
       }
     }
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
         if (gs % kCons != warp || dead) continue;
         const int slot = gs % kStages;
         bool ok = !*abort_flag;
-        if (ok) ok = mbar_wait(full0 + 8 * slot, (gs / kStages) & 1, kWaitNs);
+        if (ok) ok = mbar_wait(full0 + 8 * slot, (gs / kStages) & 1, p.wait_ns);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) {

@@ -62,6 +62,8 @@ struct alignas(128) AttnParams {
   int64_t *trace;
   int32_t B, Hq, Hkv, D, g, P, num_groups;
   float scale_log2;            // scale * log2(e)
+  int32_t stall_block;         // failure-detection test: block whose first stage gets no loads (-1: none)
+  uint64_t wait_ns;            // limit of every pipeline wait
   int8_t head_grp[KVX_MAX_KV_HEADS];
   int8_t head_row[KVX_MAX_KV_HEADS];
 };
@@ -130,4 +132,6 @@ struct kvx_plan {
   int32_t *d_n;
   kvx::SplitHead *d_split;
   int64_t *d_trace;
+  int32_t stall_block;  // kvx_plan_inject_stall
+  uint64_t wait_ns;
 };

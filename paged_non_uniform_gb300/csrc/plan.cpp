@@ -220,6 +220,8 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
     p->d_n = nullptr;
     p->d_split = nullptr;
     p->d_trace = nullptr;
+    p->stall_block = -1;
+    p->wait_ns = 2000000000ull;
     // Deterministic Budget Allocation: n = min(L, budget).
     p->n.resize((size_t)B * Hkv);
     for (int b = 0; b < B; ++b)
@@ -380,6 +382,14 @@ extern "C" int kvx_plan_cta_tokens(const kvx_plan *p, int64_t *tokens) {
 extern "C" int kvx_plan_set_trace(kvx_plan *p, int64_t *dev_trace) {
   if (!p) return KVX_EINVAL;
   p->d_trace = dev_trace;
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_inject_stall(kvx_plan *p, int32_t block, uint64_t wait_limit_ns) {
+  if (!p) return KVX_EINVAL;
+  if (wait_limit_ns < 1000000ull || wait_limit_ns > 10000000000ull) return KVX_ERANGE;
+  p->stall_block = block < 0 ? -1 : block;
+  p->wait_ns = wait_limit_ns;
   return KVX_OK;
 }
 

@@ -87,6 +87,7 @@ lib.kvx_plan_group_pages.argtypes = [_vp, _vp]
 lib.kvx_plan_items.argtypes = [_vp, _vp, _vp]
 lib.kvx_plan_cta_tokens.argtypes = [_vp, _vp]
 lib.kvx_plan_set_trace.argtypes = [_vp, _vp]
+lib.kvx_plan_inject_stall.argtypes = [_vp, _c.c_int32, _c.c_uint64]
 lib.kvx_plan_destroy.argtypes = [_vp]
 lib.kvx_plan_destroy.restype = None
 lib.kvx_decode_attn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c.c_float, _vp,
@@ -194,6 +195,11 @@ class Plan:
 
     def set_trace(self, dev_trace) -> None:
         _check(lib.kvx_plan_set_trace(self.handle, _dptr(dev_trace)), "kvx_plan_set_trace")
+
+    def inject_stall(self, block: int, wait_limit_ns: int) -> None:
+        """Failure-detection test hook: see kvx_plan_inject_stall."""
+        _check(lib.kvx_plan_inject_stall(self.handle, int(block), int(wait_limit_ns)),
+               "kvx_plan_inject_stall")
 
     def destroy(self) -> None:
         if self.handle:

@@ -207,3 +207,33 @@ def test_repeated_calls_and_shared_workspace(kernel):
     assert a.status() == 0
     assert max_abs(first_a, oracle_out(a_case)) <= TOL_BF16
     assert max_abs(first_b, oracle_out(b_case)) <= TOL_BF16
+
+
+def test_pipeline_wait_runs_out_and_is_reported():
+    """Failure detection without a GPU fault: one block's first stage is armed
+    but never loaded, so its wait runs out after 50 ms. The call must return
+    with KVX_DEV_TIMEOUT, and the next call on the same context, after the
+    workspace is cleared and the stall removed, must be correct again."""
+    import time
+    case = qwen3_like(11)
+    plan = make_plan(case, num_ctas=16, kernel=kvx.KVX_KERNEL_MMA)
+    dev = DeviceCase(case, plan)
+    plan.inject_stall(3, 50_000_000)
+    t0 = time.perf_counter()
+    dev.run()
+    elapsed = time.perf_counter() - t0
+    assert dev.status() & kvx.KVX_DEV_TIMEOUT
+    assert elapsed < 5.0
+    plan.inject_stall(-1, 2_000_000_000)
+    kvx.kvx_workspace_clear(dev.ws)
+    got = dev.run()
+    assert dev.status() == 0
+    assert max_abs(got, oracle_out(case)) <= TOL_BF16
+
+
+def test_stall_hook_rejects_bad_limits():
+    case = d64_bf16(12)
+    plan = make_plan(case, upload=False)
+    for bad in (0, 999_999, 20_000_000_000):
+        with pytest.raises(kvx.KvxError):
+            plan.inject_stall(0, bad)
