@@ -518,6 +518,49 @@ def measure_balance(cfg, lay, ws, stream, kvx, torch):
     return res
 
 
+def kvrm_attention(cfg, pools, stagings, bt, dev, stream, peak, steps, kvx, torch):
+    """Fixed-shape decode attention after the gather: the K and V staging
+    buffers viewed as token-major pages of 16 tokens (identity page table),
+    32 query heads over the 8 KV heads, every token kept. Also timed directly
+    on the fragmented block pool (block table as page table)."""
+    S, mb, Hkv, Hq, D = cfg.S, cfg.max_blocks, 8, 32, 128
+    L = np.ascontiguousarray(cfg.seq_tokens, dtype=np.int32)
+    plan = kvx.kvx_plan_create(S, Hq, Hkv, D, 16, 1, kvx.KVX_BF16,
+                               np.full((S, Hkv), synth.FULL, np.int32), L,
+                               np.zeros(Hkv, np.int32), 0, layout=kvx.KVX_LAYOUT_TOKEN_MAJOR)
+    kvx.kvx_plan_upload(plan)
+    g = synth.rng(77)
+    q = torch.from_numpy(synth.f32_to_bf16_bits(synth.normal(g, (S, Hq, D), "bf16")).view(
+        np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.zeros(plan.workspace_bytes() // 4 + 64, dtype=torch.int32, device=dev)
+    budget = torch.full((S * Hkv,), synth.FULL, dtype=torch.int32, device=dev)
+    Ld = torch.from_numpy(L).to(dev)
+    ident = torch.arange(S * mb, dtype=torch.int32, device=dev).view(S, mb)
+    kv_bytes = int(L.astype(np.int64).sum()) * Hkv * 2 * D * 2
+    res = {"workload": f"{S} sequences, {Hq} q / {Hkv} KV heads, D {D}, bf16, all tokens kept"}
+    for name, kp, vp, pt, npages in (("over_staging", stagings[0], stagings[1], ident, S * mb),
+                                     ("over_fragmented_pool", pools[0], pools[1], bt,
+                                      cfg.num_phys)):
+        def call():
+            kvx.kvx_decode_attn(plan, q, [kp], [vp], [npages], [pt], [pt.shape[1]], budget, Ld,
+                                0.0, out, ws, stream=stream)
+        for _ in range(3):
+            call()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        res[name] = {"value": kv_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s (KV read)",
+                     "frac": kv_bytes / (ms * 1e-3) / 1e9 / peak, "ms_per_call": ms}
+    assert kvx.kvx_workspace_status(ws) == 0
+    return res
+
+
 def bench_gather(args, dev, stream, peak, dist, world, rank):
     import torch
     from paged_non_uniform_gb300 import kvx
@@ -555,6 +598,7 @@ def bench_gather(args, dev, stream, peak, dist, world, rank):
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b) / steps, dist, dev)
     assert kvx.kvx_workspace_status(ws) == 0
+    attn = kvrm_attention(cfg, pools, stagings, bt, dev, stream, peak, steps, kvx, torch)
     live = sum_over_ranks(2 * cfg.live_bytes(), dist, dev)  # K and V, all ranks
     moved = 2 * live                                        # read + write
     return {"workload": f"KV-RM movement: {cfg.S} seqs, {int(cfg.seq_tokens.min())}.."
@@ -563,7 +607,8 @@ def bench_gather(args, dev, stream, peak, dist, world, rank):
                         f"randomly permuted, staging [{cfg.S}][16384] per tensor",
             "value": job_rate(moved, ms), "unit": "GB/s (read+write)",
             "payload_gbs": job_rate(live, ms), "ms_per_call": ms,
-            "frac": job_rate(moved, ms) / world / peak, "launches_per_call": 4}
+            "frac": job_rate(moved, ms) / world / peak, "launches_per_call": 4,
+            "attention": attn}
 
 
 def main():

@@ -81,6 +81,16 @@ extern "C" {
 #define KVX_KERNEL_MMA 1  /* bf16 only: bulk-tensor loads + warp-level MMA */
 #define KVX_KERNEL_SIMT 2 /* CUDA-core kernel, fp32 or bf16 */
 
+/* ---- page layouts ------------------------------------------------------ */
+/* A head-group page holds P token slots for each of the |G| heads of its
+ * group, for K and (in a separate pool) for V:
+ *  HEAD_MAJOR  [|G|][P][D]: the slots of one head are contiguous
+ *              (Tangram's head-group page, Fig. 8(b));
+ *  TOKEN_MAJOR [P][|G|][D]: the heads of one token are contiguous, the block
+ *              layout of KV-RM's block pager and staging buffer (Fig. 2). */
+#define KVX_LAYOUT_HEAD_MAJOR 0
+#define KVX_LAYOUT_TOKEN_MAJOR 1
+
 /* ---- gather flags ------------------------------------------------------ */
 #define KVX_ZERO_TAIL 1 /* zero each staging row past its live blocks */
 
@@ -99,6 +109,7 @@ typedef struct kvx_shape {
   int32_t page_size;  /* P, tokens per page: 8, 16, 32, 64 or 128 */
   int32_t num_groups; /* head groups, <= KVX_MAX_GROUPS */
   int32_t dtype;      /* KVX_F32 or KVX_BF16 (q, K and V share it) */
+  int32_t layout;     /* page layout: KVX_LAYOUT_HEAD_MAJOR or KVX_LAYOUT_TOKEN_MAJOR */
 } kvx_shape;
 
 typedef struct kvx_plan kvx_plan;
@@ -212,12 +223,15 @@ void kvx_plan_destroy(kvx_plan *plan);
  * Head-group page addressing (Tangram, Fig. 8(b)): head h belongs to group
  * G = head_group[h] and has row r = its rank within G. Its t-th kept token is
  * in physical page p = page_tables[G][b * page_table_stride[G] + t / P],
- * at k_pools[G] + ((p * |G| + r) * P + t % P) * D elements (same for V).
+ * at k_pools[G] + ((p * |G| + r) * P + t % P) * D elements with the
+ * head-major layout, or k_pools[G] + ((p * P + t % P) * |G| + r) * D with
+ * the token-major layout (same for V).
  *
  *   plan              an uploaded plan built for these shapes and budgets.
  *   q                 [B][Hq][D] of the plan's dtype (device).
  *   k_pools, v_pools  host arrays [num_groups] of device pointers, each a
- *                     pool [pool_pages[G]][|G|][P][D] of the plan's dtype,
+ *                     pool of pool_pages[G] pages, [|G|][P][D] (head-major)
+ *                     or [P][|G|][D] (token-major) of the plan's dtype,
  *                     16-byte aligned.
  *   pool_pages        host int64 [num_groups], pages in each pool.
  *   page_tables       host array [num_groups] of device int32 pointers, each

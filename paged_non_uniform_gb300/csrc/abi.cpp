@@ -38,20 +38,31 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// A 3-D bf16 tensor map over a pool of rows of D elements, viewed as
-// {64 elements, rows, D/64 halves} with strides {2 B, D*2 B, 128 B}: one box
-// {64, box_rows, D/64} fetches box_rows whole rows and lands in shared memory
-// as [half][row][128 B], 128-byte swizzled, zero-filled out of bounds.
-static bool encode_pool_map(CUtensorMap *tm, const void *base, int64_t rows,
-                            int D, int box_rows) {
+// A 5-D bf16 tensor map over one head-group pool, dims (innermost first)
+// {64 elements, P slots, D/64 halves, |G| heads, pages}: one box
+// {64, box_rows, D/64, 1, 1} fetches box_rows token rows of one head of one
+// page and lands in shared memory as [half][row][128 B], 128-byte swizzled,
+// zero-filled out of bounds. The two page layouts differ only in strides.
+static bool encode_pool_map(CUtensorMap *tm, const void *base, int64_t pages,
+                            int gsize, int P, int D, int layout, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
+  const cuuint64_t row = (cuuint64_t)D * 2;  // bytes of one token row of one head
   const cuuint32_t halves = (cuuint32_t)(D / 64);
-  cuuint64_t dims[3] = {64u, (cuuint64_t)rows, halves};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, 128u};
-  cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, halves};
-  cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+  cuuint64_t dims[5] = {64u, (cuuint64_t)P, halves, (cuuint64_t)gsize, (cuuint64_t)pages};
+  cuuint64_t strides[4];
+  if (layout == KVX_LAYOUT_HEAD_MAJOR) {  // [|G|][P][D]
+    strides[0] = row;                     // slot
+    strides[2] = row * P;                 // head
+  } else {                                // [P][|G|][D]
+    strides[0] = row * gsize;             // slot
+    strides[2] = row;                     // head
+  }
+  strides[1] = 128u;                      // half
+  strides[3] = row * P * gsize;           // page
+  cuuint32_t box[5] = {64u, (cuuint32_t)box_rows, halves, 1u, 1u};
+  cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -109,8 +120,7 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
     if (!k_pools[gi] || !v_pools[gi] || !page_tables[gi]) return KVX_EINVAL;
     if (!aligned(k_pools[gi], 16) || !aligned(v_pools[gi], 16)) return KVX_EINVAL;
     if (pool_pages[gi] < 1) return KVX_EINVAL;
-    const int64_t rows = pool_pages[gi] * plan->group_size[gi] * (int64_t)P;
-    if (rows >= ((int64_t)1 << 31) - 128) return KVX_ERANGE;
+    if (pool_pages[gi] >= ((int64_t)1 << 31) - 1) return KVX_ERANGE;
     int32_t mx = 0;
     for (int b = 0; b < B; ++b) mx = std::max(mx, plan->group_pages[(size_t)gi * B + b]);
     if (page_table_stride[gi] < std::max(mx, 1)) return KVX_ERANGE;
@@ -123,8 +133,10 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
     gd.size = plan->group_size[gi];
     if (plan->kernel == KVX_KERNEL_MMA) {
       const int box = std::min(P, kStageTokens);
-      if (!encode_pool_map(&p.tmK[gi], k_pools[gi], rows, D, box) ||
-          !encode_pool_map(&p.tmV[gi], v_pools[gi], rows, D, box))
+      if (!encode_pool_map(&p.tmK[gi], k_pools[gi], pool_pages[gi], plan->group_size[gi], P, D,
+                           s.layout, box) ||
+          !encode_pool_map(&p.tmV[gi], v_pools[gi], pool_pages[gi], plan->group_size[gi], P, D,
+                           s.layout, box))
         return set_cuda_error(cudaErrorInvalidValue);
     }
   }
@@ -156,6 +168,7 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   p.g = g;
   p.P = P;
   p.num_groups = G;
+  p.layout = s.layout;
   p.stall_block = plan->stall_block;
   p.wait_ns = plan->wait_ns;
   const float sc = scale == 0.f ? 1.0f / std::sqrt((float)D) : scale;

@@ -10,9 +10,10 @@
 //
 // Data path, per thread block (one per SM, persistent over its items):
 //  * one producer warp walks the items' pages through the head group's page
-//    table (Fig. 8(b)) and issues bulk-tensor loads of each page slot's K and
-//    V rows (token-major, 128-byte swizzled, two 64-element halves of a row)
-//    into a ring of 32-token stages, completing on per-stage mbarriers;
+//    table (Fig. 8(b)) and issues one bulk-tensor load per page slot of K and
+//    of V (a 5-D tensor map {64 elements, slot, half, head, page} covers both
+//    page layouts; the box lands as [half][token row][128 B], 128-byte
+//    swizzled) into a ring of 32-token stages, completing on mbarriers;
 //  * kCons consumer warps take the stages round-robin (ring slot s always
 //    belongs to warp s % kCons, so each warp sees its slots' mbarrier phases
 //    in order). Per stage a warp
@@ -263,7 +264,6 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       const int32_t *pt = gd.page_table + (size_t)b * gd.stride;
       const void *tmk = &p.tmK[gi];
       const void *tmv = &p.tmV[gi];
-      const int rows_ext = (int)(gd.num_pages * gd.size * P);
       const int maxpg = (item.end - 1) / P;
       int win = -1;
       int32_t my_page = 0;
@@ -309,19 +309,17 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
 #else
           if (lane == 0) {
 #endif
-            int y;
+            int pg = page;
             if (page < 0 || (int64_t)page >= gd.num_pages) {
               atomicOr(p.status, KVX_DEV_BAD_PAGE);
-              y = rows_ext;  // whole box past the end: loads zeros
-            } else {
-              y = (page * gd.size + row) * P + (tb & (P - 1));
+              pg = (int)gd.num_pages;  // whole box past the last page: loads zeros
             }
             const uint32_t d = kdst + (uint32_t)i * box_bytes;
             // Failure-detection test only: the chosen block arms its first
             // stage but loads nothing, so that stage's wait runs out.
             if (!(gs == 0 && (int)blockIdx.x == p.stall_block)) {
-              tma_load_3d(d, tmk, 0, y, 0, full, pol);
-              tma_load_3d(d + C::kTile, tmv, 0, y, 0, full, pol);
+              tma_load_5d(d, tmk, 0, tb & (P - 1), 0, row, pg, full, pol);
+              tma_load_5d(d + C::kTile, tmv, 0, tb & (P - 1), 0, row, pg, full, pol);
             }
           }
         }

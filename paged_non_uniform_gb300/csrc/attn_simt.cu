@@ -78,7 +78,9 @@ __global__ void __launch_bounds__(kWarps * 32)
 #pragma unroll
         for (int i = 0; i < DL; ++i) kv[i] = vv[i] = 0.f;
       } else {
-        const size_t rr = ((size_t)page * gd.size + row) * P + (t & (P - 1));
+        const size_t rr = p.layout == KVX_LAYOUT_HEAD_MAJOR
+                              ? ((size_t)page * gd.size + row) * P + (t & (P - 1))
+                              : ((size_t)page * P + (t & (P - 1))) * gd.size + row;
 #pragma unroll
         for (int i = 0; i < DL; ++i) {
           kv[i] = to_f(kp[rr * D + lane + 32 * i]);

@@ -60,7 +60,7 @@ struct alignas(128) AttnParams {
   float2 *part_ml;             // [slots][g] = (max in log2 units, sum)
   uint32_t *status;
   int64_t *trace;
-  int32_t B, Hq, Hkv, D, g, P, num_groups;
+  int32_t B, Hq, Hkv, D, g, P, num_groups, layout;
   float scale_log2;            // scale * log2(e)
   int32_t stall_block;         // failure-detection test: block whose first stage gets no loads (-1: none)
   uint64_t wait_ns;            // limit of every pipeline wait

@@ -177,6 +177,8 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
   if (!is_pow2(s->page_size) || s->page_size < 8 || s->page_size > 128)
     return KVX_EUNSUPPORTED;
   if (s->dtype != KVX_F32 && s->dtype != KVX_BF16) return KVX_EUNSUPPORTED;
+  if (s->layout != KVX_LAYOUT_HEAD_MAJOR && s->layout != KVX_LAYOUT_TOKEN_MAJOR)
+    return KVX_EUNSUPPORTED;
   if (policy < KVX_PLAN_BALANCED || policy > KVX_PLAN_UNIFORM)
     return KVX_EINVAL;
   if (kernel < KVX_KERNEL_AUTO || kernel > KVX_KERNEL_SIMT) return KVX_EINVAL;

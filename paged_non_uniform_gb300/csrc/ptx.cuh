@@ -79,23 +79,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return pol;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap,
-                                            int x, int y, uint32_t bar,
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, int c0,
+                                            int c1, int c2, int c3, int c4, uint32_t bar,
                                             uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_"
-      "tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap,
-                                            int x, int y, int z, uint32_t bar,
-                                            uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_"
-      "tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(pol)
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_"
+      "tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(pol)
       : "memory");
 }
 

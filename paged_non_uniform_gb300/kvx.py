@@ -40,6 +40,8 @@ KVX_KERNEL_AUTO = 0
 KVX_KERNEL_MMA = 1
 KVX_KERNEL_SIMT = 2
 KVX_ZERO_TAIL = 1
+KVX_LAYOUT_HEAD_MAJOR = 0
+KVX_LAYOUT_TOKEN_MAJOR = 1
 KVX_MAX_GROUPS = 16
 KVX_WS_HEADER_BYTES = 256
 
@@ -62,7 +64,8 @@ _vp = _c.c_void_p
 
 class kvx_shape(_c.Structure):
     _fields_ = [("B", _c.c_int32), ("Hq", _c.c_int32), ("Hkv", _c.c_int32), ("D", _c.c_int32),
-                ("page_size", _c.c_int32), ("num_groups", _c.c_int32), ("dtype", _c.c_int32)]
+                ("page_size", _c.c_int32), ("num_groups", _c.c_int32), ("dtype", _c.c_int32),
+                ("layout", _c.c_int32)]
 
 
 class kvx_plan_stats(_c.Structure):
@@ -215,8 +218,8 @@ class Plan:
 
 def kvx_plan_create(B, Hq, Hkv, D, page_size, num_groups, dtype, head_budget, seq_len,
                     head_group, num_ctas=0, policy=KVX_PLAN_BALANCED,
-                    kernel=KVX_KERNEL_AUTO) -> Plan:
-    shape = kvx_shape(B, Hq, Hkv, D, page_size, num_groups, dtype)
+                    kernel=KVX_KERNEL_AUTO, layout=KVX_LAYOUT_HEAD_MAJOR) -> Plan:
+    shape = kvx_shape(B, Hq, Hkv, D, page_size, num_groups, dtype, layout)
     hb, sl, hg = _i32(head_budget).reshape(-1), _i32(seq_len).reshape(-1), _i32(head_group)
     h = _vp()
     rc = lib.kvx_plan_create(_c.byref(shape), hb.ctypes.data, sl.ctypes.data, hg.ctypes.data,

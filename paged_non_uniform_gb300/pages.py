@@ -6,8 +6,10 @@ pages, [pages][|G|][P][D] per K and per V, and its own page table per
 sequence. All heads of a group walk the same pages; head h of G owns slot
 row r(h) (its rank within G, ascending head order) of every page. Token t of
 head (b, h) -- the head's t-th kept token in ascending position -- lives at
-page page_table[G][b][t // P], row r(h), slot t % P. Slots past a head's
-kept count are padding and are never read.
+page page_table[G][b][t // P], row r(h), slot t % P. A page is laid out
+[|G|][P][D] (head-major) or [P][|G|][D] (token-major, the block layout of
+"KV-RM: Regularizing KV-Cache Movement for Static-Graph LLM Serving"). Slots
+past a head's kept count are padding and are never read.
 
 These helpers assign physical pages to sequences (any permutation of a group's
 pages is valid: the result does not depend on where pages sit) and pack dense
@@ -66,21 +68,23 @@ def assign_pages(group_pages: np.ndarray, perms=None, spare_pages: int = 0):
 
 
 def pack_pools(k_dense, v_dense, kept, head_group, page_tables, pool_pages, P,
-               out_dtype=np.float32, fill=np.nan):
+               out_dtype=np.float32, fill=np.nan, token_major=False):
     """Scatter dense kept rows into head-group pools.
 
     k_dense, v_dense: [B][Hkv][Lmax][D] arrays already holding values of the
     storage type; kept: B*Hkv index arrays (ascending positions kept by each
     head); out_dtype: np.float32, or np.uint16 for bf16 bit patterns (then
     k_dense / v_dense must be uint16 too). Padding slots get `fill`.
-    Returns a list of (k_pool, v_pool), each [pool_pages][|G|][P][D].
+    Returns a list of (k_pool, v_pool), each [pool_pages][|G|][P][D]
+    (head-major) or [pool_pages][P][|G|][D] (token_major=True).
     """
     B, Hkv, _, D = k_dense.shape
     hg = np.asarray(head_group, dtype=np.int32)
     rows, sizes = head_rows(hg), group_sizes(hg)
     pools = []
     for g in range(len(page_tables)):
-        shape = (pool_pages[g], int(sizes[g]), P, D)
+        shape = ((pool_pages[g], P, int(sizes[g]), D) if token_major
+                 else (pool_pages[g], int(sizes[g]), P, D))
         if out_dtype == np.uint16:
             fillv = np.uint16(0x7FC0) if (isinstance(fill, float) and np.isnan(fill)) else np.uint16(fill)
             kp = np.full(shape, fillv, dtype=np.uint16)
@@ -96,6 +100,10 @@ def pack_pools(k_dense, v_dense, kept, head_group, page_tables, pool_pages, P,
             if np.any(pages < 0):
                 raise ValueError("page table shorter than the kept tokens")
             kp, vp = pools[g]
-            kp[pages, r, t % P] = k_dense[b, h, ix]
-            vp[pages, r, t % P] = v_dense[b, h, ix]
+            if token_major:
+                kp[pages, t % P, r] = k_dense[b, h, ix]
+                vp[pages, t % P, r] = v_dense[b, h, ix]
+            else:
+                kp[pages, r, t % P] = k_dense[b, h, ix]
+                vp[pages, r, t % P] = v_dense[b, h, ix]
     return pools

@@ -21,11 +21,11 @@ def num_groups(case) -> int:
 
 
 def make_plan(case, num_ctas=0, policy=kvx.KVX_PLAN_BALANCED, kernel=kvx.KVX_KERNEL_AUTO,
-              upload=True):
+              upload=True, layout=kvx.KVX_LAYOUT_HEAD_MAJOR):
     dtype = kvx.KVX_BF16 if case.dtype == "bf16" else kvx.KVX_F32
     plan = kvx.kvx_plan_create(case.B, case.Hq, case.Hkv, case.D, case.P, num_groups(case),
                                dtype, case.budget, case.seq_len, case.head_group, num_ctas,
-                               policy, kernel)
+                               policy, kernel, layout)
     if upload:
         kvx.kvx_plan_upload(plan)
     return plan
@@ -43,15 +43,16 @@ class DeviceCase:
                  for g in range(G)]
         self.tables, self.pool_pages = pages.assign_pages(gp, perms, spare_pages)
         k, v = (case.k, case.v) if dense_override is None else dense_override
+        tm = plan.shape.layout == kvx.KVX_LAYOUT_TOKEN_MAJOR
         if case.dtype == "bf16":
             kb, vb = synth.f32_to_bf16_bits(k), synth.f32_to_bf16_bits(v)
             pools = pages.pack_pools(kb, vb, case.kept, case.head_group, self.tables,
-                                     self.pool_pages, case.P, np.uint16, fill)
+                                     self.pool_pages, case.P, np.uint16, fill, token_major=tm)
             conv = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
             self.q = conv(synth.f32_to_bf16_bits(case.q))
         else:
             pools = pages.pack_pools(k, v, case.kept, case.head_group, self.tables,
-                                     self.pool_pages, case.P, np.float32, fill)
+                                     self.pool_pages, case.P, np.float32, fill, token_major=tm)
             conv = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
             self.q = conv(case.q)
         self.k_pools = [conv(kp) for kp, _ in pools]

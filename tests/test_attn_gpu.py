@@ -237,3 +237,22 @@ def test_stall_hook_rejects_bad_limits():
     for bad in (0, 999_999, 20_000_000_000):
         with pytest.raises(kvx.KvxError):
             plan.inject_stall(0, bad)
+
+
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+@pytest.mark.parametrize("name", ["qwen3_like", "qwen25_like", "g8_p8", "p64", "d64"])
+def test_token_major_pages_match_head_major_bit_for_bit(kernel, name):
+    """KV-RM's token-major block layout and the head-major head-group page give
+    the same bits: the kernels stage both into the same shared-memory tiles."""
+    case = BF16_CASES[name]()
+    a = DeviceCase(case, make_plan(case, num_ctas=9, kernel=kernel)).run()
+    b = DeviceCase(case, make_plan(case, num_ctas=9, kernel=kernel,
+                                   layout=kvx.KVX_LAYOUT_TOKEN_MAJOR), perm_seed=3).run()
+    assert np.array_equal(a, b)
+    assert max_abs(b, oracle_out(case)) <= TOL_BF16
+
+
+def test_token_major_fp32_tiny():
+    case = synth.tiny(0, "one")
+    got = DeviceCase(case, make_plan(case, num_ctas=3, layout=kvx.KVX_LAYOUT_TOKEN_MAJOR)).run()
+    assert max_abs(got, oracle_out(case)) <= TOL_F32
