@@ -44,6 +44,7 @@ def parse():
                     choices=["qwen3_4b", "qwen3_4b_32k", "qwen25_32b", "llama3_sparse"])
     ap.add_argument("--no-gather", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-group-sweep", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -424,6 +425,11 @@ def run_ours(args, rank, world):
     e2e_ms = max_over_ranks((time.perf_counter() - h0) * 1e3 / e2e_steps, dist, dev)
     e2e_value = job_rate(bytes_job, e2e_ms)
 
+    # ---- head-group size sweep (first layers of the same workload)
+    gsweep = None
+    if rank == 0 and not args.no_group_sweep:
+        gsweep = group_sweep(cfg, table, dev, stream, peak, kvx, torch)
+
     # ---- gather (KV-RM movement workload)
     gather = None
     if not args.no_gather:
@@ -465,6 +471,7 @@ def run_ours(args, rank, world):
             "plan_host_us_per_layer": float(np.mean(plan_us)),
             "gather": gather,
             "balance": balance,
+            "group_sweep": gsweep,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -515,6 +522,60 @@ def measure_balance(cfg, lay, ws, stream, kvx, torch):
                      "tokens_per_block_max": int(st["max_cta_tokens"]),
                      "plan_host_us": float(st["plan_us"])}
         p.destroy()
+    return res
+
+
+def group_sweep(cfg0, table, dev, stream, peak, kvx, torch, layers=4, reps=20):
+    """Head-group size G (KV heads sharing one page table) against page
+    fragmentation, page-table entries, footprint and kernel throughput, over
+    the first `layers` layers (Tangram Figs. 8(c) and 11; G = Hkv is the
+    unified page)."""
+    from synth.device import TableLayer
+    res = {}
+    for G in (1, 2, 4, 8):
+        if cfg0.Hkv % G:
+            continue
+        cfg = synth.regroup(cfg0, G)
+        plans, lays, alloc, used, entries = [], [], 0, 0, 0
+        for l in range(layers):
+            p = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                                    kvx.KVX_BF16, cfg.budget[l], cfg.seq_len, cfg.head_group[l], 0)
+            kvx.kvx_plan_upload(p)
+            st = p.stats()
+            alloc += st["slots_allocated"]
+            used += st["slots_used"]
+            entries += int(p.group_pages().sum())
+            plans.append(p)
+            lays.append(TableLayer(cfg, l, table, p.group_pages(), seed=0))
+        ws = torch.zeros(max(p.workspace_bytes() for p in plans) // 4 + 64, dtype=torch.int32,
+                         device=dev)
+        out = torch.empty((cfg.B, cfg.Hq, cfg.D), dtype=torch.float32, device=dev)
+
+        def step():
+            for l in range(layers):
+                L = lays[l]
+                kvx.kvx_decode_attn(plans[l], L.q, L.k_pools, L.v_pools, L.pool_pages, L.pt,
+                                    L.strides, L.budget, L.seq_len, 0.0, out, ws, stream=stream)
+        for _ in range(3):
+            step()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        assert kvx.kvx_workspace_status(ws) == 0
+        ms = a.elapsed_time(b) / reps
+        kvb = sum(cfg.kv_bytes_layer(l) for l in range(layers))
+        res[f"G{G}"] = {"groups_per_layer": cfg.num_groups,
+                        "fragmentation": 1.0 - used / alloc,
+                        "footprint_gb": alloc * 2 * cfg.D * 2 / 1e9,
+                        "page_table_entries": entries,
+                        "kv_gbs": kvb / (ms * 1e-3) / 1e9,
+                        "frac": kvb / (ms * 1e-3) / 1e9 / peak}
+        del plans, lays, ws
+        torch.cuda.empty_cache()
     return res
 
 

@@ -195,6 +195,26 @@ def groups_by_budget(rate: np.ndarray, cuts) -> np.ndarray:
     return hg
 
 
+def regroup(cfg: "DecodeConfig", heads_per_group: int) -> "DecodeConfig":
+    """The same workload with head groups of `heads_per_group` KV heads each:
+    per layer, heads sorted by retention (descending, ties to the lower id) and
+    cut into equal groups. heads_per_group = Hkv is one unified page over all
+    heads; 1 gives every head its own page table."""
+    import copy
+    G = heads_per_group
+    if cfg.Hkv % G:
+        raise ValueError("heads_per_group must divide Hkv")
+    out = copy.copy(cfg)
+    hg = np.zeros_like(cfg.head_group)
+    for layer in range(cfg.layers):
+        rate = cfg.n[layer].astype(np.float64).sum(0) / cfg.seq_len.astype(np.float64).sum()
+        hg[layer] = groups_by_budget(rate, [G] * (cfg.Hkv // G))
+    out.head_group = hg
+    out.num_groups = cfg.Hkv // G
+    out.name = f"{cfg.name}_G{G}"
+    return out
+
+
 def _rate_to_count(rate: float, L: int) -> int:
     return min(L, max(1, int(math.ceil(rate * L))))
 

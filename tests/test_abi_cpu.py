@@ -172,3 +172,21 @@ def test_gather_rejects_bad_arguments(kvx):
     # unknown flag
     rc = kvx.lib.kvx_gather_coalesce(256, 256, 2, 4, 1, p, 8, 32, p, 128, 8, 256, ws, None)
     assert rc == kvx.KVX_EINVAL
+
+
+def test_group_size_trades_fragmentation_for_tables(kvx, orc):
+    """Larger head groups mean fewer page-table entries but more padding slots;
+    the planner's counts follow the oracle's page counts for every G."""
+    cfg = synth.decode_config("qwen3_4b", seed=0, layers=1)
+    frag, entries = [], []
+    for G in (1, 2, 4, 8):
+        c = synth.regroup(cfg, G)
+        plan = kvx.kvx_plan_create(c.B, c.Hq, c.Hkv, c.D, c.P, c.num_groups, kvx.KVX_BF16,
+                                   c.budget[0], c.seq_len, c.head_group[0], 152)
+        pages = orc.group_pages(c.n[0], c.head_group[0], c.P)
+        assert np.array_equal(plan.group_pages(), pages)
+        st = plan.stats()
+        frag.append(1 - st["slots_used"] / st["slots_allocated"])
+        entries.append(int(pages.sum()))
+    assert frag == sorted(frag) and frag[0] < frag[-1]
+    assert entries == sorted(entries, reverse=True)

@@ -118,7 +118,8 @@ def test_page_size_and_grouping_invariance():
     base = qwen3_like(3)
     ref = oracle_out(base)
     for P in (16, 32):
-        for hg in ([0, 1, 2, 3, 4, 5, 6, 7], [0] * 8, list(base.head_group)):
+        for hg in ([0, 1, 2, 3, 4, 5, 6, 7], [0, 0, 1, 1, 2, 2, 3, 3], [0, 0, 0, 0, 1, 1, 1, 1],
+                   [0] * 8, list(base.head_group)):
             case = synth.dense_case(base.B, base.Hq, base.Hkv, base.D, base.seq_len, base.n,
                                     "bf16", seed=3, P=P, head_group=hg)
             got = DeviceCase(case, make_plan(case)).run()
