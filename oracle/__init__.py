@@ -70,6 +70,8 @@ class Oracle:
         lib.oracle_runs.restype = _c.c_int64
         lib.oracle_gather.argtypes = [_c.c_int, _c.c_int, _I32, _I32, _U8, _c.c_int64,
                                       _c.c_int64, _U8, _c.c_int64, _c.c_int]
+        lib.oracle_select_topk.argtypes = [_c.c_int, _c.c_int, _c.c_int, _F64, _F64, _c.c_int,
+                                           _c.c_int, _I32, _c.c_void_p]
         lib.oracle_num_threads.restype = _c.c_int
         self.lib = lib
 
@@ -180,6 +182,21 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_gather: invalid arguments")
         return staging
+
+    # -- sparse selection --------------------------------------------
+    def select_topk(self, q, k, top, recent, want_scores=False):
+        """q: [g][D]; k: [L][D]. Returns ascending kept positions (and scores)."""
+        q = np.ascontiguousarray(q, dtype=np.float64)
+        k = np.ascontiguousarray(k, dtype=np.float64)
+        g, D = q.shape
+        L = k.shape[0]
+        kept = np.zeros(max(top + recent, 1), dtype=np.int32)
+        sc = np.zeros(L, dtype=np.float64) if want_scores else None
+        n = self.lib.oracle_select_topk(L, D, g, q, k, int(top), int(recent), kept,
+                                        sc.ctypes.data if sc is not None else None)
+        if n < 0:
+            raise ValueError("oracle_select_topk: invalid arguments")
+        return (kept[:n], sc) if want_scores else kept[:n]
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())

@@ -336,3 +336,68 @@ int oracle_gather(int S, int max_blocks, const int32_t *bt, const int32_t *nb,
   }
   return 0;
 }
+
+/* KVDrive, Fig. 7 / Fig. 16: the critical KV entries of a head are those
+ * with the largest attention scores; the grouped query heads of one KV head
+ * score a token by the sum of their dot products, i.e. <k_t, sum_j q_j>. */
+typedef struct {
+  double s;
+  int32_t t;
+} oracle_scored;
+
+static int oracle_cmp_scored(const void *a, const void *b) {
+  const oracle_scored *x = (const oracle_scored *)a, *y = (const oracle_scored *)b;
+  if (x->s != y->s) return x->s > y->s ? -1 : 1; /* larger score first */
+#if ORACLE_MUTANT == 16
+  return x->t > y->t ? -1 : (x->t < y->t); /* ties: higher position first */
+#else
+  return x->t < y->t ? -1 : (x->t > y->t); /* ties: lower position first */
+#endif
+}
+
+static int oracle_cmp_i32(const void *a, const void *b) {
+  const int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+  return x < y ? -1 : (x > y);
+}
+
+int oracle_select_topk(int L, int D, int g, const double *q, const double *k,
+                       int top, int recent, int32_t *kept, double *scores) {
+  if (L <= 0 || D <= 0 || g <= 0 || top < 0 || recent < 0 || !q || !k || !kept)
+    return -1;
+  double *Q = (double *)calloc((size_t)D, sizeof(double));
+  if (!Q) return -1;
+#if ORACLE_MUTANT == 17
+  for (int d = 0; d < D; ++d) Q[d] = q[d]; /* only the first query head */
+#else
+  for (int j = 0; j < g; ++j)
+    for (int d = 0; d < D; ++d) Q[d] += q[(size_t)j * D + d];
+#endif
+  const int n = L - recent > 0 ? L - recent : 0;
+  oracle_scored *c = (oracle_scored *)malloc(sizeof(oracle_scored) * (size_t)(n > 0 ? n : 1));
+  if (!c) {
+    free(Q);
+    return -1;
+  }
+  for (int t = 0; t < n; ++t) {
+    double s = 0.0;
+    for (int d = 0; d < D; ++d) s += k[(size_t)t * D + d] * Q[d];
+    c[t].s = s;
+    c[t].t = t;
+  }
+  if (scores) {
+    for (int t = 0; t < L; ++t) scores[t] = t < n ? c[t].s : 0.0;
+  }
+  qsort(c, (size_t)n, sizeof(oracle_scored), oracle_cmp_scored);
+  const int ntop = top < n ? top : n;
+  int cnt = 0;
+  for (int i = 0; i < ntop; ++i) kept[cnt++] = c[i].t;
+#if ORACLE_MUTANT == 18
+  for (int t = n + 1; t < L; ++t) kept[cnt++] = t; /* recent window one short */
+#else
+  for (int t = n; t < L; ++t) kept[cnt++] = t;
+#endif
+  qsort(kept, (size_t)cnt, sizeof(int32_t), oracle_cmp_i32);
+  free(c);
+  free(Q);
+  return cnt;
+}

@@ -107,6 +107,19 @@ int oracle_gather(int S, int max_blocks, const int32_t *bt, const int32_t *nb,
                   const uint8_t *pool, int64_t num_phys, int64_t block_bytes,
                   uint8_t *staging, int64_t row_bytes, int zero_tail);
 
+/* Kept set of one KV head for sparse long-context decode ("KVDrive", Fig. 7
+ * and Fig. 16: attention over the critical top-K entries plus a recent
+ * window). With Q = sum of the head's g query vectors,
+ *   score_t = <k_t, Q> for t in [0, L - recent),
+ *   kept = the min(top, L - recent) positions with the largest scores (equal
+ *          scores: lower position first) and every position of
+ *          [max(0, L - recent), L), in ascending order.
+ * q: [g][D]; k: [L][D]; kept: room for top + recent entries; scores
+ * (optional, may be NULL): [L], score_t for t < L - recent, 0 after.
+ * Returns the number of kept positions, or -1. */
+int oracle_select_topk(int L, int D, int g, const double *q, const double *k,
+                       int top, int recent, int32_t *kept, double *scores);
+
 /* Number of OpenMP threads the oracle uses (1 without OpenMP). */
 int oracle_num_threads(void);
 

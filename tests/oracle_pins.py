@@ -332,6 +332,48 @@ def pin_gather_stamped_blocks(orc):
         assert not blocks[cfg.nb[s]:].any()
 
 
+# ------------------------------------------------------ sparse selection
+def pin_select_closed_form(orc):
+    """Keys along one axis with known scores: the kept set is the top positions
+    by that coordinate plus the recent window, ascending."""
+    L, D, top, recent = 40, 8, 5, 3
+    q = np.zeros((2, D))
+    q[0, 2], q[1, 2] = 1.5, 0.5          # Q = 2 e_2 (sum of the two query heads)
+    c = synth.rng(13).permutation(L).astype(np.float64)
+    k = np.zeros((L, D))
+    k[:, 2] = c
+    kept = orc.select_topk(q, k, top, recent)
+    cand = np.arange(L - recent)
+    best = cand[np.argsort(-c[cand])[:top]]
+    expect = np.sort(np.concatenate([best, np.arange(L - recent, L)]))
+    assert np.array_equal(kept, expect), (kept, expect)
+
+
+def pin_select_ties_and_edges(orc):
+    D = 4
+    q = np.array([[1.0, -2.0, 0.5, 0.0], [-1.0, 2.0, -0.5, 0.0]])  # Q = 0: every score ties
+    k = synth.rng(14).standard_normal((30, D))
+    assert np.array_equal(orc.select_topk(q, k, 4, 2), [0, 1, 2, 3, 28, 29])
+    # budget at least the candidates: everything is kept
+    assert np.array_equal(orc.select_topk(q, k, 40, 2), np.arange(30))
+    # sequence shorter than the recent window: everything is kept
+    assert np.array_equal(orc.select_topk(q, k[:3], 4, 5), np.arange(3))
+
+
+def pin_select_permutation_equivariance(orc):
+    """Relabelling token positions (away from the recent window) relabels the
+    selection; the recent window stays."""
+    gen = synth.rng(15)
+    L, D, top, recent = 60, 16, 7, 4
+    q = gen.standard_normal((4, D))
+    k = gen.standard_normal((L, D))
+    perm = np.concatenate([gen.permutation(L - recent), np.arange(L - recent, L)])
+    a = orc.select_topk(q, k, top, recent)
+    inv = np.argsort(perm)
+    b = orc.select_topk(q, k[perm], top, recent)
+    assert np.array_equal(np.sort(perm[b]), a)
+
+
 ALL_PINS = [
     pin_golden_two_token, pin_golden_kept_subset, pin_full_budget_equals_sdpa,
     pin_subset_equals_sdpa_on_kept_rows, pin_single_token, pin_equal_keys_give_mean,
@@ -339,4 +381,5 @@ ALL_PINS = [
     pin_weights_sum_to_one, pin_scale_invariance, pin_gqa_mapping,
     pin_budget_resolution, pin_group_pages, pin_footprint, pin_plan_coverage,
     pin_gather_golden, pin_runs_golden, pin_runs_closed_form, pin_gather_stamped_blocks,
+    pin_select_closed_form, pin_select_ties_and_edges, pin_select_permutation_equivariance,
 ]

@@ -23,6 +23,9 @@ MUTANTS = {
     13: "gather copies one stale block past num_blocks",
     14: "coverage ignores tokens past n",
     15: "budget resolved with max instead of min",
+    16: "selection ties broken toward the higher position",
+    17: "selection scores with the first query head only",
+    18: "recent window one token short",
 }
 
 
