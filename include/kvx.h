@@ -308,6 +308,57 @@ int kvx_gather_read_runs(const void *workspace, int32_t S, int32_t max_blocks,
                          int32_t *run_count, int32_t *runs);
 
 /* ---------------------------------------------------------------------------
+ * kvx_select_topk -- kept-set selection for sparse long-context decode
+ * ("KVDrive", Fig. 7 and Fig. 16: decode attends to the top-K critical KV
+ * entries of each head; here together with a recent window).
+ *
+ * For sequence b and KV head h, with Q = the sum of h's g = Hq/Hkv query
+ * vectors (the grouped query heads score a token by the sum of their dot
+ * products):
+ *     score_t = <k_t, Q>   (fp32)            for t < L_b - recent,
+ *     kept    = the min(top, L_b - recent) largest scores (equal scores:
+ *               lower position first), then [max(0, L_b - recent), L_b);
+ *               ascending positions.
+ *   keys        device bf16 [B][Hkv][Lmax][D], D = 64 or 128, 16-byte aligned.
+ *   q           device bf16 [B][Hq][D].
+ *   seq_len     device int32 [B], each in [1, Lmax].
+ *   kept_idx    device int32 [B*Hkv][top + recent]; entries past the count
+ *               are set to -1.
+ *   kept_count  device int32 [B*Hkv].
+ *   workspace   device, >= kvx_select_workspace_bytes(B, Hkv, Lmax), 256-byte
+ *               aligned (holds the scores).
+ * The cut is decided on fp32 scores: positions whose scores lie within fp32
+ * rounding of the cut may be exchanged with respect to an exact selection.
+ * ------------------------------------------------------------------------- */
+int kvx_select_workspace_bytes(int32_t B, int32_t Hkv, int32_t Lmax, size_t *bytes);
+
+int kvx_select_topk(const void *keys, const void *q, const int32_t *seq_len,
+                    int32_t B, int32_t Hq, int32_t Hkv, int32_t D, int32_t Lmax,
+                    int32_t top, int32_t recent, int32_t *kept_idx,
+                    int32_t *kept_count, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* ---------------------------------------------------------------------------
+ * kvx_pack_kept -- compaction of kept rows into head-group pages (Tangram,
+ * Fig. 8(b)). For every head (b, h) of the plan and i < n[b][h] (the plan's
+ * kept count), copies row kept_idx[(b*Hkv + h) * kept_stride + i] of the
+ * dense keys and values into token i of the head's pages, with the plan's
+ * page layout and groups (same addressing as kvx_decode_attn).
+ *   keys, values  device bf16 [B][Hkv][Lmax][D], 16-byte aligned.
+ *   pools, page tables: as for kvx_decode_attn (written here).
+ *   workspace     device, >= KVX_WS_HEADER_BYTES: its status word collects
+ *                 KVX_DEV_BAD_BLOCK (a kept index outside [0, Lmax)) and
+ *                 KVX_DEV_BAD_PAGE; such rows are not copied.
+ * Errors: KVX_EINVAL, KVX_ERANGE, KVX_ESTATE, KVX_EUNSUPPORTED (fp32 plans).
+ * ------------------------------------------------------------------------- */
+int kvx_pack_kept(const kvx_plan *plan, const void *keys, const void *values,
+                  int32_t Lmax, const int32_t *kept_idx, int32_t kept_stride,
+                  void *const *k_pools, void *const *v_pools,
+                  const int64_t *pool_pages, const int32_t *const *page_tables,
+                  const int32_t *page_table_stride, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * kvx_gather_coalesce_noalloc -- kvx_gather_coalesce without a workspace.
  *
  * The pages have no counterpart of this entry point: it exists for callers

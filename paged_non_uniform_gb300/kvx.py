@@ -102,6 +102,13 @@ lib.kvx_gather_coalesce.argtypes = [_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32
                                     _c.c_int64, _c.c_int64, _vp, _c.c_int64, _c.c_int32, _vp,
                                     _c.c_size_t, _vp]
 lib.kvx_gather_read_runs.argtypes = [_vp, _c.c_int32, _c.c_int32, _vp, _vp]
+lib.kvx_select_workspace_bytes.argtypes = [_c.c_int32, _c.c_int32, _c.c_int32,
+                                           _c.POINTER(_c.c_size_t)]
+lib.kvx_select_topk.argtypes = [_vp, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32,
+                                _c.c_int32, _c.c_int32, _c.c_int32, _vp, _vp, _vp, _c.c_size_t,
+                                _vp]
+lib.kvx_pack_kept.argtypes = [_vp, _vp, _vp, _c.c_int32, _vp, _c.c_int32, _vp, _vp, _vp, _vp,
+                              _vp, _vp, _c.c_size_t, _vp]
 lib.kvx_gather_coalesce_noalloc.argtypes = [_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _vp,
                                             _c.c_int64, _c.c_int64, _vp, _c.c_int64,
                                             _c.c_int32, _vp, _vp]
@@ -296,6 +303,38 @@ def kvx_gather_read_runs(workspace, S: int, max_blocks: int):
     _check(lib.kvx_gather_read_runs(_dptr(workspace), int(S), int(max_blocks), cnt.ctypes.data,
                                     runs.ctypes.data), "kvx_gather_read_runs")
     return cnt[:S], runs[:S]
+
+
+def kvx_select_workspace_bytes(B: int, Hkv: int, Lmax: int) -> int:
+    v = _c.c_size_t(0)
+    _check(lib.kvx_select_workspace_bytes(int(B), int(Hkv), int(Lmax), _c.byref(v)),
+           "kvx_select_workspace_bytes")
+    return int(v.value)
+
+
+def kvx_select_topk(keys, q, seq_len, B, Hq, Hkv, D, Lmax, top, recent, kept_idx, kept_count,
+                    workspace, workspace_bytes=None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib.kvx_select_topk(_dptr(keys), _dptr(q), _dptr(seq_len), int(B), int(Hq), int(Hkv),
+                             int(D), int(Lmax), int(top), int(recent), _dptr(kept_idx),
+                             _dptr(kept_count), _dptr(workspace), int(workspace_bytes),
+                             _stream(stream))
+    _check(rc, "kvx_select_topk")
+
+
+def kvx_pack_kept(plan: Plan, keys, values, Lmax, kept_idx, kept_stride, k_pools, v_pools,
+                  pool_pages, page_tables, page_table_stride, workspace, workspace_bytes=None,
+                  stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    pp = np.ascontiguousarray(np.asarray(pool_pages, dtype=np.int64))
+    ps = _i32(page_table_stride)
+    rc = lib.kvx_pack_kept(plan.handle, _dptr(keys), _dptr(values), int(Lmax), _dptr(kept_idx),
+                           int(kept_stride), _ptr_array(k_pools), _ptr_array(v_pools),
+                           pp.ctypes.data, _ptr_array(page_tables), ps.ctypes.data,
+                           _dptr(workspace), int(workspace_bytes), _stream(stream))
+    _check(rc, "kvx_pack_kept")
 
 
 def kvx_gather_coalesce_noalloc(block_table, num_blocks, S, max_blocks, pools, num_phys_blocks,

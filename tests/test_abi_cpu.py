@@ -190,3 +190,21 @@ def test_group_size_trades_fragmentation_for_tables(kvx, orc):
         entries.append(int(pages.sum()))
     assert frag == sorted(frag) and frag[0] < frag[-1]
     assert entries == sorted(entries, reverse=True)
+
+
+def test_select_and_pack_reject_bad_arguments(kvx):
+    ws = kvx.kvx_select_workspace_bytes(2, 2, 100)
+    assert ws == kvx.KVX_WS_HEADER_BYTES + 4 * 2 * 2 * 100
+    rc = kvx.lib.kvx_select_topk(256, 256, 256, 2, 8, 2, 96, 100, 10, 4, 256, 256, 256, ws, None)
+    assert rc == kvx.KVX_EUNSUPPORTED
+    rc = kvx.lib.kvx_select_topk(256, 256, 256, 2, 7, 2, 128, 100, 10, 4, 256, 256, 256, ws, None)
+    assert rc == kvx.KVX_EINVAL
+    rc = kvx.lib.kvx_select_topk(256, 256, 256, 2, 8, 2, 128, 100, 10, 4, 256, 256, 256, 16, None)
+    assert rc == kvx.KVX_EINVAL
+    case = synth.tiny(0)
+    plan = _plan(kvx, case, num_ctas=2)
+    p = (kvx._vp * 2)(256, 256)
+    rc = kvx.lib.kvx_pack_kept(plan.handle, 256, 256, 100, 256, 100, p, p,
+                               np.array([4, 4], np.int64).ctypes.data, p,
+                               np.array([8, 8], np.int32).ctypes.data, 256, 256, None)
+    assert rc == kvx.KVX_ESTATE

@@ -1,0 +1,171 @@
+"""Sparse kept-set selection (kvx_select_topk), page packing (kvx_pack_kept)
+and attention over the packed pages, against the fp64 oracle.
+
+The cut is decided on fp32 scores, the oracle decides it on fp64 scores. The
+unique part is compared exactly: every position whose score lies outside the
+fp32 error band around the cut must be kept or dropped as the oracle decides;
+positions inside the band may be exchanged, and the counts must agree. The
+band is rigorous: for <k, Q> with Q = sum_j q_j summed in fp32,
+|fl(score) - score| <= gamma_D * sum_d |k_d Q_d| + 3u * sum_d |k_d| sum_j |q_jd|,
+u = 2^-24, gamma_D = D u / (1 - D u).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from paged_non_uniform_gb300 import kvx, pages
+
+pytestmark = pytest.mark.gpu
+U = 2.0 ** -24
+
+
+def _bf16(a):
+    return torch.from_numpy(synth.f32_to_bf16_bits(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def make(seed, B, Hq, Hkv, D, L, const_keys=False):
+    g = synth.rng(seed)
+    Lmax = int(max(L))
+    q = synth.normal(g, (B, Hq, D), "bf16")
+    k = synth.normal(g, (B, Hkv, Lmax, D), "bf16")
+    v = synth.normal(g, (B, Hkv, Lmax, D), "bf16")
+    if const_keys:
+        k[:] = k[:, :, :1]
+    return q, k, v, np.asarray(L, np.int32)
+
+
+def gpu_select(q, k, L, top, recent):
+    B, Hq, D = q.shape
+    Hkv, Lmax = k.shape[1], k.shape[2]
+    kept = torch.full((B * Hkv, top + recent), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(B * Hkv, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(kvx.kvx_select_workspace_bytes(B, Hkv, Lmax) // 4 + 64, dtype=torch.int32,
+                     device="cuda")
+    kvx.kvx_select_topk(_bf16(k), _bf16(q), torch.from_numpy(L).cuda(), B, Hq, Hkv, D, Lmax,
+                        top, recent, kept, cnt, ws)
+    torch.cuda.synchronize()
+    return kept.cpu().numpy(), cnt.cpu().numpy()
+
+
+def check_head(orc, qh, kh, top, recent, got):
+    """got: GPU kept positions of one head. Returns True if equal to the oracle's."""
+    ref, sc = orc.select_topk(qh, kh, top, recent, want_scores=True)
+    assert got.size == ref.size
+    assert np.all(np.diff(got) > 0)
+    L = kh.shape[0]
+    n = max(0, L - recent)
+    assert np.array_equal(got[got >= n], np.arange(n, L))
+    if np.array_equal(got, ref):
+        return True
+    D = kh.shape[1]
+    Q = qh.astype(np.float64).sum(0)
+    gam = D * U / (1 - D * U)
+    eps = gam * np.abs(kh[:n]) @ np.abs(Q) + 3 * U * np.abs(kh[:n]) @ np.abs(qh).sum(0)
+    thr = np.sort(sc[:n])[::-1][min(top, n) - 1]
+    amb = np.abs(sc[:n] - thr) <= eps + eps.max()
+    diff = np.setxor1d(got, ref)
+    assert np.all(amb[diff]), diff[~amb[diff]]
+    return False
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_selection_matches_oracle(D):
+    q, k, v, L = make(1, 3, 16, 4, D, [5000, 3100, 700])
+    top, recent = 300, 64
+    kept, cnt = gpu_select(q, k, L, top, recent)
+    orc = oracle.load()
+    same = 0
+    for b in range(3):
+        for h in range(4):
+            bh = b * 4 + h
+            c = int(cnt[bh])
+            assert c == min(top, L[b] - recent) + min(recent, L[b])
+            assert np.all(kept[bh, c:] == -1)
+            same += check_head(orc, q[b, 4 * h:4 * h + 4], k[b, h, :L[b]], top, recent,
+                               kept[bh, :c])
+    assert same >= 10
+
+
+def test_selection_ties_and_edges():
+    orc = oracle.load()
+    # all keys of a head equal: every score ties, the lowest positions win
+    q, k, v, L = make(2, 2, 8, 2, 128, [900, 400], const_keys=True)
+    kept, cnt = gpu_select(q, k, L, 50, 10)
+    for bh in range(4):
+        b = bh // 2
+        exp = np.concatenate([np.arange(50), np.arange(L[b] - 10, L[b])])
+        assert np.array_equal(kept[bh, :cnt[bh]], exp)
+    # budget >= candidates, sequence shorter than the window, no top at all
+    q, k, v, L = make(3, 3, 8, 2, 128, [120, 5, 300])
+    for top, recent in ((200, 16), (0, 16), (10, 0)):
+        kept, cnt = gpu_select(q, k, L, top, recent)
+        for bh in range(6):
+            b = bh // 2
+            h = bh % 2
+            ref = orc.select_topk(q[b, 4 * h:4 * h + 4], k[b, h, :L[b]], top, recent)
+            assert cnt[bh] == ref.size
+            check_head(orc, q[b, 4 * h:4 * h + 4], k[b, h, :L[b]], top, recent,
+                       kept[bh, :cnt[bh]])
+
+
+@pytest.mark.parametrize("layout", [kvx.KVX_LAYOUT_HEAD_MAJOR, kvx.KVX_LAYOUT_TOKEN_MAJOR])
+def test_select_pack_attend_end_to_end(layout):
+    """GPU selection -> packing into head-group pages -> attention, against the
+    oracle's selection and attention, head by head where the kept sets agree;
+    the packed slots are compared bit for bit with the dense rows."""
+    B, Hq, Hkv, D, P = 2, 32, 8, 128, 16
+    top, recent = 512, 64
+    q, k, v, L = make(4, B, Hq, Hkv, D, [6000, 4000])
+    kept, cnt = gpu_select(q, k, L, top, recent)
+    n = cnt.reshape(B, Hkv)
+    hg = np.array([0, 0, 0, 0, 1, 1, 1, 1], np.int32)
+    plan = kvx.kvx_plan_create(B, Hq, Hkv, D, P, 2, kvx.KVX_BF16, n, L, hg, 11, layout=layout)
+    kvx.kvx_plan_upload(plan)
+    gp = plan.group_pages()
+    tables, npages = pages.assign_pages(gp, [synth.page_permutation(40 + i, int(gp[i].sum()) + 2)
+                                             for i in range(2)], 2)
+    sizes = pages.group_sizes(hg)
+    shape = (lambda i: (npages[i], P, int(sizes[i]), D)) if layout else \
+        (lambda i: (npages[i], int(sizes[i]), P, D))
+    kp = [torch.zeros(shape(i), dtype=torch.bfloat16, device="cuda") for i in range(2)]
+    vp = [torch.zeros(shape(i), dtype=torch.bfloat16, device="cuda") for i in range(2)]
+    pt = [torch.from_numpy(t).cuda() for t in tables]
+    ws = torch.zeros(plan.workspace_bytes() // 4 + 64, dtype=torch.int32, device="cuda")
+    kd, vd = _bf16(k), _bf16(v)
+    kvx.kvx_pack_kept(plan, kd, vd, k.shape[2], torch.from_numpy(kept).cuda(), top + recent, kp,
+                      vp, npages, pt, [t.shape[1] for t in tables], ws)
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    kvx.kvx_decode_attn(plan, _bf16(q), kp, vp, npages, pt, [t.shape[1] for t in tables],
+                        torch.from_numpy(n.reshape(-1).copy()).cuda(),
+                        torch.from_numpy(L).cuda(), 0.0, out, ws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    # packed slots: bit-exact copies of the dense rows the GPU selected
+    rows = pages.head_rows(hg)
+    kbits = synth.f32_to_bf16_bits(k)
+    kph = [p.view(torch.int16).cpu().numpy().view(np.uint16) for p in kp]
+    for b in range(B):
+        for h in range(Hkv):
+            gi, r = int(hg[h]), int(rows[h])
+            idx = kept[b * Hkv + h, :n[b, h]]
+            t = np.arange(idx.size)
+            pg = tables[gi][b, t // P]
+            slots = kph[gi][pg, t % P, r] if layout else kph[gi][pg, r, t % P]
+            assert np.array_equal(slots, kbits[b, h, idx])
+    orc = oracle.load()
+    g = Hq // Hkv
+    agree = 0
+    for b in range(B):
+        for h in range(Hkv):
+            qh, kh, vh = q[b, h * g:(h + 1) * g], k[b, h, :L[b]], v[b, h, :L[b]]
+            if check_head(orc, qh, kh, top, recent, kept[b * Hkv + h, :n[b, h]]):
+                agree += 1
+                ref_idx = orc.select_topk(qh, kh, top, recent)
+                ref = orc.attn_head(qh, kh, vh, ref_idx, 1.0 / math.sqrt(D))
+                assert np.abs(got[b, h * g:(h + 1) * g] - ref).max() <= 2e-3
+    assert agree >= 14
