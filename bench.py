@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--no-gather", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-group-sweep", action="store_true")
+    ap.add_argument("--no-sparse", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
 
@@ -430,6 +431,10 @@ def run_ours(args, rank, world):
     if rank == 0 and not args.no_group_sweep:
         gsweep = group_sweep(cfg, table, dev, stream, peak, kvx, torch)
 
+    sparse = None
+    if rank == 0 and not args.no_sparse:
+        sparse = sparse_select(dev, stream, peak, kvx, torch)
+
     # ---- gather (KV-RM movement workload)
     gather = None
     if not args.no_gather:
@@ -472,6 +477,7 @@ def run_ours(args, rank, world):
             "gather": gather,
             "balance": balance,
             "group_sweep": gsweep,
+            "sparse_select": sparse,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -576,6 +582,74 @@ def group_sweep(cfg0, table, dev, stream, peak, kvx, torch, layers=4, reps=20):
                         "frac": kvb / (ms * 1e-3) / 1e9 / peak}
         del plans, lays, ws
         torch.cuda.empty_cache()
+    return res
+
+
+def sparse_select(dev, stream, peak, kvx, torch, reps=10):
+    """The selection step before sparse decode on one layer of the Llama-3-8B
+    shaped workload (batch 8 x 122k, 32/8 heads): score every candidate key
+    against the summed GQA query and keep the top 2048 plus the last 128
+    (kvx_select_topk), pack the kept rows into pages (kvx_pack_kept), attend
+    (kvx_decode_attn). Dense keys and values are tiled from a value table."""
+    from synth.device import ValueTable
+    cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
+    B, Hq, Hkv, D, L, P = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, int(cfg.seq_len[0]), cfg.P
+    top, recent = 2048, 128
+    table = ValueTable(seed=31, rows=1 << 18, D=D, dtype="bf16", device=dev)
+    keys = torch.empty((B, Hkv, L, D), dtype=torch.bfloat16, device=dev)
+    vals = torch.empty_like(keys)
+    table.fill(keys, 11)
+    table.fill(vals, 77777)
+    q = torch.from_numpy(synth.f32_to_bf16_bits(synth.normal(synth.rng(5), (B, Hq, D), "bf16"))
+                         .view(np.int16)).view(torch.bfloat16).to(dev)
+    sl = torch.from_numpy(cfg.seq_len).to(dev)
+    kept = torch.zeros((B * Hkv, top + recent), dtype=torch.int32, device=dev)
+    cnt = torch.zeros(B * Hkv, dtype=torch.int32, device=dev)
+    sws = torch.zeros(kvx.kvx_select_workspace_bytes(B, Hkv, L) // 4 + 64, dtype=torch.int32,
+                      device=dev)
+    n = np.full((B, Hkv), top + recent, np.int32)
+    hg = np.zeros(Hkv, np.int32)
+    plan = kvx.kvx_plan_create(B, Hq, Hkv, D, P, 1, kvx.KVX_BF16, n, cfg.seq_len, hg, 0)
+    kvx.kvx_plan_upload(plan)
+    gp = plan.group_pages()
+    npages = [int(gp.sum())]
+    pt = torch.from_numpy(np.arange(npages[0], dtype=np.int32).reshape(B, -1)).to(dev)
+    kp = torch.empty((npages[0], Hkv, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    aws = torch.zeros(plan.workspace_bytes() // 4 + 64, dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    budget = torch.from_numpy(n.reshape(-1).copy()).to(dev)
+    stages = {
+        "select": lambda: kvx.kvx_select_topk(keys, q, sl, B, Hq, Hkv, D, L, top, recent, kept,
+                                              cnt, sws, stream=stream),
+        "pack": lambda: kvx.kvx_pack_kept(plan, keys, vals, L, kept, top + recent, [kp], [vp],
+                                          npages, [pt], [pt.shape[1]], aws, stream=stream),
+        "attention": lambda: kvx.kvx_decode_attn(plan, q, [kp], [vp], npages, [pt],
+                                                 [pt.shape[1]], budget, sl, 0.0, out, aws,
+                                                 stream=stream),
+    }
+    res = {"workload": f"1 layer, batch {B} x {L} tokens, {Hq} q / {Hkv} KV heads, D {D}, bf16; "
+                       f"keep top {top} + last {recent} per head"}
+    for name, fn in stages.items():
+        for _ in range(3):
+            fn()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = {"us": a.elapsed_time(b) / reps * 1e3}
+    key_bytes = B * Hkv * (L - recent) * D * 2
+    res["select"]["keys_gbs"] = key_bytes / (res["select"]["us"] * 1e-6) / 1e9
+    res["select"]["frac"] = res["select"]["keys_gbs"] / peak
+    kv_kept = B * Hkv * (top + recent) * D * 2 * 2
+    res["pack"]["gbs_read_write"] = 2 * kv_kept / (res["pack"]["us"] * 1e-6) / 1e9
+    res["attention"]["kv_gbs"] = kv_kept / (res["attention"]["us"] * 1e-6) / 1e9
+    assert kvx.kvx_workspace_status(aws) == 0 and kvx.kvx_workspace_status(sws) == 0
+    del keys, vals, kp, vp
+    torch.cuda.empty_cache()
     return res
 
 

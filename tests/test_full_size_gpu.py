@@ -94,3 +94,32 @@ def test_full_size_sparse_with_selected_tokens(table):
         ref = orc.attn_head(qh, K, V, kept, 1.0 / math.sqrt(cfg.D))
         err = float(np.abs(got[b, h * g:(h + 1) * g] - ref).max())
         assert err <= TOL, (b, h, err)
+
+
+def test_full_size_gpu_selection_sampled_heads(table):
+    """Batch 8 x 122k dense keys (Llama-3-8B shapes, one layer, tiled from the
+    value table): the GPU kept set of sampled heads against the oracle's
+    selection, outside the fp32 error band around the cut."""
+    from test_select_gpu import check_head
+    cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
+    B, Hq, Hkv, D, L = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, int(cfg.seq_len[0])
+    top, recent = 2048, 128
+    keys = torch.empty((B, Hkv, L, D), dtype=torch.bfloat16, device="cuda")
+    table.fill(keys, 4242)
+    q = synth.normal(synth.rng(99), (B, Hq, D), "bf16")
+    qd = torch.from_numpy(synth.f32_to_bf16_bits(q).view(np.int16)).view(torch.bfloat16).cuda()
+    kept = torch.zeros((B * Hkv, top + recent), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(B * Hkv, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(kvx.kvx_select_workspace_bytes(B, Hkv, L) // 4 + 64, dtype=torch.int32,
+                     device="cuda")
+    kvx.kvx_select_topk(keys, qd, torch.from_numpy(cfg.seq_len).cuda(), B, Hq, Hkv, D, L, top,
+                        recent, kept, cnt, ws)
+    torch.cuda.synchronize()
+    kept, cnt = kept.cpu().numpy(), cnt.cpu().numpy()
+    assert np.all(cnt == top + recent)
+    orc = oracle.load()
+    g = Hq // Hkv
+    for b, h in [(0, 0), (2, 5), (7, 7)]:
+        bh = b * Hkv + h
+        kh = table.host_rows(4242, bh * L + np.arange(L, dtype=np.int64))
+        check_head(orc, q[b, h * g:(h + 1) * g], kh, top, recent, kept[bh])
