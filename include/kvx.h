@@ -58,7 +58,8 @@ extern "C" {
 #define KVX_DEV_BAD_BUDGET 2u  /* min(seq_len, head_budget) differs from the plan */
 #define KVX_DEV_TIMEOUT 4u     /* a pipeline wait gave up after its time limit */
 #define KVX_DEV_BAD_BLOCK 8u   /* a block-table entry outside [0, num_phys_blocks) */
-#define KVX_DEV_BAD_LENGTH 16u /* num_blocks[s] outside [0, max_blocks] or the row */
+#define KVX_DEV_BAD_LENGTH 16u /* num_blocks[s] outside [0, max_blocks] or the row;
+                                  a selection seq_len outside [0, Lmax] */
 
 /* ---- element types --------------------------------------------------- */
 #define KVX_F32 0
@@ -319,14 +320,19 @@ int kvx_gather_read_runs(const void *workspace, int32_t S, int32_t max_blocks,
  *     kept    = the min(top, L_b - recent) largest scores (equal scores:
  *               lower position first), then [max(0, L_b - recent), L_b);
  *               ascending positions.
- *   keys        device bf16 [B][Hkv][Lmax][D], D = 64 or 128, 16-byte aligned.
+ *   keys        device bf16 [B][Hkv][Lmax][D], D = 64 or 128, 16-byte aligned;
+ *               Lmax <= 262144 (KVX_EUNSUPPORTED beyond).
  *   q           device bf16 [B][Hq][D].
- *   seq_len     device int32 [B], each in [1, Lmax].
+ *   seq_len     device int32 [B], each in [0, Lmax]; a length outside that
+ *               range selects nothing for its sequence (count 0) and sets
+ *               KVX_DEV_BAD_LENGTH in the workspace status word
+ *               (kvx_workspace_status).
  *   kept_idx    device int32 [B*Hkv][top + recent]; entries past the count
  *               are set to -1.
  *   kept_count  device int32 [B*Hkv].
  *   workspace   device, >= kvx_select_workspace_bytes(B, Hkv, Lmax), 256-byte
- *               aligned (holds the scores).
+ *               aligned (holds the scores and a per-head histogram, which the
+ *               call clears on `stream` first).
  * The cut is decided on fp32 scores: positions whose scores lie within fp32
  * rounding of the cut may be exchanged with respect to an exact selection.
  * ------------------------------------------------------------------------- */

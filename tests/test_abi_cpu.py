@@ -193,8 +193,8 @@ def test_group_size_trades_fragmentation_for_tables(kvx, orc):
 
 
 def test_select_and_pack_reject_bad_arguments(kvx):
-    ws = kvx.kvx_select_workspace_bytes(2, 2, 100)
-    assert ws == kvx.KVX_WS_HEADER_BYTES + 4 * 2 * 2 * 100
+    ws = kvx.kvx_select_workspace_bytes(2, 2, 101)
+    assert ws == kvx.KVX_WS_HEADER_BYTES + 4 * 2048 * 2 * 2 + 4 * 2 * 2 * 104
     rc = kvx.lib.kvx_select_topk(256, 256, 256, 2, 8, 2, 96, 100, 10, 4, 256, 256, 256, ws, None)
     assert rc == kvx.KVX_EUNSUPPORTED
     rc = kvx.lib.kvx_select_topk(256, 256, 256, 2, 7, 2, 128, 100, 10, 4, 256, 256, 256, ws, None)

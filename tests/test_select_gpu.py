@@ -169,3 +169,51 @@ def test_select_pack_attend_end_to_end(layout):
                 ref = orc.attn_head(qh, kh, vh, ref_idx, 1.0 / math.sqrt(D))
                 assert np.abs(got[b, h * g:(h + 1) * g] - ref).max() <= 2e-3
     assert agree >= 14
+
+
+def test_selection_bucket_overflow_and_ragged():
+    """All-equal keys put every candidate in the cut's bucket (more than the
+    kernel keeps in shared memory, so its global fallback runs); ragged
+    lengths end inside a float4, a bitmask word and a streamed chunk."""
+    orc = oracle.load()
+    q, k, v, L = make(5, 1, 8, 2, 128, [20001], const_keys=True)
+    kept, cnt = gpu_select(q, k, L, 300, 7)
+    exp = np.concatenate([np.arange(300), np.arange(20001 - 7, 20001)])
+    for bh in range(2):
+        assert np.array_equal(kept[bh, :cnt[bh]], exp)
+    q, k, v, L = make(6, 3, 8, 2, 64, [8197 + 3, 4101, 33])
+    for top, recent in ((1000, 3), (4095, 1), (31, 2)):
+        kept, cnt = gpu_select(q, k, L, top, recent)
+        for bh in range(6):
+            b, h = bh // 2, bh % 2
+            ref = orc.select_topk(q[b, 4 * h:4 * h + 4], k[b, h, :L[b]], top, recent)
+            assert cnt[bh] == ref.size
+            assert np.all(kept[bh, cnt[bh]:] == -1)
+            check_head(orc, q[b, 4 * h:4 * h + 4], k[b, h, :L[b]], top, recent,
+                       kept[bh, :cnt[bh]])
+
+
+def test_selection_bad_length_flagged():
+    """A length above Lmax selects nothing for its sequence and sets the
+    status bit; the other sequences are unaffected."""
+    q, k, v, L = make(7, 2, 8, 2, 128, [300, 200])
+    B, Hq, D = q.shape
+    Lmax = k.shape[2]
+    top, recent = 40, 8
+    bad = np.array([Lmax + 1, 200], np.int32)
+    kept = torch.full((4, top + recent), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((4,), -7, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(kvx.kvx_select_workspace_bytes(B, 2, Lmax) // 4 + 64, dtype=torch.int32,
+                     device="cuda")
+    kvx.kvx_select_topk(_bf16(k), _bf16(q), torch.from_numpy(bad).cuda(), B, Hq, 2, D, Lmax,
+                        top, recent, kept, cnt, ws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == kvx.KVX_DEV_BAD_LENGTH
+    c = cnt.cpu().numpy()
+    kh = kept.cpu().numpy()
+    assert c[0] == 0 and c[1] == 0 and np.all(kh[:2] == -1)
+    orc = oracle.load()
+    for h in range(2):
+        ref = orc.select_topk(q[1, 4 * h:4 * h + 4], k[1, h, :200], top, recent)
+        assert c[2 + h] == ref.size
+        check_head(orc, q[1, 4 * h:4 * h + 4], k[1, h, :200], top, recent, kh[2 + h, :c[2 + h]])
