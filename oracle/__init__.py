@@ -73,6 +73,13 @@ class Oracle:
         lib.oracle_select_topk.argtypes = [_c.c_int, _c.c_int, _c.c_int, _F64, _F64, _c.c_int,
                                            _c.c_int, _I32, _c.c_void_p]
         lib.oracle_num_threads.restype = _c.c_int
+        lib.oracle_frame_new.argtypes = [_c.c_int, _c.c_int, _c.c_int32]
+        lib.oracle_frame_new.restype = _c.c_void_p
+        lib.oracle_frame_free.argtypes = [_c.c_void_p]
+        lib.oracle_frame_reserve.argtypes = [_c.c_void_p, _c.c_int, _c.c_int, _c.c_void_p]
+        lib.oracle_frame_alias.argtypes = [_c.c_void_p] + [_c.c_int] * 5
+        lib.oracle_frame_trim.argtypes = [_c.c_void_p, _c.c_int, _c.c_int, _c.c_int]
+        lib.oracle_frame_state.argtypes = [_c.c_void_p, _I32, _I32, _c.c_void_p]
         self.lib = lib
 
     # -- attention -------------------------------------------------------
@@ -200,6 +207,46 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
+
+    # -- KV-RM block pager -------------------------------------------------
+    def frame(self, S, max_blocks, num_phys):
+        return OracleFrame(self, S, max_blocks, num_phys)
+
+
+class OracleFrame:
+    """The oracle's block pager: one logical view per sequence over
+    refcounted physical blocks, edited by Reserve / Alias / Trim. Each edit
+    returns the oracle's code (0, -1 bad argument, -2 range, -3 no space)."""
+
+    def __init__(self, orc: Oracle, S: int, max_blocks: int, num_phys: int):
+        self.lib, self.S, self.M, self.N = orc.lib, S, max_blocks, num_phys
+        self.h = self.lib.oracle_frame_new(S, max_blocks, num_phys)
+        if not self.h:
+            raise ValueError("oracle_frame_new: invalid arguments")
+
+    def __del__(self):
+        if getattr(self, "h", None):
+            self.lib.oracle_frame_free(self.h)
+            self.h = None
+
+    def reserve(self, s, c):
+        out = np.zeros(max(int(c), 1), dtype=np.int32)
+        rc = self.lib.oracle_frame_reserve(self.h, int(s), int(c), out.ctypes.data)
+        return rc, out[:max(int(c), 0)] if rc == 0 else out[:0]
+
+    def alias(self, dst, dj, src, sj, c):
+        return self.lib.oracle_frame_alias(self.h, int(dst), int(dj), int(src), int(sj), int(c))
+
+    def trim(self, s, begin, end):
+        return self.lib.oracle_frame_trim(self.h, int(s), int(begin), int(end))
+
+    def state(self):
+        """(table [S][max_blocks] with -1 past the view, nb [S], refcount [N])."""
+        table = np.zeros((self.S, self.M), dtype=np.int32)
+        nb = np.zeros(self.S, dtype=np.int32)
+        rc = np.zeros(self.N, dtype=np.int32)
+        self.lib.oracle_frame_state(self.h, table.reshape(-1), nb, rc.ctypes.data)
+        return table, nb, rc
 
 
 _default: Oracle | None = None

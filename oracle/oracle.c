@@ -401,3 +401,150 @@ int oracle_select_topk(int L, int D, int g, const double *q, const double *k,
   free(Q);
   return cnt;
 }
+
+/* KV-RM, Fig. 2 (block pager) and Fig. 3 (Alias, Trim, Reserve sealed by
+ * one Frame commit). Plain arrays; every edit validates first and then
+ * applies, so a failed edit changes nothing. */
+struct oracle_frame {
+  int S, M;
+  int32_t N;
+  int32_t *table; /* [S][M], -1 past nb */
+  int32_t *nb;    /* [S] */
+  int32_t *rc;    /* [N] references from table entries */
+};
+
+oracle_frame *oracle_frame_new(int S, int max_blocks, int32_t num_phys) {
+  if (S <= 0 || max_blocks <= 0 || num_phys <= 0) return NULL;
+  oracle_frame *f = (oracle_frame *)calloc(1, sizeof(oracle_frame));
+  if (!f) return NULL;
+  f->S = S;
+  f->M = max_blocks;
+  f->N = num_phys;
+  f->table = (int32_t *)malloc(sizeof(int32_t) * (size_t)S * (size_t)max_blocks);
+  f->nb = (int32_t *)calloc((size_t)S, sizeof(int32_t));
+  f->rc = (int32_t *)calloc((size_t)num_phys, sizeof(int32_t));
+  if (!f->table || !f->nb || !f->rc) {
+    oracle_frame_free(f);
+    return NULL;
+  }
+  for (size_t i = 0; i < (size_t)S * (size_t)max_blocks; ++i) f->table[i] = -1;
+  return f;
+}
+
+void oracle_frame_free(oracle_frame *f) {
+  if (!f) return;
+  free(f->table);
+  free(f->nb);
+  free(f->rc);
+  free(f);
+}
+
+static void oracle_frame_release(oracle_frame *f, int32_t p) {
+#if ORACLE_MUTANT != 20
+  f->rc[p] -= 1;
+#else
+  (void)f;
+  (void)p;
+#endif
+}
+
+int oracle_frame_reserve(oracle_frame *f, int s, int c, int32_t *out) {
+  if (!f || s < 0 || s >= f->S || c < 0) return -1;
+  if (f->nb[s] + c > f->M) return -2;
+  int32_t nfree = 0;
+  for (int32_t p = 0; p < f->N; ++p) nfree += f->rc[p] == 0;
+  if (c > nfree) return -3;
+  if (c == 0) return 0;
+  int32_t *pick = (int32_t *)malloc(sizeof(int32_t) * (size_t)c);
+  if (!pick) return -1;
+  /* lowest-addressed run of c consecutive free blocks */
+  int32_t start = -1, run = 0;
+  for (int32_t p = 0; p < f->N; ++p) {
+    run = f->rc[p] == 0 ? run + 1 : 0;
+    if (run == c) {
+#if ORACLE_MUTANT == 19
+      start = p - c; /* off by one */
+      if (start < 0) start = 0;
+#else
+      start = p - c + 1;
+#endif
+      break;
+    }
+  }
+  if (start >= 0) {
+    for (int i = 0; i < c; ++i) pick[i] = start + i;
+  } else {
+    /* no such run: the c lowest-numbered free blocks */
+    int i = 0;
+#if ORACLE_MUTANT == 23
+    for (int32_t p = f->N - 1; p >= 0 && i < c; --p)
+#else
+    for (int32_t p = 0; p < f->N && i < c; ++p)
+#endif
+      if (f->rc[p] == 0) pick[i++] = p;
+  }
+  for (int i = 0; i < c; ++i) {
+    f->table[(size_t)s * f->M + f->nb[s] + i] = pick[i];
+    f->rc[pick[i]] += 1;
+    if (out) out[i] = pick[i];
+  }
+  f->nb[s] += c;
+  free(pick);
+  return 0;
+}
+
+int oracle_frame_alias(oracle_frame *f, int dst, int dj, int src, int sj, int c) {
+  if (!f || dst < 0 || dst >= f->S || src < 0 || src >= f->S || c < 0) return -1;
+  if (sj < 0 || sj + c > f->nb[src]) return -2;
+  if (dj < 0 || dj > f->nb[dst] || dj + c > f->M) return -2;
+  if (c == 0) return 0;
+  int32_t *val = (int32_t *)malloc(sizeof(int32_t) * (size_t)c);
+  if (!val) return -1;
+  int32_t *srow = f->table + (size_t)src * f->M;
+  int32_t *drow = f->table + (size_t)dst * f->M;
+#if ORACLE_MUTANT == 21
+  /* reads each source after the earlier writes */
+  for (int i = 0; i < c; ++i) {
+    int32_t v = srow[sj + i];
+    if (dj + i < f->nb[dst]) oracle_frame_release(f, drow[dj + i]);
+    drow[dj + i] = v;
+    f->rc[v] += 1;
+  }
+#else
+  for (int i = 0; i < c; ++i) val[i] = srow[sj + i];
+  for (int i = 0; i < c; ++i) {
+    if (dj + i < f->nb[dst]) oracle_frame_release(f, drow[dj + i]);
+    drow[dj + i] = val[i];
+    f->rc[val[i]] += 1;
+  }
+#endif
+  if (dj + c > f->nb[dst]) f->nb[dst] = dj + c;
+  free(val);
+  return 0;
+}
+
+int oracle_frame_trim(oracle_frame *f, int s, int begin, int end) {
+  if (!f || s < 0 || s >= f->S) return -1;
+  if (begin < 0 || begin > end || end > f->nb[s]) return -2;
+  int32_t *row = f->table + (size_t)s * f->M;
+  const int n = f->nb[s];
+#if ORACLE_MUTANT != 24
+  for (int j = 0; j < begin; ++j) oracle_frame_release(f, row[j]);
+#endif
+#if ORACLE_MUTANT == 22
+  for (int j = end + 1; j < n; ++j) oracle_frame_release(f, row[j]);
+#else
+  for (int j = end; j < n; ++j) oracle_frame_release(f, row[j]);
+#endif
+  for (int j = 0; j < end - begin; ++j) row[j] = row[begin + j];
+  for (int j = end - begin; j < n; ++j) row[j] = -1;
+  f->nb[s] = end - begin;
+  return 0;
+}
+
+void oracle_frame_state(const oracle_frame *f, int32_t *table, int32_t *nb,
+                        int32_t *refcount) {
+  memcpy(table, f->table, sizeof(int32_t) * (size_t)f->S * (size_t)f->M);
+  memcpy(nb, f->nb, sizeof(int32_t) * (size_t)f->S);
+  if (refcount) memcpy(refcount, f->rc, sizeof(int32_t) * (size_t)f->N);
+}

@@ -123,6 +123,36 @@ int oracle_select_topk(int L, int D, int g, const double *q, const double *k,
 /* Number of OpenMP threads the oracle uses (1 without OpenMP). */
 int oracle_num_threads(void);
 
+/* ---- KV-RM block pager and Frame commit (KV-RM, Fig. 2 and Fig. 3) ----
+ * The logical KV view of sequence s is a list of physical block ids
+ * table[s][0 .. nb[s]); a physical block may be referenced from several
+ * places (after Alias) and is free when nothing references it. Runtime
+ * variability is expressed as three mapping edits; a Frame commit publishes
+ * the edited view as the one descriptor of the next decode step, so the
+ * committed state is exactly the state after all edits so far.
+ *
+ * Placement (not fixed by the pages; stated here): Reserve(s, c) takes the
+ * lowest-addressed run of c consecutive free blocks if one exists, else the
+ * c lowest-numbered free blocks, ascending.
+ *
+ * Edits return 0, -1 (bad sequence or negative count), -2 (index range), or
+ * -3 (not enough free blocks); a failed edit changes nothing. */
+typedef struct oracle_frame oracle_frame;
+oracle_frame *oracle_frame_new(int S, int max_blocks, int32_t num_phys);
+void oracle_frame_free(oracle_frame *f);
+/* Appends c new blocks to sequence s; their ids go to out[0..c) if out. */
+int oracle_frame_reserve(oracle_frame *f, int s, int c, int32_t *out);
+/* Logical blocks [dj, dj+c) of dst refer to the physical blocks that
+ * logical blocks [sj, sj+c) of src refer to (read before any write);
+ * dj <= nb[dst]; the view of dst grows to max(nb[dst], dj+c). */
+int oracle_frame_alias(oracle_frame *f, int dst, int dj, int src, int sj, int c);
+/* Sequence s keeps logical blocks [begin, end) of its view, renumbered from
+ * 0; the others are released (Trim(s, 0, 0) ends the sequence). */
+int oracle_frame_trim(oracle_frame *f, int s, int begin, int end);
+/* The committed descriptor: table [S][max_blocks] (-1 past nb[s]), nb [S];
+ * refcount [num_phys] (may be NULL). */
+void oracle_frame_state(const oracle_frame *f, int32_t *table, int32_t *nb,
+                        int32_t *refcount);
 #ifdef __cplusplus
 }
 #endif

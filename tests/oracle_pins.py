@@ -374,6 +374,137 @@ def pin_select_permutation_equivariance(orc):
     assert np.array_equal(np.sort(perm[b]), a)
 
 
+# ------------------------------------------------ KV-RM block pager
+def read_frame_golden():
+    """(S, max_blocks, num_phys, steps, refcount) of tests/golden/frame_edits.txt;
+    a step is (op, args, code, views, free)."""
+    cfg, steps, rc = None, [], None
+    with open(os.path.join(GOLDEN, "frame_edits.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("config"):
+                cfg = [int(x) for x in line.split()[1:]]
+            elif line.startswith("refcount"):
+                rc = [int(x) for x in line.split()[1:]]
+            elif line.startswith("step"):
+                cols = [c.strip() for c in line[len("step"):].split("|")]
+                op, *args = cols[0].split()
+                ints = lambda c: [] if c == "-" else [int(x) for x in c.split()]
+                steps.append((op, [int(x) for x in args], int(cols[1]),
+                              [ints(c) for c in cols[2:-1]], ints(cols[-1])))
+    return cfg[0], cfg[1], cfg[2], steps, rc
+
+
+def pager_views(pager):
+    table, nb, rc = pager.state()
+    return [list(table[s, :nb[s]]) for s in range(table.shape[0])], table, nb, rc
+
+
+def replay_frame_golden(pager, S, M, N, steps, rc_final):
+    """Replays the hand-worked edit sequence on any pager with reserve / alias /
+    trim / state and checks every intermediate state."""
+    for i, (op, args, code, views, free) in enumerate(steps):
+        before = pager_views(pager)[0]
+        if op == "reserve":
+            got, ids = pager.reserve(*args)
+        else:
+            got = getattr(pager, op)(*args)
+        assert got == code, (i, op, args, got, code)
+        now, table, nb, rc = pager_views(pager)
+        assert now == views, (i, op, args, now, views)
+        assert list(np.flatnonzero(rc == 0)) == free, (i, op, np.flatnonzero(rc == 0), free)
+        assert np.all(table[np.arange(M)[None, :] >= nb[:, None]] == -1)
+        if op == "reserve" and code == 0:
+            s = args[0]
+            assert list(ids) == now[s][len(before[s]):], (i, ids)
+    assert list(pager_views(pager)[3]) == rc_final
+
+
+def pin_frame_golden(orc):
+    S, M, N, steps, rc = read_frame_golden()
+    replay_frame_golden(orc.frame(S, M, N), S, M, N, steps, rc)
+
+
+def pin_frame_closed_form(orc):
+    """On a fresh pool, consecutive reserves lay the sequences end to end;
+    ending every sequence frees the whole pool, after which one reserve of
+    the whole pool takes blocks 0..N-1 in order."""
+    S, M, N = 5, 12, 40
+    f = orc.frame(S, M, N)
+    sizes = [3, 7, 1, 12, 5]
+    off = 0
+    for s, c in enumerate(sizes):
+        code, ids = f.reserve(s, c)
+        assert code == 0 and list(ids) == list(range(off, off + c)), (s, ids)
+        off += c
+    views, table, nb, rc = pager_views(f)
+    assert list(nb) == sizes and rc.sum() == sum(sizes)
+    assert np.all(rc[:off] == 1) and np.all(rc[off:] == 0)
+    for s in range(S):
+        assert f.trim(s, 0, 0) == 0
+    assert not pager_views(f)[3].any()
+    g = orc.frame(1, N, N)
+    code, ids = g.reserve(0, N)
+    assert code == 0 and list(ids) == list(range(N))
+    assert g.reserve(0, 1)[0] == -2  # view full
+    h = orc.frame(2, 4, 3)
+    assert h.reserve(0, 4)[0] == -3 and h.reserve(0, 3)[0] == 0
+
+
+def pin_frame_invariants(orc):
+    """Random edit streams: every block's reference count equals the number of
+    view entries naming it, free blocks are exactly the unreferenced ones, a
+    failed edit changes nothing, Trim keeps exactly the asked slice, Alias
+    copies the source entries as they were, and Reserve hands out free blocks
+    only, distinct, appended in order."""
+    gen = synth.rng(77)
+    S, M, N = 6, 12, 40
+    f = orc.frame(S, M, N)
+    for it in range(600):
+        views, table, nb, rc = pager_views(f)
+        op = gen.integers(0, 3)
+        if op == 0:
+            s, c = int(gen.integers(0, S)), int(gen.integers(0, 5))
+            code, ids = f.reserve(s, c)
+            ok = nb[s] + c <= M and c <= int((rc == 0).sum())
+            assert (code == 0) == ok, (it, code)
+            if ok:
+                assert len(set(ids.tolist())) == c and np.all(rc[ids] == 0)
+        elif op == 1:
+            dst, src = int(gen.integers(0, S)), int(gen.integers(0, S))
+            c = int(gen.integers(0, 4))
+            sj, dj = int(gen.integers(0, nb[src] + 2)), int(gen.integers(0, nb[dst] + 2))
+            code = f.alias(dst, dj, src, sj, c)
+            ok = sj + c <= nb[src] and dj <= nb[dst] and dj + c <= M
+            assert (code == 0) == ok, (it, code)
+            if ok:
+                now = pager_views(f)[0]
+                assert now[dst][dj:dj + c] == views[src][sj:sj + c]
+                assert now[dst][:dj] == views[dst][:dj]
+                assert now[dst][dj + c:] == views[dst][dj + c:]
+        else:
+            s = int(gen.integers(0, S))
+            b = int(gen.integers(0, nb[s] + 2))
+            e = int(gen.integers(0, nb[s] + 2))
+            code = f.trim(s, b, e)
+            ok = b <= e <= nb[s]
+            assert (code == 0) == ok, (it, code)
+            if ok:
+                assert pager_views(f)[0][s] == views[s][b:e]
+        now, table2, nb2, rc2 = pager_views(f)
+        if code != 0:
+            assert now == views and np.array_equal(rc2, rc)
+        count = np.bincount(np.concatenate([np.asarray(v, np.int64) for v in now] + [[]]).astype(
+            np.int64), minlength=N)
+        assert np.array_equal(count, rc2), it
+        edited = s if op != 1 else dst
+        for r in range(S):
+            if r != edited:
+                assert now[r] == views[r], (it, r)
+
+
 ALL_PINS = [
     pin_golden_two_token, pin_golden_kept_subset, pin_full_budget_equals_sdpa,
     pin_subset_equals_sdpa_on_kept_rows, pin_single_token, pin_equal_keys_give_mean,
@@ -382,4 +513,5 @@ ALL_PINS = [
     pin_budget_resolution, pin_group_pages, pin_footprint, pin_plan_coverage,
     pin_gather_golden, pin_runs_golden, pin_runs_closed_form, pin_gather_stamped_blocks,
     pin_select_closed_form, pin_select_ties_and_edges, pin_select_permutation_equivariance,
+    pin_frame_golden, pin_frame_closed_form, pin_frame_invariants,
 ]

@@ -26,6 +26,12 @@ MUTANTS = {
     16: "selection ties broken toward the higher position",
     17: "selection scores with the first query head only",
     18: "recent window one token short",
+    19: "reserve run starts one block early",
+    20: "released blocks keep their reference",
+    21: "alias reads sources after its own writes",
+    22: "trim keeps one block past the end",
+    23: "reserve fallback takes the highest free blocks",
+    24: "trim keeps references to the dropped front blocks",
 }
 
 
