@@ -43,6 +43,7 @@ def parse():
     ap.add_argument("--workload", default="qwen3_4b",
                     choices=["qwen3_4b", "qwen3_4b_32k", "qwen25_32b", "llama3_sparse"])
     ap.add_argument("--no-gather", action="store_true")
+    ap.add_argument("--no-frame", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-group-sweep", action="store_true")
     ap.add_argument("--no-sparse", action="store_true")
@@ -696,6 +697,118 @@ def kvrm_attention(cfg, pools, stagings, bt, dev, stream, peak, steps, kvx, torc
     return res
 
 
+def frame_churn(cfg, pools, stagings, dev, stream, peak, kvx, torch, steps, lookahead,
+                warm=1500, p_eos=1.0 / 400, p_share=0.25):
+    """KV-RM decode loop with runtime variability (KV-RM, Fig. 3): every step
+    each live sequence gains a token; a sequence that needs a new block
+    Reserves `lookahead` blocks; with probability p_eos a sequence ends (Trim
+    to nothing) and a new one takes its slot, sharing a prefix of a random
+    live sequence with probability p_share (Alias) before reserving the
+    rest; a sequence at the row limit drops its oldest block (Trim). One
+    Frame commit per step seals the edits; the coalesced gather then moves
+    the committed descriptor's blocks into the staging rows. Times the host
+    edits, the commit (host and device) and the gather."""
+    import time
+    S, M, N = cfg.S, cfg.max_blocks, cfg.num_phys
+    bt_tok = 16  # tokens per block of the gather workload
+    g = synth.rng(4242 + lookahead)
+    f = kvx.Frame(S, M, N)
+    tokens = cfg.seq_tokens.astype(np.int64).copy()
+    nbv = np.zeros(S, np.int64)
+
+    def need(t):
+        return np.minimum(M, -(-t // bt_tok))
+
+    def grow(s):
+        want = int(need(tokens[s]))
+        if want > nbv[s]:
+            c = int(min(M - nbv[s], max(want - nbv[s], lookahead)))
+            assert f.reserve(s, c)[0] == kvx.KVX_OK
+            nbv[s] += c
+
+    for s in range(S):
+        grow(s)
+
+    def edits():
+        eos = np.flatnonzero(g.random(S) < p_eos)
+        tokens[:] += 1
+        for s in eos:
+            assert f.trim(int(s), 0, 0) == kvx.KVX_OK
+            nbv[s] = 0
+            tokens[s] = int(g.integers(512, M * bt_tok - 512))
+            if g.random() < p_share:
+                r = int(g.integers(0, S))
+                k = int(min(nbv[r], need(tokens[s]) // 2))
+                if r != s and k > 0:
+                    assert f.alias(int(s), 0, r, 0, k) == kvx.KVX_OK
+                    nbv[s] = k
+        full = np.flatnonzero(tokens > M * bt_tok)
+        for s in full:
+            assert f.trim(int(s), 1, int(nbv[s])) == kvx.KVX_OK
+            nbv[s] -= 1
+            tokens[s] -= bt_tok
+        for s in np.flatnonzero(need(tokens) > nbv):
+            grow(int(s))
+
+    for _ in range(warm):
+        edits()
+        f.commit(stream)
+    ws = torch.zeros(kvx.kvx_gather_workspace_bytes(S, M) // 4 + 64, dtype=torch.int32,
+                     device=dev)
+
+    def gather():
+        bt, nb = f.active()
+        kvx.kvx_gather_coalesce(bt, nb, S, M, pools, N, cfg.block_bytes, stagings,
+                                cfg.row_bytes, 0, ws, stream=stream)
+
+    for _ in range(3):
+        edits()
+        f.commit(stream)
+        gather()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t_edit = t_commit = 0.0
+    records = launches = blocks = 0
+    l0, wait0 = f.stats()["launches"], f.stats()["wait_ns"]
+    w0 = time.perf_counter()
+    for i in range(steps):
+        t0 = time.perf_counter()
+        edits()
+        t1 = time.perf_counter()
+        ev[i][0].record(stream)
+        f.commit(stream)
+        t2 = time.perf_counter()
+        ev[i][1].record(stream)
+        gather()
+        ev[i][2].record(stream)
+        t_edit += t1 - t0
+        t_commit += t2 - t1
+        records += f.stats()["last_records"]
+        blocks += int(nbv.sum())
+    torch.cuda.synchronize()
+    wall_us = (time.perf_counter() - w0) / steps * 1e6
+    launches = f.stats()["launches"] - l0
+    wait_us = (f.stats()["wait_ns"] - wait0) / 1e3 / steps
+    assert kvx.kvx_workspace_status(ws) == 0
+    commit_us = sum(e[0].elapsed_time(e[1]) for e in ev) / steps * 1e3
+    gather_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    table, nb, _ = f.state()
+    runs = sum(int(1 + np.count_nonzero(np.diff(table[s, :nb[s]]) != 1)) if nb[s] else 0
+               for s in range(S))
+    moved = 2 * 2 * blocks / steps * cfg.block_bytes  # K and V, read + write
+    return {"steps": steps, "lookahead_blocks": lookahead,
+            "edit_host_us": t_edit / steps * 1e6,
+            "commit_host_us": t_commit / steps * 1e6 - wait_us,
+            "commit_wait_us": wait_us,
+            "commit_device_us": commit_us, "records_per_step": records / steps,
+            "h2d_bytes_per_step": 8 * records / steps, "apply_launches_per_step": launches / steps,
+            "gather_ms": gather_ms, "gather_gbs": moved / gather_ms / 1e6,
+            "gather_frac": moved / gather_ms / 1e6 / peak,
+            "blocks_per_seq": blocks / steps / S, "runs_per_seq": runs / S,
+            "step_wall_us": wall_us,
+            "submit_share": (t_edit / steps * 1e6 + t_commit / steps * 1e6 - wait_us) / wall_us}
+
+
 def bench_gather(args, dev, stream, peak, dist, world, rank):
     import torch
     from paged_non_uniform_gb300 import kvx
@@ -734,6 +847,19 @@ def bench_gather(args, dev, stream, peak, dist, world, rank):
     ms = max_over_ranks(a.elapsed_time(b) / steps, dist, dev)
     assert kvx.kvx_workspace_status(ws) == 0
     attn = kvrm_attention(cfg, pools, stagings, bt, dev, stream, peak, steps, kvx, torch)
+    frame = None
+    if not args.no_frame and rank == 0:
+        churn_steps = max(20, min(200, args.steps))
+        frame = {"workload": f"{cfg.S} sequences over the same pools: +1 token per step each, "
+                             "EOS p=1/400 per sequence and step (Trim), new prompts of 512.."
+                             "15872 tokens, 25% sharing half a live prefix (Alias), Reserve "
+                             "on demand, oldest block dropped at 16384 tokens (Trim); one "
+                             "Frame commit then one coalesced gather per step; 1500 steps of "
+                             "churn before timing",
+                 "lookahead_1": frame_churn(cfg, pools, stagings, dev, stream, peak, kvx,
+                                            torch, churn_steps, 1),
+                 "lookahead_8": frame_churn(cfg, pools, stagings, dev, stream, peak, kvx,
+                                            torch, churn_steps, 8)}
     live = sum_over_ranks(2 * cfg.live_bytes(), dist, dev)  # K and V, all ranks
     moved = 2 * live                                        # read + write
     return {"workload": f"KV-RM movement: {cfg.S} seqs, {int(cfg.seq_tokens.min())}.."
@@ -743,7 +869,7 @@ def bench_gather(args, dev, stream, peak, dist, world, rank):
             "value": job_rate(moved, ms), "unit": "GB/s (read+write)",
             "payload_gbs": job_rate(live, ms), "ms_per_call": ms,
             "frac": job_rate(moved, ms) / world / peak, "launches_per_call": 4,
-            "attention": attn}
+            "attention": attn, "frame_commit": frame}
 
 
 def main():

@@ -52,6 +52,7 @@ extern "C" {
 #define KVX_EUNSUPPORTED (-5) /* head_dim / page size / dtype / GQA combination */
 #define KVX_ESTATE (-6)       /* plan used before kvx_plan_upload */
 #define KVX_ESCRATCH (-7)     /* kvx_gather_coalesce_noalloc: problem too large for its static scratch */
+#define KVX_ENOBLOCKS (-8)    /* kvx_frame_reserve: fewer free physical blocks than asked */
 
 /* ---- device status bits (workspace status word) ---------------------- */
 #define KVX_DEV_BAD_PAGE 1u    /* a page-table entry outside [0, pool_pages) */
@@ -307,6 +308,86 @@ int kvx_gather_coalesce(const int32_t *block_table, const int32_t *num_blocks,
  * {first physical block, first logical block, length in blocks}. */
 int kvx_gather_read_runs(const void *workspace, int32_t S, int32_t max_blocks,
                          int32_t *run_count, int32_t *runs);
+
+/* ---------------------------------------------------------------------------
+ * KV-RM block pager and Frame commit ("KV-RM", Fig. 2: block pager; Fig. 3:
+ * runtime variability expressed as mapping edits Alias, Trim and Reserve,
+ * sealed by a single Frame commit that swaps a shadow descriptor in as the
+ * active one).
+ *
+ * A frame object holds, for S sequences, the logical view of each sequence:
+ * a list of at most max_blocks physical block ids out of a pool of
+ * num_phys_blocks. A block may appear in several views (after Alias); it is
+ * free when no view names it. Edits change the host view only; a commit
+ * publishes it as the device descriptor that kvx_gather_coalesce reads:
+ *     block_table int32 [S][max_blocks], entries past num_blocks[s] are -1;
+ *     num_blocks  int32 [S].
+ * Two device descriptors are kept (active and shadow). kvx_frame_commit
+ * enqueues on `stream` one host-to-device copy of the entries and lengths
+ * that changed since the shadow was last current (this frame and the one
+ * before) and one kernel that writes them into the shadow, then makes the
+ * shadow active. Work that reads a descriptor must be ordered before the
+ * commit after the one that made it active (it becomes the shadow that
+ * commit writes); on one stream this holds by construction.
+ *
+ * Placement: Reserve(s, c) takes the lowest-addressed run of c consecutive
+ * free blocks if there is one, else the c lowest-numbered free blocks in
+ * ascending order (runs keep descriptor merging effective).
+ *
+ * Errors: KVX_EINVAL (null frame, sequence outside [0, S), negative count),
+ * KVX_ERANGE (block index or length out of range), KVX_ENOBLOCKS (fewer free
+ * blocks than asked), KVX_ENOMEM (host), KVX_ECUDA. A failed edit changes
+ * nothing. Device memory is allocated on first use (commit or active). One
+ * frame is used by one host thread at a time.
+ * ------------------------------------------------------------------------- */
+typedef struct kvx_frame kvx_frame;
+
+typedef struct {
+  int64_t commits;         /* frames committed so far */
+  int64_t free_blocks;     /* physical blocks no view names */
+  int64_t pending_entries; /* table entries edited since the last commit */
+  int64_t pending_rows;    /* view lengths changed since the last commit */
+  int64_t last_records;    /* (index, value) records the last commit uploaded */
+  int64_t last_bytes;      /* bytes it copied host -> device */
+  int64_t launches;        /* apply-kernel launches so far */
+  int64_t wait_ns;         /* host time commits spent waiting for the record
+                              buffers of the commit before last (stream work
+                              queued ahead of it) */
+} kvx_frame_stats;
+
+/* S >= 1, max_blocks >= 1, num_phys_blocks >= 1; S * max_blocks + S must fit
+ * in int32 (KVX_ERANGE). All views start empty, all blocks free. */
+int kvx_frame_create(int32_t S, int32_t max_blocks, int32_t num_phys_blocks,
+                     kvx_frame **out);
+/* Frees host and device memory; call after the work reading its descriptors. */
+int kvx_frame_destroy(kvx_frame *frame);
+/* Reserve: appends count new blocks to the view of seq (nb[seq] + count <=
+ * max_blocks); writes their ids to ids[0..count) when ids is not NULL. */
+int kvx_frame_reserve(kvx_frame *frame, int32_t seq, int32_t count, int32_t *ids);
+/* Alias: view entries [dst_block, dst_block+count) of dst name the blocks
+ * that entries [src_block, src_block+count) of src name (all read before
+ * any is written, so overlapping ranges of one view are fine). dst_block <=
+ * nb[dst]; the view of dst grows to max(nb[dst], dst_block+count) <=
+ * max_blocks. Blocks no longer named become free. */
+int kvx_frame_alias(kvx_frame *frame, int32_t dst, int32_t dst_block, int32_t src,
+                    int32_t src_block, int32_t count);
+/* Trim: seq keeps view entries [begin_block, end_block), renumbered from 0
+ * (0 <= begin <= end <= nb[seq]); the others are released. Trim(s, 0, 0)
+ * ends a sequence; Trim(s, k, nb) drops its k oldest blocks. */
+int kvx_frame_trim(kvx_frame *frame, int32_t seq, int32_t begin_block, int32_t end_block);
+/* Frame commit (see above). Asynchronous on `stream`; the host record
+ * buffers of a commit are reused two commits later, after its copy ended. */
+int kvx_frame_commit(kvx_frame *frame, void *stream);
+/* Device pointers of the active descriptor (valid until the frame is
+ * destroyed; their contents change with the second commit after this one). */
+int kvx_frame_active(kvx_frame *frame, const int32_t **block_table,
+                     const int32_t **num_blocks);
+/* Host copy of the edited view (including edits not yet committed):
+ * block_table [S][max_blocks], num_blocks [S], refcount [num_phys_blocks];
+ * any may be NULL. */
+int kvx_frame_view(const kvx_frame *frame, int32_t *block_table, int32_t *num_blocks,
+                   int32_t *refcount);
+int kvx_frame_get_stats(const kvx_frame *frame, kvx_frame_stats *out);
 
 /* ---------------------------------------------------------------------------
  * kvx_select_topk -- kept-set selection for sparse long-context decode

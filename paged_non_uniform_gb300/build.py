@@ -16,7 +16,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libkvx.so")
-SOURCES = ["plan.cpp", "abi.cpp", "attn_mma.cu", "attn_simt.cu", "gather.cu", "select.cu"]
+SOURCES = ["plan.cpp", "abi.cpp", "attn_mma.cu", "attn_simt.cu", "gather.cu", "select.cu",
+           "frame.cu"]
 HEADERS = [os.path.join(CSRC, "kvx_internal.h"), os.path.join(CSRC, "ptx.cuh"),
            os.path.join(CSRC, "split_merge.cuh"),
            os.path.join(ROOT, "include", "kvx.h")]

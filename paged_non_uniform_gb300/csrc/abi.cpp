@@ -84,6 +84,7 @@ extern "C" const char *kvx_status_string(int s) {
     case KVX_ECUDA: return "CUDA runtime error";
     case KVX_EUNSUPPORTED: return "unsupported shape, page size, dtype or GQA factor";
     case KVX_ESTATE: return "plan not uploaded";
+    case KVX_ENOBLOCKS: return "fewer free physical blocks than asked";
     case KVX_ESCRATCH: return "problem needs more scratch than the static buffer of kvx_gather_coalesce_noalloc holds";
     default: return "unknown status";
   }

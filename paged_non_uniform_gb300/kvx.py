@@ -24,6 +24,7 @@ KVX_ECUDA = -4
 KVX_EUNSUPPORTED = -5
 KVX_ESTATE = -6
 KVX_ESCRATCH = -7
+KVX_ENOBLOCKS = -8
 
 KVX_DEV_BAD_PAGE = 1
 KVX_DEV_BAD_BUDGET = 2
@@ -109,6 +110,23 @@ lib.kvx_select_topk.argtypes = [_vp, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_int3
                                 _vp]
 lib.kvx_pack_kept.argtypes = [_vp, _vp, _vp, _c.c_int32, _vp, _c.c_int32, _vp, _vp, _vp, _vp,
                               _vp, _vp, _c.c_size_t, _vp]
+
+class kvx_frame_stats(_c.Structure):
+    _fields_ = [("commits", _c.c_int64), ("free_blocks", _c.c_int64),
+                ("pending_entries", _c.c_int64), ("pending_rows", _c.c_int64),
+                ("last_records", _c.c_int64), ("last_bytes", _c.c_int64),
+                ("launches", _c.c_int64), ("wait_ns", _c.c_int64)]
+
+
+lib.kvx_frame_create.argtypes = [_c.c_int32, _c.c_int32, _c.c_int32, _c.POINTER(_vp)]
+lib.kvx_frame_destroy.argtypes = [_vp]
+lib.kvx_frame_reserve.argtypes = [_vp, _c.c_int32, _c.c_int32, _vp]
+lib.kvx_frame_alias.argtypes = [_vp] + [_c.c_int32] * 5
+lib.kvx_frame_trim.argtypes = [_vp, _c.c_int32, _c.c_int32, _c.c_int32]
+lib.kvx_frame_commit.argtypes = [_vp, _vp]
+lib.kvx_frame_active.argtypes = [_vp, _c.POINTER(_vp), _c.POINTER(_vp)]
+lib.kvx_frame_view.argtypes = [_vp, _vp, _vp, _vp]
+lib.kvx_frame_get_stats.argtypes = [_vp, _c.POINTER(kvx_frame_stats)]
 lib.kvx_gather_coalesce_noalloc.argtypes = [_vp, _vp, _c.c_int32, _c.c_int32, _c.c_int32, _vp,
                                             _c.c_int64, _c.c_int64, _vp, _c.c_int64,
                                             _c.c_int32, _vp, _vp]
@@ -350,3 +368,55 @@ def kvx_gather_coalesce_noalloc(block_table, num_blocks, S, max_blocks, pools, n
                                          _ptr_array(stagings), int(staging_row_bytes), int(flags),
                                          _dptr(status), _stream(stream))
     _check(rc, "kvx_gather_coalesce_noalloc")
+
+
+class Frame:
+    """KV-RM block pager with double-buffered device descriptors
+    (kvx_frame_*). Edits return the library's status code; commit raises."""
+
+    def __init__(self, S: int, max_blocks: int, num_phys_blocks: int):
+        h = _vp()
+        _check(lib.kvx_frame_create(int(S), int(max_blocks), int(num_phys_blocks),
+                                    _c.byref(h)), "kvx_frame_create")
+        self.handle, self.S, self.M, self.N = h, int(S), int(max_blocks), int(num_phys_blocks)
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            lib.kvx_frame_destroy(self.handle)
+            self.handle = None
+
+    def reserve(self, seq: int, count: int):
+        ids = np.zeros(max(int(count), 1), dtype=np.int32)
+        rc = lib.kvx_frame_reserve(self.handle, int(seq), int(count), ids.ctypes.data)
+        return rc, (ids[:max(int(count), 0)] if rc == KVX_OK else ids[:0])
+
+    def alias(self, dst: int, dst_block: int, src: int, src_block: int, count: int) -> int:
+        return lib.kvx_frame_alias(self.handle, int(dst), int(dst_block), int(src),
+                                   int(src_block), int(count))
+
+    def trim(self, seq: int, begin_block: int, end_block: int) -> int:
+        return lib.kvx_frame_trim(self.handle, int(seq), int(begin_block), int(end_block))
+
+    def commit(self, stream=None) -> None:
+        _check(lib.kvx_frame_commit(self.handle, _stream(stream)), "kvx_frame_commit")
+
+    def active(self):
+        """Device addresses (block_table, num_blocks) of the active descriptor."""
+        bt, nb = _vp(), _vp()
+        _check(lib.kvx_frame_active(self.handle, _c.byref(bt), _c.byref(nb)),
+               "kvx_frame_active")
+        return int(bt.value), int(nb.value)
+
+    def state(self):
+        """Host view: (block_table [S][max_blocks], num_blocks [S], refcount [N])."""
+        bt = np.zeros((self.S, self.M), dtype=np.int32)
+        nb = np.zeros(self.S, dtype=np.int32)
+        rc = np.zeros(self.N, dtype=np.int32)
+        _check(lib.kvx_frame_view(self.handle, bt.ctypes.data, nb.ctypes.data, rc.ctypes.data),
+               "kvx_frame_view")
+        return bt, nb, rc
+
+    def stats(self) -> dict:
+        st = kvx_frame_stats()
+        _check(lib.kvx_frame_get_stats(self.handle, _c.byref(st)), "kvx_frame_get_stats")
+        return {k: int(getattr(st, k)) for k, _ in kvx_frame_stats._fields_}
