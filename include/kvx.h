@@ -129,6 +129,10 @@ typedef struct kvx_plan_stats {
   int64_t slots_allocated;   /* token slots in allocated group pages (all heads) */
   int64_t slots_used;        /* token slots holding kept tokens (= total_tokens) */
   double plan_us;            /* host time spent building the plan */
+  int32_t item_overhead;     /* tokens the balanced plan charges per item on top of
+                                its tokens (the per-item cost of query load,
+                                cross-warp merge and partial write) */
+  int32_t pad_;
 } kvx_plan_stats;
 
 /* Text for a status code. Never NULL. */

@@ -247,6 +247,37 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   __syncthreads();
   // Everything above touches only this block's shared memory and the kernel
   // parameters; global inputs may come from the previous kernel in the stream.
+  if (warp == kCons && p.pf_tokens > 0) {
+    // While that kernel finishes, warm L2 with the first pf_tokens tokens of
+    // this block's items. A prefetch changes no data, so a page-table entry
+    // that the previous kernel is still rewriting costs at most a wasted
+    // prefetch; the entries are read through L2 only (ld.global.cg), leaving
+    // no copy in L1 for the loads after the wait.
+    const int box_h = P < kStageTokens ? P : kStageTokens;
+    int left = p.pf_tokens;
+    for (int it = it0; it < it1 && left > 0; ++it) {
+      const Item item = p.items[it];
+      const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
+      const int gi = p.head_grp[h], row = p.head_row[h];
+      const GroupDesc &gd = p.grp[gi];
+      const int32_t *pt = gd.page_table + (size_t)b * gd.stride;
+      const int end = min(item.end, item.begin + left);
+      const int nbox = (end - item.begin + box_h - 1) / box_h;
+      for (int j = lane; j < nbox; j += 32) {
+        const int tb = item.begin + j * box_h;
+        const int32_t page = __ldcg(pt + tb / P);
+        if (page >= 0 && (int64_t)page < gd.num_pages) {
+          tma_prefetch_5d(&p.tmK[gi], 0, tb & (P - 1), 0, row, page);
+          tma_prefetch_5d(&p.tmV[gi], 0, tb & (P - 1), 0, row, page);
+        }
+      }
+      left -= end - item.begin;
+    }
+  }
+  // The plan was uploaded (synchronously) before any call: its first item can
+  // be read before the wait too.
+  Item item0{};
+  if (it0 < it1) item0 = p.items[it0];
   pdl_wait();
 
   if (warp == kCons) {
@@ -257,7 +288,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     int gs = 0;
     bool dead = false;
     for (int it = it0; it < it1 && !dead; ++it) {
-      const Item item = p.items[it];
+      const Item item = it == it0 ? item0 : p.items[it];
       const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
       const int gi = p.head_grp[h], row = p.head_row[h];
       const GroupDesc &gd = p.grp[gi];
@@ -344,7 +375,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     int gs = 0;
     bool dead = false;
     for (int it = it0; it < it1; ++it) {
-      const Item item = p.items[it];
+      const Item item = it == it0 ? item0 : p.items[it];
       const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
       if (warp == 0 && lane == 0) {
         const int L = __ldg(p.seq_len + b), bud = __ldg(p.head_budget + item.bh);

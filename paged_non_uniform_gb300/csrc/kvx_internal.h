@@ -41,6 +41,12 @@ struct GroupDesc {
   int32_t size;
 };
 
+// Bytes of K/V (whole grid) that the tensor-core kernel prefetches into L2
+// while the previous kernel of the stream finishes.
+#ifndef KVX_ATTN_PREFETCH_MB
+#define KVX_ATTN_PREFETCH_MB 48
+#endif
+
 // Kernel parameters of the attention kernels (passed by value as a
 // __grid_constant__ argument; the tensor maps keep their 128-byte alignment).
 struct alignas(128) AttnParams {
@@ -63,6 +69,7 @@ struct alignas(128) AttnParams {
   int32_t B, Hq, Hkv, D, g, P, num_groups, layout;
   float scale_log2;            // scale * log2(e)
   int32_t stall_block;         // failure-detection test: block whose first stage gets no loads (-1: none)
+  int32_t pf_tokens;           // tokens per block warmed into L2 before the dependency wait
   uint64_t wait_ns;            // limit of every pipeline wait
   int8_t head_grp[KVX_MAX_KV_HEADS];
   int8_t head_row[KVX_MAX_KV_HEADS];

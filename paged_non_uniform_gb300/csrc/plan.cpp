@@ -21,7 +21,10 @@ int set_cuda_error(cudaError_t e);  // abi.cpp
 // Cost, in tokens, charged per work item on top of its tokens: the query
 // load, the cross-warp merge and the partial write of an item take about as
 // long as streaming this many tokens.
-static int item_overhead_tokens() { return 64; }
+#ifndef KVX_ITEM_OVERHEAD_TOKENS
+#define KVX_ITEM_OVERHEAD_TOKENS 160
+#endif
+static int item_overhead_tokens() { return KVX_ITEM_OVERHEAD_TOKENS; }
 
 static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -343,6 +346,8 @@ extern "C" int kvx_plan_get_stats(const kvx_plan *p, kvx_plan_stats *st) {
     for (int b = 0; b < B; ++b)
       alloc += (int64_t)p->group_pages[(size_t)gi * B + b] * p->group_size[gi] * P;
   st->slots_allocated = alloc;
+  st->item_overhead = item_overhead_tokens();
+  st->pad_ = 0;
   st->slots_used = tot;
   st->plan_us = p->plan_us;
   return KVX_OK;

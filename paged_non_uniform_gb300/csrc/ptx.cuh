@@ -89,6 +89,15 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// L2 prefetch of one box of a 5-D tensor map (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_5d(const void *tmap, int c0, int c1, int c2,
+                                                int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.prefetch.tensor.5d.L2.global.tile [%0, {%1, %2, %3, %4, %5}];" ::"l"(tmap),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -74,7 +74,8 @@ class kvx_plan_stats(_c.Structure):
                 ("num_split_heads", _c.c_int32), ("kernel", _c.c_int32), ("policy", _c.c_int32),
                 ("total_tokens", _c.c_int64), ("max_cta_tokens", _c.c_int64),
                 ("mean_cta_tokens", _c.c_double), ("slots_allocated", _c.c_int64),
-                ("slots_used", _c.c_int64), ("plan_us", _c.c_double)]
+                ("slots_used", _c.c_int64), ("plan_us", _c.c_double),
+                ("item_overhead", _c.c_int32), ("pad_", _c.c_int32)]
 
 
 lib.kvx_status_string.restype = _c.c_char_p
