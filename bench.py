@@ -61,7 +61,8 @@ def peaks():
         return FALLBACK_HBM, "fallback"
 
 
-KERNEL_SOURCES = ["attn_mma.cu", "ptx.cuh", "split_merge.cuh", "kvx_internal.h"]
+KERNEL_SOURCES = ["attn_mma.cu", "ptx.cuh", "split_merge.cuh", "kvx_internal.h", "abi.cpp",
+                  "plan.cpp"]
 PROFILE = os.path.join(ROOT, "profiles", "attn_mma_qwen3_4b.md")
 
 
