@@ -172,14 +172,7 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   p.layout = s.layout;
   p.stall_block = plan->stall_block;
   p.wait_ns = plan->wait_ns;
-  // L2 warm-up before the dependency wait: KVX_ATTN_PREFETCH_MB of the grid's
-  // first K/V bytes in total, split evenly over the blocks
-  {
-    const int64_t per_token = 2ll * D * (s.dtype == KVX_BF16 ? 2 : 4);
-    const int64_t pf = ((int64_t)KVX_ATTN_PREFETCH_MB << 20) /
-                       ((int64_t)std::max(plan->num_ctas, 1) * per_token);
-    p.pf_tokens = (int32_t)std::min<int64_t>(pf, 1 << 30);
-  }
+  p.pf_tokens = plan->pf_tokens;
   const float sc = scale == 0.f ? 1.0f / std::sqrt((float)D) : scale;
   p.scale_log2 = (float)((double)sc * 1.4426950408889634);
 

@@ -247,9 +247,10 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   __syncthreads();
   // Everything above touches only this block's shared memory and the kernel
   // parameters; global inputs may come from the previous kernel in the stream.
-  if (warp == kCons && p.pf_tokens > 0) {
+  if (warp == kCons - 1 && p.pf_tokens > 0) {
     // While that kernel finishes, warm L2 with the first pf_tokens tokens of
-    // this block's items. A prefetch changes no data, so a page-table entry
+    // this block's items (done by the consumer warp whose first stage comes
+    // last, so that the producer's first loads are not held up). A prefetch changes no data, so a page-table entry
     // that the previous kernel is still rewriting costs at most a wasted
     // prefetch; the entries are read through L2 only (ld.global.cg), leaving
     // no copy in L1 for the loads after the wait.

@@ -41,10 +41,17 @@ struct GroupDesc {
   int32_t size;
 };
 
-// Bytes of K/V (whole grid) that the tensor-core kernel prefetches into L2
-// while the previous kernel of the stream finishes.
+// L2 warm-up by the tensor-core kernel while the previous kernel of the
+// stream finishes: up to KVX_ATTN_PREFETCH_MB of K/V over the whole grid,
+// and only for short launches (mean block load at most
+// KVX_ATTN_PREFETCH_MAX_BLOCK_TOKENS), where the start-up is a large share of
+// the launch; a long launch gains nothing and its first loads would queue
+// behind the prefetches.
 #ifndef KVX_ATTN_PREFETCH_MB
-#define KVX_ATTN_PREFETCH_MB 48
+#define KVX_ATTN_PREFETCH_MB 16
+#endif
+#ifndef KVX_ATTN_PREFETCH_MAX_BLOCK_TOKENS
+#define KVX_ATTN_PREFETCH_MAX_BLOCK_TOKENS 1024
 #endif
 
 // Kernel parameters of the attention kernels (passed by value as a
@@ -141,4 +148,5 @@ struct kvx_plan {
   int64_t *d_trace;
   int32_t stall_block;  // kvx_plan_inject_stall
   uint64_t wait_ns;
+  int32_t pf_tokens;    // tokens per block warmed into L2 before the dependency wait
 };

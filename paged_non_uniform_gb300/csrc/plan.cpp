@@ -227,6 +227,7 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
     p->d_trace = nullptr;
     p->stall_block = -1;
     p->wait_ns = 2000000000ull;
+    p->pf_tokens = 0;
     // Deterministic Budget Allocation: n = min(L, budget).
     p->n.resize((size_t)B * Hkv);
     for (int b = 0; b < B; ++b)
@@ -257,6 +258,15 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
     else
       plan_uniform(p, sms);
     finish_splits(p);
+    // L2 warm-up amount (short launches only)
+    int64_t total = 0;
+    for (int64_t v : p->cta_tokens) total += v;
+    const int64_t mean = total / std::max(p->num_ctas, 1);
+    const int64_t per_token = 2ll * s->D * (s->dtype == KVX_BF16 ? 2 : 4);
+    p->pf_tokens = 0;
+    if (mean <= KVX_ATTN_PREFETCH_MAX_BLOCK_TOKENS)
+      p->pf_tokens = (int32_t)std::min<int64_t>(
+          mean, ((int64_t)KVX_ATTN_PREFETCH_MB << 20) / (std::max(p->num_ctas, 1) * per_token));
   } catch (const std::bad_alloc &) {
     delete p;
     return KVX_ENOMEM;
