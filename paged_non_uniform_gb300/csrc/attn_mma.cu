@@ -6,9 +6,9 @@
 // Multi-turn LLM Serving", AOT Load Balancing, Fig. 13), the softmax
 // attention of the g query heads of KV head h over those tokens, either as
 // the final output (item covers the head) or as a log-sum-exp partial
-// (max, sum, un-normalised output) merged later by the combine kernel.
+// (max, sum, un-normalised output) merged in the same launch (below).
 //
-// Data path, per thread block (one per SM, persistent over its items):
+// Data path, per thread block (two per SM, persistent over their items):
 //  * one producer warp walks the items' pages through the head group's page
 //    table (Fig. 8(b)) and issues one bulk-tensor load per page slot of K and
 //    of V (a 5-D tensor map {64 elements, slot, half, head, page} covers both
@@ -16,7 +16,8 @@
 //    swizzled) into a ring of 32-token stages, completing on mbarriers;
 //  * kCons consumer warps take the stages round-robin (ring slot s always
 //    belongs to warp s % kCons, so each warp sees its slots' mbarrier phases
-//    in order). Per stage a warp
+//    in order). Each warp owns kStages / kCons slots, so one of its slots is
+//    loading while it computes on another. Per stage a warp
 //    computes S^T = K Q^T on m16n8k16 bf16 MMAs (16 tokens x 8 query columns;
 //    GQA query heads of one KV head are the columns), runs the online softmax
 //    on the accumulator fragments (column max by three shuffles), transposes
@@ -42,19 +43,24 @@ namespace {
 
 // Tuning knobs (compile-time).
 #ifndef KVX_ATTN_CONS
-#define KVX_ATTN_CONS 4          // consumer warps per block
+#define KVX_ATTN_CONS 3          // consumer warps per block
 #endif
 #ifndef KVX_ATTN_STAGES
-#define KVX_ATTN_STAGES 4        // ring depth, in 32-token stages
+#define KVX_ATTN_STAGES 6        // ring depth, in 32-token stages (2 slots per consumer)
 #endif
 #ifndef KVX_ATTN_CTAS_PER_SM
 #define KVX_ATTN_CTAS_PER_SM 2   // resident blocks per SM
+#endif
+#ifndef KVX_ATTN_MERGE_BUFS
+#define KVX_ATTN_MERGE_BUFS 1    // cross-warp merge records (2: alternate between items)
 #endif
 #ifndef KVX_TMA_LANES
 #define KVX_TMA_LANES 1          // issue a stage's boxes from separate lanes
 #endif
 constexpr int kCons = KVX_ATTN_CONS;
 constexpr int kStages = KVX_ATTN_STAGES;
+constexpr int kMergeBufs = KVX_ATTN_MERGE_BUFS;
+static_assert(kMergeBufs == 1 || kMergeBufs == 2, "one or two merge buffers");
 // Stage gs goes to consumer warp gs % kCons and ring slot gs % kStages. With
 // kStages a multiple of kCons every slot belongs to one warp, which waits on
 // that slot's phases strictly in order. Otherwise a warp could wait for phase
@@ -70,7 +76,7 @@ struct Cfg {
   static constexpr int kMS = D + 4;                   // merge row stride (floats)
   static constexpr int kMW = 8 * kMS + 16;            // floats per warp record
   static constexpr int kSmem =
-      1024 + kStages * kStage + 2 * kCons * kMW * 4 + 2 * kStages * 8 + 16;
+      1024 + kStages * kStage + kMergeBufs * kCons * kMW * 4 + 2 * kStages * 8 + 16;
 };
 
 // Shared-memory layout of a stage's K (or V) tile: the stage's 32 tokens
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   uint8_t *smem =
       (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   float *merge = (float *)(smem + kStages * C::kStage);
-  uint64_t *bars = (uint64_t *)(merge + 2 * kCons * C::kMW);
+  uint64_t *bars = (uint64_t *)(merge + kMergeBufs * kCons * C::kMW);
   volatile int *abort_flag = (volatile int *)(bars + 2 * kStages);
   volatile int *last_flag = abort_flag + 1;
   const uint32_t stage0 = smem_u32(smem);
@@ -428,7 +434,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
         l0 += __shfl_xor_sync(0xffffffffu, l0, sh);
         l1 += __shfl_xor_sync(0xffffffffu, l1, sh);
       }
-      float *buf = merge + ((it - it0) & 1) * kCons * C::kMW;
+      float *buf = merge + ((it - it0) % kMergeBufs) * kCons * C::kMW;
       float *mw = buf + warp * C::kMW;
 #pragma unroll
       for (int dm = 0; dm < NK; ++dm) {
@@ -464,6 +470,9 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
           if (d == 0) p.part_ml[(size_t)item.slot * g + qi] = make_float2(M, Ls);
         }
       }
+      // one merge buffer: the next item may overwrite it only after every
+      // consumer has read it (a split item's ticket syncs below do that)
+      if (kMergeBufs == 1 && item.slot < 0) consumer_sync(kCons * 32);
       if (item.slot >= 0) {
         // Publish this piece; the block that finishes the head's last piece
         // merges all of them and rearms the counter for the next call.
