@@ -416,8 +416,9 @@ int kvx_frame_get_stats(const kvx_frame *frame, kvx_frame_stats *out);
  *               are set to -1.
  *   kept_count  device int32 [B*Hkv].
  *   workspace   device, >= kvx_select_workspace_bytes(B, Hkv, Lmax), 256-byte
- *               aligned (holds the scores and a per-head histogram, which the
- *               call clears on `stream` first).
+ *               aligned (holds the scores, a per-head histogram and bucket
+ *               count, which the call clears on `stream` first, and per head a
+ *               list of up to 8192 candidates near the cut and a bitmask).
  * The cut is decided on fp32 scores: positions whose scores lie within fp32
  * rounding of the cut may be exchanged with respect to an exact selection.
  * ------------------------------------------------------------------------- */

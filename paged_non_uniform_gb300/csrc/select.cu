@@ -14,11 +14,13 @@
 // Kernels, in stream order:
 //   score   streams every candidate key row once (HBM-bound), fp32 dot with Q,
 //           and counts the first radix digit (top 11 key bits) per head;
-//   topk    one block per head: radix select (11/11/10 bits) of the cut on
-//           order-preserving keys -- first digit from the score kernel, the
-//           rest over the cut's bucket, gathered into shared memory while the
-//           scores stream through once -- then bitmasks of the kept
-//           positions and an ordered write, ascending;
+//   bucket  many blocks per head: each reads a span of scores once, sets the
+//           positions whose first radix digit is above the cut's in a
+//           bitmask and appends those in the cut's bucket to a list;
+//   topk    one block per head: the other two radix digits (11/11/10 bits
+//           on order-preserving keys) over the bucket list in shared
+//           memory, then bitmasks of the kept positions and an ordered
+//           write, ascending;
 //   pack    copies kept row i of each head into token i of its pages.
 #include <cuda_bf16.h>
 
@@ -44,6 +46,12 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The float whose order-preserving key is k (inverse of order_key for keys
+// of numbers).
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Length of sequence b, or 0 when it lies outside [0, Lmax] (the top-k
 // kernel then reports KVX_DEV_BAD_LENGTH).
 #define KVX_SELECT_LEN(p, b) \
@@ -58,8 +66,12 @@ struct SelectParams {
   int32_t *kept_idx;          // [B*Hkv][stride]
   int32_t *kept_count;        // [B*Hkv]
   uint32_t *status;
+  uint2 *blist;               // [B*Hkv][kBucketCap] (key, position) of the cut's first-digit bucket
+  int32_t *bcnt;              // [B*Hkv] bucket sizes (zeroed per call with hist0)
+  uint32_t *bgt;              // [B*Hkv][wstride] bitmask: first digit above the cut's
   int32_t B, Hq, Hkv, D, Lmax, top, recent, stride;
   int32_t ldsc;               // score row stride: Lmax rounded up to a multiple of 4
+  int32_t wstride;            // bitmask row stride in words
 };
 
 template <int D>
@@ -136,203 +148,226 @@ __global__ void __launch_bounds__(kScoreThreads) select_score_kernel(const Selec
     if (hist[i]) atomicAdd(gh + i, hist[i]);
 }
 
-// Plain bulk copy global -> shared (addresses 16-byte aligned, bytes a
-// multiple of 16), completing on `bar` with a transaction count of `bytes`.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, "
-      "[%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kBucketCap = 8192;           // keys of the cut's first-digit bucket
-constexpr int kStageFloats = 4 * kTopkThreads;  // scores per streamed chunk (one float4 a thread)
-constexpr int kStages = 4;
+constexpr int kBucketCap = 8192;       // (key, position) pairs kept per head
+constexpr int kBucketThreads = 512;
+constexpr int kBucketSpan = 16384;     // positions per bucket block (8 float4 per thread)
+constexpr int kBlockBucketCap = 4096;  // bucket entries one bucket block stages in shared memory
 constexpr int kMaxSelectLmax = 1 << 18;
-constexpr uint64_t kSelectWaitNs = 2000000000ull;
 
-// Dynamic shared memory of the top-k kernel: the score chunk ring, the bucket
-// list, then the above-cut and at-cut bitmasks of all candidate positions.
+size_t select_wstride(int Lmax) { return (((size_t)Lmax + 31) / 32 + 3) & ~size_t(3); }
+
+// Dynamic shared memory of the top-k kernel: the bucket list, then the
+// above-cut and at-cut bitmasks of all candidate positions.
 size_t topk_smem_bytes(int Lmax) {
-  const size_t words = ((size_t)Lmax + 31) / 32;
-  return (size_t)kStages * kStageFloats * sizeof(float) + (size_t)kBucketCap * sizeof(uint2) +
-         2 * words * sizeof(uint32_t);
+  return (size_t)kBucketCap * sizeof(uint2) + 2 * select_wstride(Lmax) * sizeof(uint32_t);
 }
 
 // Finds, from a histogram of nb bins, the bin (counted from the top) that
-// holds the k-th largest key and the rank of that key inside the bin. Run by
-// warp 0; lane l owns bins nb-1-l*per .. nb-per-l*per.
-__device__ __forceinline__ void find_digit(const int *hist, int nb, int k, uint32_t *s_digit,
-                                           int *s_k) {
-  const int lane = threadIdx.x & 31, per = nb / 32;
+// holds the k-th largest key and the rank of that key inside the bin. All NT
+// threads of the block call it:
+// thread t owns nb / NT consecutive bins from the top, a two-level scan gives
+// each thread the count above its bins, and the thread whose bins hold the
+// k-th key resolves it. wsum: NT / 32 ints of shared scratch.
+template <int NT>
+__device__ __forceinline__ void find_digit_block(const int *hist, int nb, int k,
+                                                 uint32_t *s_digit, int *s_k, int *wsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = nb / NT;
   int sum = 0;
-  for (int e = 0; e < per; ++e) sum += hist[nb - 1 - lane * per - e];
+  for (int e = 0; e < per; ++e) sum += hist[nb - 1 - tid * per - e];
   int incl = sum;
 #pragma unroll
   for (int sh = 1; sh < 32; sh <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, sh);
     if (lane >= sh) incl += y;
   }
-  const int before = incl - sum;
-  if (before < k && k <= incl) {
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < NT / 32 ? wsum[lane] : 0;
+    int x = v;
+#pragma unroll
+    for (int sh = 1; sh < 32; sh <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, sh);
+      if (lane >= sh) x += y;
+    }
+    if (lane < NT / 32) wsum[lane] = x - v;
+  }
+  __syncthreads();
+  const int before = wsum[warp] + incl - sum;
+  if (before < k && k <= before + sum) {
     int acc = before;
     for (int e = 0; e < per; ++e) {
-      const int c = hist[nb - 1 - lane * per - e];
+      const int c = hist[nb - 1 - tid * per - e];
       if (acc + c >= k) {
-        *s_digit = (uint32_t)(nb - 1 - lane * per - e);
+        *s_digit = (uint32_t)(nb - 1 - tid * per - e);
         *s_k = k - acc;
         break;
       }
       acc += c;
     }
   }
+  __syncthreads();
 }
 
-// Issues the bulk copy of score chunk c (positions [c*kStageFloats, ...) of
-// the n candidates, rounded up to whole float4s) into its ring slot.
-__device__ __forceinline__ void issue_chunk(const float *sc, int n, int c, float *ring,
-                                            uint64_t *bars) {
-  const int t0 = c * kStageFloats;
-  const int len = min(kStageFloats, n - t0);
-  const uint32_t bytes = (uint32_t)((len + 3) & ~3) * 4u;
-  const int slot = c % kStages;
-  const uint32_t bar = smem_u32(&bars[slot]);
-  mbar_arrive_expect_tx(bar, bytes);
-  bulk_load(smem_u32(ring + (size_t)slot * kStageFloats), sc + t0, bytes, bar);
+// Cut search shared by both kernels: the candidate count of a head and
+// whether a cut has to be found (0 < ksel < n).
+struct HeadSel {
+  int L, n, ksel;
+  bool search;
+};
+__device__ __forceinline__ HeadSel head_sel(const SelectParams &p, int bh) {
+  HeadSel h;
+  h.L = KVX_SELECT_LEN(p, bh / p.Hkv);
+  h.n = max(0, h.L - p.recent);
+  h.ksel = min(p.top, h.n);
+  h.search = h.ksel > 0 && h.ksel < h.n;
+  return h;
+}
+
+// Bucket pass, grid (position spans, heads). Every block finds the cut's
+// first digit d0 from the score kernel's histogram, then reads its span of
+// scores once (float4 per lane): positions whose first digit is above d0 go
+// into the above-cut bitmask (word j of a warp's 128 positions is collected
+// from lanes 8j..8j+7), positions in the bucket d0 are appended to the head's
+// (key, position) list: staged in shared memory (one shared atomic per warp)
+// and copied out after one global atomic per block (many atomics on one
+// global counter would serialise).
+__global__ void __launch_bounds__(kBucketThreads, 2) select_bucket_kernel(const SelectParams p) {
+  __shared__ int hist[2048];
+  __shared__ uint2 sl[kBlockBucketCap];
+  __shared__ uint32_t s_digit;
+  __shared__ int s_k, s_cnt, s_base;
+  __shared__ int wsum[kBucketThreads / 32];
+  const int bh = blockIdx.y;
+  const HeadSel hs = head_sel(p, bh);
+  const int t_begin = blockIdx.x * kBucketSpan;
+  if (!hs.search || t_begin >= hs.n) return;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n = hs.n, nwords = (n + 31) >> 5;
+  const float4 *sc4 = reinterpret_cast<const float4 *>(p.scores + (size_t)bh * p.ldsc);
+  uint32_t *gtw = p.bgt + (size_t)bh * p.wstride;
+  uint2 *list = p.blist + (size_t)bh * kBucketCap;
+  constexpr int UA = kBucketSpan / 4 / kBucketThreads;
+  const int i0 = t_begin / 4, n4 = (n + 3) >> 2;
+  // the span's scores are loaded while the cut's first digit is found
+  float4 v[UA];
+#pragma unroll
+  for (int j = 0; j < UA; ++j) {
+    const int i4 = i0 + j * kBucketThreads + tid;
+    v[j] = i4 < n4 ? __ldcg(sc4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int i = tid; i < 2048; i += kBucketThreads) hist[i] = p.hist0[(size_t)bh * 2048 + i];
+  if (tid == 0) s_cnt = 0;
+  __syncthreads();
+  find_digit_block<kBucketThreads>(hist, 2048, hs.ksel, &s_digit, &s_k, wsum);
+  const uint32_t d0 = s_digit;
+  // Away from NaN, infinities and the two zeros (digits 0..3, 1023, 1024 and
+  // 2044 up), the bucket d0 is the float interval [lo, hi) of its keys, so
+  // two float compares classify a score; the key is computed only for the
+  // few scores in the bucket. Elsewhere every score's key is compared.
+  const bool fast = d0 >= 4 && d0 <= 2043 && d0 != 1023 && d0 != 1024;
+  const float lo = key_float(d0 << 21), hi = key_float((d0 + 1) << 21);
+#pragma unroll
+  for (int j = 0; j < UA; ++j) {
+    const int t = 4 * (i0 + j * kBucketThreads + tid);
+    if (t - 4 * lane >= n) break;  // warp-uniform: the warp's 128 positions start past n
+    const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+    uint32_t ng = 0, nb = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const bool in = t + e < n;
+      bool above, inb;
+      if (fast) {
+        above = f[e] >= hi;
+        inb = f[e] >= lo && !above;
+      } else {
+        const uint32_t dg = order_key(f[e]) >> 21;
+        above = dg > d0;
+        inb = dg == d0;
+      }
+      ng |= (uint32_t)(in && above) << e;
+      nb |= (uint32_t)(in && inb) << e;
+    }
+    uint32_t wg = ng << (4 * (lane & 7));
+#pragma unroll
+    for (int sh = 1; sh < 8; sh <<= 1) wg |= __shfl_xor_sync(0xffffffffu, wg, sh);
+    if ((lane & 7) == 0 && (t >> 5) < nwords) gtw[t >> 5] = wg;
+    if (nb) {
+      int off = atomicAdd(&s_cnt, __popc(nb));
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if ((nb >> e) & 1u) {
+          if (off < kBlockBucketCap) sl[off] = make_uint2(order_key(f[e]), (uint32_t)(t + e));
+          ++off;
+        }
+    }
+  }
+  __syncthreads();
+  const int c = s_cnt;
+  // a block whose bucket share does not fit marks the whole head as
+  // overflowed (its count alone exceeds the list)
+  if (tid == 0) s_base = atomicAdd(p.bcnt + bh, c > kBlockBucketCap ? kBucketCap + 1 : c);
+  __syncthreads();
+  if (c <= kBlockBucketCap)
+    for (int i = tid; i < c && s_base + i < kBucketCap; i += kBucketThreads)
+      list[s_base + i] = sl[i];
 }
 
 // One block per head. The cut (the key of the ksel-th largest candidate) is
-// found by a radix select over 11, 11 and 10 bits, MSB first; the first
-// digit's histogram comes from the score kernel.
-//   stream  the head's scores pass once through a ring of shared-memory
-//           chunks (bulk copies); each position whose first digit is above
-//           the cut's goes into the above-cut bitmask, each one in the cut's
-//           bucket into a (key, position) list;
-//   cut     the other two digits are selected over the list;
-//   mark    list entries above the cut join the above-cut bitmask, entries
-//           equal to it the at-cut bitmask;
-//   write   each warp writes the selected positions of its words in
-//           ascending order, keys equal to the cut lowest position first.
-// If the bucket overflows the list, the two digits and the bitmasks are
-// computed by scans of the scores in global memory instead.
+// found by a radix select over 11, 11 and 10 bits, MSB first: the first digit
+// from the score kernel's histogram, the other two over the bucket list that
+// the bucket pass gathered (loaded into shared memory). List entries above
+// the cut join the above-cut bitmask, entries equal to it the at-cut
+// bitmask; each warp then writes the selected positions of its words in
+// ascending order, keys equal to the cut lowest position first. If the bucket
+// overflowed the list, the two digits and the bitmasks come from scans of
+// the scores in global memory instead.
 __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectParams p) {
-  extern __shared__ __align__(128) uint8_t dsm[];
-  float *ring = reinterpret_cast<float *>(dsm);
-  uint2 *list = reinterpret_cast<uint2 *>(ring + kStages * kStageFloats);
+  extern __shared__ __align__(16) uint8_t dsm[];
+  uint2 *list = reinterpret_cast<uint2 *>(dsm);
   uint32_t *gtw = reinterpret_cast<uint32_t *>(list + kBucketCap);
-  uint32_t *eqw = gtw + ((p.Lmax + 31) >> 5);
+  uint32_t *eqw = gtw + p.wstride;
   __shared__ int hist[2048];
   __shared__ int wcnt[2][kTopkWarps];
-  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ int wsum[kTopkWarps];
   __shared__ uint32_t s_digit;
-  __shared__ int s_k, s_cnt, s_abort;
+  __shared__ int s_k;
   const int bh = blockIdx.x;
-  const int b = bh / p.Hkv;
-  const int L = KVX_SELECT_LEN(p, b);
+  const HeadSel hs = head_sel(p, bh);
+  const int L = hs.L, n = hs.n, ksel = hs.ksel;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0 && L != p.seq_len[b]) atomicOr(p.status, KVX_DEV_BAD_LENGTH);
-  const int n = max(0, L - p.recent);
-  const int ksel = min(p.top, n);
+  if (tid == 0 && L != p.seq_len[bh / p.Hkv]) atomicOr(p.status, KVX_DEV_BAD_LENGTH);
   const int nwords = (n + 31) >> 5;
   const float *sc = p.scores + (size_t)bh * p.ldsc;
   int32_t *out = p.kept_idx + (size_t)bh * p.stride;
-  const bool take_all = ksel >= n, none = ksel == 0;
-  const bool search = !take_all && !none;
-  const int nch = (n + kStageFloats - 1) / kStageFloats;
-  if (tid == 0) {
-    s_cnt = 0;
-    s_abort = 0;
-    for (int i = 0; i < kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
-    fence_barrier_init();
-  }
-  // above-cut words start as "all candidates" or "none"; at-cut words empty
+  const bool take_all = ksel >= n;
+  const int cnt = hs.search ? min(p.bcnt[bh], kBucketCap + 1) : 0;
+  const bool in_smem = cnt <= kBucketCap;
+  // bitmasks: above-cut from the bucket pass (or all / none), at-cut empty
+  const uint32_t *ggt = p.bgt + (size_t)bh * p.wstride;
   for (int w = tid; w < nwords; w += kTopkThreads) {
     const int rem = n - 32 * w;
-    gtw[w] = take_all ? (rem >= 32 ? 0xffffffffu : (1u << rem) - 1u) : 0u;
+    gtw[w] = hs.search ? (in_smem ? __ldcg(ggt + w) : 0u)
+                       : (take_all ? (rem >= 32 ? 0xffffffffu : (1u << rem) - 1u) : 0u);
     eqw[w] = 0u;
   }
-  if (search)
+  if (hs.search) {
+    if (in_smem)
+      for (int i = tid; i < cnt; i += kTopkThreads)
+        list[i] = __ldcg(p.blist + (size_t)bh * kBucketCap + i);
     for (int i = tid; i < 2048; i += kTopkThreads) hist[i] = p.hist0[(size_t)bh * 2048 + i];
+  }
   __syncthreads();
   uint32_t prefix = 0;
   int k = ksel;
-  if (search) {
-    if (tid == 0)
-      for (int c = 0; c < min(kStages, nch); ++c) issue_chunk(sc, n, c, ring, bars);
-    if (warp == 0) find_digit(hist, 2048, k, &s_digit, &s_k);
-    __syncthreads();
-    const uint32_t d0 = s_digit;
-    prefix = d0 << 21;
+  if (hs.search) {
+    find_digit_block<kTopkThreads>(hist, 2048, k, &s_digit, &s_k, wsum);
+    prefix = s_digit << 21;
     uint32_t mask = 0x7FFu << 21;
     k = s_k;
-    // stream: one float4 of each chunk per thread
-    int c_stop = nch;
-    for (int c = 0; c < nch; ++c) {
-      const int slot = c % kStages;
-      if (!mbar_wait(smem_u32(&bars[slot]), (uint32_t)(c / kStages) & 1u, kSelectWaitNs))
-        s_abort = 1;
-      const int t = c * kStageFloats + 4 * tid;
-      const float4 v = reinterpret_cast<const float4 *>(ring + (size_t)slot * kStageFloats)[tid];
-      const float f[4] = {v.x, v.y, v.z, v.w};
-      uint32_t ng = 0, nb = 0;
-      uint32_t u[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        u[e] = order_key(f[e]);
-        const bool in = t + e < n;
-        ng |= (uint32_t)(in && (u[e] >> 21) > d0) << e;
-        nb |= (uint32_t)(in && (u[e] >> 21) == d0) << e;
-      }
-      // above-cut bits: lanes 8j..8j+7 hold word j of the warp's 128 positions
-      uint32_t wg = ng << (4 * (lane & 7));
-#pragma unroll
-      for (int sh = 1; sh < 8; sh <<= 1) wg |= __shfl_xor_sync(0xffffffffu, wg, sh);
-      const int w = (t >> 5);
-      if ((lane & 7) == 0 && w < nwords) gtw[w] = wg;
-      // bucket entries: one shared atomic per warp
-      if (__any_sync(0xffffffffu, nb != 0)) {
-        const int cntl = __popc(nb);
-        int incl = cntl;
-#pragma unroll
-        for (int sh = 1; sh < 32; sh <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, incl, sh);
-          if (lane >= sh) incl += y;
-        }
-        int base = 0;
-        if (lane == 31) base = atomicAdd(&s_cnt, incl);
-        int off = __shfl_sync(0xffffffffu, base, 31) + incl - cntl;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((nb >> e) & 1u) {
-            if (off < kBucketCap) list[off] = make_uint2(u[e], (uint32_t)(t + e));
-            ++off;
-          }
-      }
-      __syncthreads();
-      if (s_abort) {
-        c_stop = c;
-        break;
-      }
-      if (tid == 0 && c + kStages < nch) issue_chunk(sc, n, c + kStages, ring, bars);
-    }
-    if (s_abort) {
-      // let copies still in flight land before the block exits: chunks up
-      // to c_stop + kStages - 1 were issued
-      if (tid == 0) {
-        const int last = min(nch, c_stop + kStages) - 1;
-        for (int c = max(c_stop, last - kStages + 1); c <= last; ++c)
-          mbar_wait(smem_u32(&bars[c % kStages]), (uint32_t)(c / kStages) & 1u, kSelectWaitNs);
-        atomicOr(p.status, KVX_DEV_TIMEOUT);
-        p.kept_count[bh] = 0;
-      }
-      for (int i = tid; i < p.stride; i += kTopkThreads) out[i] = -1;
-      return;
-    }
-    const int cnt = s_cnt;
-    const bool in_smem = cnt <= kBucketCap;
+    __syncthreads();
     for (int pass = 1; pass < 3; ++pass) {
       const int bits = pass == 1 ? 11 : 10;
       const int shift = pass == 1 ? 10 : 0;
@@ -351,8 +386,7 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectP
         }
       }
       __syncthreads();
-      if (warp == 0) find_digit(hist, nbins, k, &s_digit, &s_k);
-      __syncthreads();
+      find_digit_block<kTopkThreads>(hist, nbins, k, &s_digit, &s_k, wsum);
       prefix |= s_digit << shift;
       mask |= (uint32_t)(nbins - 1) << shift;
       k = s_k;
@@ -499,11 +533,28 @@ __global__ void __launch_bounds__(kPackThreads) pack_kept_kernel(const __grid_co
 
 using namespace kvx;
 
+// Workspace: header | hist0 int32 [BH][2048] | bcnt int32 [BH] | scores f32
+// [BH][ldsc] | blist uint2 [BH][kBucketCap] | bgt uint32 [BH][wstride], each
+// section 256-byte aligned; hist0 and bcnt are cleared by one memset per call.
+struct SelectWs {
+  size_t hist0, bcnt, scores, blist, bgt, total;
+};
+SelectWs select_ws_offsets(size_t BH, size_t ldsc, size_t wstride) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  SelectWs w;
+  w.hist0 = KVX_WS_HEADER_BYTES;
+  w.bcnt = w.hist0 + sizeof(int32_t) * 2048 * BH;
+  w.scores = al(w.bcnt + sizeof(int32_t) * BH);
+  w.blist = al(w.scores + sizeof(float) * BH * ldsc);
+  w.bgt = al(w.blist + sizeof(uint2) * BH * kBucketCap);
+  w.total = al(w.bgt + sizeof(uint32_t) * BH * wstride);
+  return w;
+}
+
 extern "C" int kvx_select_workspace_bytes(int32_t B, int32_t Hkv, int32_t Lmax, size_t *bytes) {
   if (!bytes || B < 1 || Hkv < 1 || Lmax < 1) return KVX_EINVAL;
-  const size_t ldsc = ((size_t)Lmax + 3) & ~size_t(3);
-  *bytes = KVX_WS_HEADER_BYTES + sizeof(int32_t) * 2048 * (size_t)B * Hkv +
-           sizeof(float) * (size_t)B * Hkv * ldsc;
+  const size_t BH = (size_t)B * Hkv, ldsc = ((size_t)Lmax + 3) & ~size_t(3);
+  *bytes = select_ws_offsets(BH, ldsc, select_wstride(Lmax)).total;
   return KVX_OK;
 }
 
@@ -526,9 +577,15 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
   p.keys = (const __nv_bfloat16 *)keys;
   p.q = (const __nv_bfloat16 *)q;
   p.seq_len = seq_len;
-  p.hist0 = (int32_t *)((char *)workspace + KVX_WS_HEADER_BYTES);
-  p.scores = (float *)((char *)workspace + KVX_WS_HEADER_BYTES +
-                       sizeof(int32_t) * 2048 * (size_t)B * Hkv);
+  const size_t BH = (size_t)B * Hkv;
+  const SelectWs wl = select_ws_offsets(BH, ((size_t)Lmax + 3) & ~size_t(3), select_wstride(Lmax));
+  char *ws = (char *)workspace;
+  p.hist0 = (int32_t *)(ws + wl.hist0);
+  p.bcnt = (int32_t *)(ws + wl.bcnt);
+  p.scores = (float *)(ws + wl.scores);
+  p.blist = (uint2 *)(ws + wl.blist);
+  p.bgt = (uint32_t *)(ws + wl.bgt);
+  p.wstride = (int32_t)select_wstride(Lmax);
   p.kept_idx = kept_idx;
   p.kept_count = kept_count;
   p.status = (uint32_t *)workspace;
@@ -542,7 +599,7 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
   p.stride = top + recent;
   p.ldsc = (Lmax + 3) & ~3;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e0 = cudaMemsetAsync(p.hist0, 0, sizeof(int32_t) * 2048 * (size_t)B * Hkv, st);
+  cudaError_t e0 = cudaMemsetAsync(p.hist0, 0, wl.scores - wl.hist0, st);
   if (e0 != cudaSuccess) return set_cuda_error(e0);
   const dim3 sgrid((Lmax + kScoreTokensPerBlock - 1) / kScoreTokensPerBlock, B * Hkv);
   if (D == 128)
@@ -561,6 +618,8 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
       configured[dev] = 1;
     }
   }
+  const dim3 bgrid((Lmax + kBucketSpan - 1) / kBucketSpan, B * Hkv);
+  select_bucket_kernel<<<bgrid, kBucketThreads, 0, st>>>(p);
   select_topk_kernel<<<B * Hkv, kTopkThreads, topk_smem_bytes(Lmax), st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);
