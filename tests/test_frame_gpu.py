@@ -126,3 +126,69 @@ def test_gather_through_committed_descriptors():
     assert kvx.kvx_workspace_status(ws) == 0
     for frame, (st, ref) in enumerate(zip(stagings, expect)):
         assert np.array_equal(st.cpu().numpy(), ref), frame
+
+
+def test_full_size_churn_matches_oracle():
+    """The benchmark's churn on its full pool (256 sequences, at most 1024
+    blocks each, 655 360 physical blocks): per step every sequence gains a
+    token, sequences end (Trim) and are replaced by new prompts that share a
+    live prefix (Alias) or not, full windows drop their oldest block (Trim),
+    blocks are reserved 8 at a time; one commit per step. The committed
+    device descriptor equals the oracle pager's state at sampled steps."""
+    cfg = synth.gather_config(seed=0)
+    S, M, N, bt_tok, look = cfg.S, cfg.max_blocks, cfg.num_phys, 16, 8
+    f = kvx.Frame(S, M, N)
+    o = oracle.load().frame(S, M, N)
+    gen = synth.rng(4242)
+    tokens = cfg.seq_tokens.astype(np.int64).copy()
+    nbv = np.zeros(S, np.int64)
+
+    def both(op, *args):
+        if op == "reserve":
+            a, ia = f.reserve(*args)
+            b, ib = o.reserve(*args)
+            assert np.array_equal(ia, ib), (op, args)
+        else:
+            a, b = getattr(f, op)(*args), getattr(o, op)(*args)
+        assert (a == kvx.KVX_OK) == (b == 0), (op, args, a, b)
+        return b
+
+    def need(t):
+        return int(min(M, -(-int(t) // bt_tok)))
+
+    def grow(s):
+        want = need(tokens[s])
+        if want > nbv[s]:
+            c = int(min(M - nbv[s], max(want - nbv[s], look)))
+            assert both("reserve", s, c) == 0
+            nbv[s] += c
+
+    for s in range(S):
+        grow(s)
+    stream = torch.cuda.Stream()
+    for step in range(120):
+        tokens += 1
+        for s in np.flatnonzero(gen.random(S) < 1.0 / 100):
+            s = int(s)
+            assert both("trim", s, 0, 0) == 0
+            nbv[s] = 0
+            tokens[s] = int(gen.integers(512, M * bt_tok - 512))
+            r = int(gen.integers(0, S))
+            k = int(min(nbv[r], need(tokens[s]) // 2))
+            if gen.random() < 0.25 and r != s and k > 0:
+                assert both("alias", s, 0, r, 0, k) == 0
+                nbv[s] = k
+        for s in np.flatnonzero(tokens > M * bt_tok):
+            s = int(s)
+            assert both("trim", s, 1, int(nbv[s])) == 0
+            nbv[s] -= 1
+            tokens[s] -= bt_tok
+        for s in range(S):
+            grow(s)
+        f.commit(stream)
+        if step % 20 == 19:
+            stream.synchronize()
+            bt, nb = active(f)
+            table, onb, _ = o.state()
+            assert np.array_equal(nb.cpu().numpy(), onb), step
+            assert np.array_equal(bt.cpu().numpy(), table), step

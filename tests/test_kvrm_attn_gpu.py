@@ -81,3 +81,48 @@ def test_attention_over_staging_and_over_fragmented_pool(seed):
     kept = [np.arange(L[s], dtype=np.int32) for s in range(S) for _ in range(Hkv)]
     ref = oracle.load().decode_attn(q, kd, vd, L, kept, 1.0 / math.sqrt(D))
     assert float(np.abs(over_staging - ref).max()) <= TOL
+
+
+def test_full_size_kvrm_attention_sampled_sequences():
+    """The benchmark's KV-RM workload at full size: 256 sequences of 512..16k
+    tokens, 32 KB blocks randomly permuted over a 40 GiB K+V pool, gathered
+    into [256][16384] staging rows; attention over the staging rows and
+    directly over the pool must agree bit for bit everywhere, and match the
+    oracle on sampled sequences (rebuilt on the host from the value table)."""
+    from synth.device import ValueTable
+    cfg = synth.gather_config(seed=0)
+    S, Hq, Hkv, D, mb = cfg.S, 32, 8, 128, cfg.max_blocks
+    table = ValueTable(seed=21, rows=1 << 18, D=D, dtype="bf16")
+    shifts = [7, 1007]
+    pools, stagings = [], []
+    for t in range(2):
+        p = torch.empty((cfg.num_phys, 16, Hkv, D), dtype=torch.bfloat16, device="cuda")
+        table.fill(p, shifts[t])
+        pools.append(p)
+        stagings.append(torch.zeros((S, mb * 16, Hkv, D), dtype=torch.bfloat16, device="cuda"))
+    bt = torch.from_numpy(cfg.bt).cuda()
+    ws = torch.zeros(kvx.kvx_gather_workspace_bytes(S, mb) // 4 + 64, dtype=torch.int32,
+                     device="cuda")
+    kvx.kvx_gather_coalesce(bt, torch.from_numpy(cfg.nb).cuda(), S, mb, pools, cfg.num_phys,
+                            cfg.block_bytes, stagings, cfg.row_bytes, 0, ws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == 0
+    L = np.ascontiguousarray(cfg.seq_tokens, dtype=np.int32)
+    q = synth.normal(synth.rng(77), (S, Hq, D), "bf16")
+    q_dev = _bf16_dev(q)
+    ident = torch.arange(S * mb, dtype=torch.int32, device="cuda").view(S, mb)
+    over_staging = _attn(S, Hq, Hkv, D, L, q_dev, stagings[0], stagings[1], ident, S * mb)
+    direct = _attn(S, Hq, Hkv, D, L, q_dev, pools[0], pools[1], bt, cfg.num_phys)
+    assert np.array_equal(over_staging, direct)
+    orc = oracle.load()
+    rows_per_block = 16 * Hkv
+    for s in sorted({0, S - 1, int(np.argmax(L)), int(np.argmin(L)), 17, 101}):
+        tok = np.arange(L[s])
+        blk = cfg.bt[s, tok // 16].astype(np.int64)
+        # pool row of (token, head): block * 128 + (token % 16) * 8 + head
+        ids = (blk * rows_per_block + (tok % 16) * Hkv)[:, None] + np.arange(Hkv)
+        kd = table.host_rows(shifts[0], ids.reshape(-1)).reshape(L[s], Hkv, D).transpose(1, 0, 2)
+        vd = table.host_rows(shifts[1], ids.reshape(-1)).reshape(L[s], Hkv, D).transpose(1, 0, 2)
+        kept = [np.arange(L[s], dtype=np.int32)] * Hkv
+        ref = orc.decode_attn(q[s:s + 1], kd[None], vd[None], L[s:s + 1], kept, 1.0 / math.sqrt(D))
+        assert float(np.abs(over_staging[s] - ref[0]).max()) <= TOL, s
