@@ -257,3 +257,45 @@ def test_token_major_fp32_tiny():
     case = synth.tiny(0, "one")
     got = DeviceCase(case, make_plan(case, num_ctas=3, layout=kvx.KVX_LAYOUT_TOKEN_MAJOR)).run()
     assert max_abs(got, oracle_out(case)) <= TOL_F32
+
+
+def mha_p128_16_groups(seed=0):
+    """Limits: 64 KV heads (no GQA), 16 head groups, pages of 128 tokens."""
+    g = synth.rng(seed + 50)
+    L = [1000, 300]
+    n = [[int(g.integers(1, L[b] + 1)) if h % 5 else L[b] for h in range(64)] for b in range(2)]
+    return synth.dense_case(2, 64, 64, 128, L, n, "bf16", seed=seed, P=128,
+                            head_group=np.arange(64, dtype=np.int32) % 16)
+
+
+def g7_d64_p8(seed=0):
+    """GQA factor 7, head dimension 64, pages of 8 tokens, 4 groups."""
+    L = [257, 1031, 64]
+    n = [[257, 31, 1, 200, 8, 9, 257, 100], [1031, 500, 17, 1030, 33, 1, 2, 64],
+         [64, 64, 1, 63, 32, 33, 7, 64]]
+    return synth.dense_case(3, 56, 8, 64, L, n, "bf16", seed=seed, P=8,
+                            head_group=[0, 1, 2, 3, 0, 1, 2, 3])
+
+
+def g3_p32(seed=0):
+    """GQA factor 3, pages of 32 tokens."""
+    return synth.dense_case(2, 12, 4, 128, [900, 33], [[900, 450, 31, 32], [33, 1, 33, 17]],
+                            "bf16", seed=seed, P=32, head_group=[0, 0, 1, 1])
+
+
+EXTREME_CASES = {"mha_p128_16_groups": mha_p128_16_groups, "g7_d64_p8": g7_d64_p8,
+                 "g3_p32": g3_p32}
+
+
+@pytest.mark.parametrize("name", sorted(EXTREME_CASES))
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+@pytest.mark.parametrize("layout", [kvx.KVX_LAYOUT_HEAD_MAJOR, kvx.KVX_LAYOUT_TOKEN_MAJOR])
+def test_extreme_shapes(name, kernel, layout):
+    case = EXTREME_CASES[name]()
+    plan = make_plan(case, num_ctas=0, kernel=kernel, layout=layout)
+    dev = DeviceCase(case, plan)
+    got = dev.run()
+    assert np.all(np.isfinite(got))
+    err = max_abs(got, oracle_out(case))
+    assert err <= TOL_BF16, err
+    assert dev.status() == 0
