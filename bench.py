@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -257,7 +258,8 @@ def job_rate(total_bytes: float, ms: float) -> float:
 class Clocks:
     def __init__(self):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "bench_clocks.csv")
+        self.path = os.environ.get("KVX_BENCH_CLOCKS") or os.path.join(
+            tempfile.gettempdir(), "kvx_bench_clocks.csv")
 
     def start(self):
         try:

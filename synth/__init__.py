@@ -221,7 +221,7 @@ def _rate_to_count(rate: float, L: int) -> int:
 
 def decode_config(name: str, seed: int = 0, layers: int | None = None,
                   batch: int | None = None) -> DecodeConfig:
-    """Recipes of the decode workloads (shapes as stated in the design doc):
+    """Recipes of the decode workloads:
 
     qwen3_4b      36 layers, 32/8 heads, D 128, bf16, batch 16, L ~ U{8192..32768};
                   per layer 2 random KV heads keep everything, the other 6 keep a
