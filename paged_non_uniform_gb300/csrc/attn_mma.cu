@@ -475,14 +475,22 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       if (kMergeBufs == 1 && item.slot < 0) consumer_sync(kCons * 32);
       if (item.slot >= 0) {
         // Publish this piece; the block that finishes the head's last piece
-        // merges all of them and rearms the counter for the next call.
-        __threadfence();
+        // merges all of them and rearms the counter for the next call. After
+        // the barrier, one thread's fence before the ticket releases every
+        // partial write of the block (the fence is cumulative over writes the
+        // barrier ordered before it), and the last block's fence after the
+        // ticket acquires the other blocks' partials for all its threads
+        // through the second barrier.
         consumer_sync(kCons * 32);
-        if (tid == 0)
-          *last_flag = atomicAdd(p.counters + item.split, 1) == p.split[item.split].count - 1;
+        if (tid == 0) {
+          __threadfence();
+          const bool last =
+              atomicAdd(p.counters + item.split, 1) == p.split[item.split].count - 1;
+          if (last) __threadfence();
+          *last_flag = last;
+        }
         consumer_sync(kCons * 32);
         if (*last_flag) {
-          __threadfence();
           merge_split<D, kCons * 32>(p, p.split[item.split], tid);
           if (tid == 0) p.counters[item.split] = 0;
         }
