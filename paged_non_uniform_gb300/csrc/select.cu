@@ -500,32 +500,56 @@ struct PackParams {
   int32_t B, Hkv, D, P, Lmax, stride, layout;
 };
 
-// One token row per LPT lanes: kept row i of head (b, h) -> token i of its pages.
+// Kept row i of head (b, h) -> token i of its pages. LPT lanes move one row
+// (16 bytes each of K and V); a thread group handles kPackRows rows spaced
+// rows_per_block apart, with every load issued before the stores.
+constexpr int kPackRows = 4;
 __global__ void __launch_bounds__(kPackThreads) pack_kept_kernel(const __grid_constant__ PackParams p) {
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, h = bh - b * p.Hkv;
   const int n = p.n[bh];
   const int LPT = p.D / 8;  // 16-byte pieces per row
   const int rows_per_block = kPackThreads / LPT;
-  const int i = blockIdx.x * rows_per_block + threadIdx.x / LPT;
+  const int i0 = blockIdx.x * rows_per_block * kPackRows + threadIdx.x / LPT;
   const int part = threadIdx.x % LPT;
-  if (i >= n) return;
+  if (i0 >= n) return;
   const GroupDesc &gd = p.grp[p.head_grp[h]];
   const int r = p.head_row[h];
-  const int t = p.kept_idx[(size_t)bh * p.stride + i];
-  const int32_t page = gd.page_table[(size_t)b * gd.stride + i / p.P];
-  if (t < 0 || t >= p.Lmax || page < 0 || (int64_t)page >= gd.num_pages) {
-    if (part == 0) atomicOr(p.status, t < 0 || t >= p.Lmax ? KVX_DEV_BAD_BLOCK : KVX_DEV_BAD_PAGE);
-    return;
+  int t[kPackRows];
+  int32_t page[kPackRows];
+#pragma unroll
+  for (int j = 0; j < kPackRows; ++j) {
+    const int i = i0 + j * rows_per_block;
+    t[j] = i < n ? p.kept_idx[(size_t)bh * p.stride + i] : -1;
+    page[j] = i < n ? gd.page_table[(size_t)b * gd.stride + i / p.P] : -1;
   }
-  const int slot = i & (p.P - 1);
-  const size_t row = p.layout == KVX_LAYOUT_HEAD_MAJOR
-                         ? ((size_t)page * gd.size + r) * p.P + slot
-                         : ((size_t)page * p.P + slot) * gd.size + r;
-  const size_t src = ((size_t)bh * p.Lmax + t) * LPT + part;
-  const size_t dst = row * LPT + part;
-  reinterpret_cast<uint4 *>(const_cast<void *>(gd.k_pool))[dst] = __ldcs(p.keys + src);
-  reinterpret_cast<uint4 *>(const_cast<void *>(gd.v_pool))[dst] = __ldcs(p.values + src);
+  uint4 kv[kPackRows][2];
+  bool ok[kPackRows];
+#pragma unroll
+  for (int j = 0; j < kPackRows; ++j) {
+    const int i = i0 + j * rows_per_block;
+    ok[j] = i < n && t[j] >= 0 && t[j] < p.Lmax && page[j] >= 0 &&
+            (int64_t)page[j] < gd.num_pages;
+    if (i < n && !ok[j] && part == 0)
+      atomicOr(p.status, t[j] < 0 || t[j] >= p.Lmax ? KVX_DEV_BAD_BLOCK : KVX_DEV_BAD_PAGE);
+    if (ok[j]) {
+      const size_t src = ((size_t)bh * p.Lmax + t[j]) * LPT + part;
+      kv[j][0] = __ldcs(p.keys + src);
+      kv[j][1] = __ldcs(p.values + src);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kPackRows; ++j) {
+    if (!ok[j]) continue;
+    const int i = i0 + j * rows_per_block;
+    const int slot = i & (p.P - 1);
+    const size_t row = p.layout == KVX_LAYOUT_HEAD_MAJOR
+                           ? ((size_t)page[j] * gd.size + r) * p.P + slot
+                           : ((size_t)page[j] * p.P + slot) * gd.size + r;
+    const size_t dst = row * LPT + part;
+    reinterpret_cast<uint4 *>(const_cast<void *>(gd.k_pool))[dst] = kv[j][0];
+    reinterpret_cast<uint4 *>(const_cast<void *>(gd.v_pool))[dst] = kv[j][1];
+  }
 }
 
 }  // namespace
@@ -674,7 +698,7 @@ extern "C" int kvx_pack_kept(const kvx_plan *plan, const void *keys, const void 
   p.Lmax = Lmax;
   p.stride = kept_stride;
   p.layout = s.layout;
-  const int rows_per_block = kPackThreads / (s.D / 8);
+  const int rows_per_block = kPackThreads / (s.D / 8) * kPackRows;
   const dim3 grid((maxn + rows_per_block - 1) / rows_per_block, s.B * s.Hkv);
   if (grid.x > 0)
     pack_kept_kernel<<<grid, kPackThreads, 0, (cudaStream_t)stream>>>(p);
