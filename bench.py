@@ -407,25 +407,48 @@ def run_ours(args, rank, world):
                          pin_memory=True)
     for l in range(cfg.layers):
         q_host[l].copy_(layers[l].q.cpu())
-    out_host = torch.empty((cfg.layers, cfg.B, cfg.Hq, cfg.D), dtype=torch.float32,
-                           pin_memory=True)
-    q_dev = torch.empty_like(q_host, device=dev)
     e2e_steps = max(3, args.steps // 2)
+    # Every step copies its q from pinned host memory and reads its outputs
+    # back. The copies run on a second stream, double-buffered: step k+1's q
+    # goes up and step k-1's outputs come down while step k computes.
+    q_dev = [torch.empty_like(q_host, device=dev) for _ in range(2)]
+    out_dev = [torch.empty_like(outs) for _ in range(2)]
+    out_host = [torch.empty(tuple(outs.shape), dtype=torch.float32, pin_memory=True)
+                for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # q of buffer i is on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # compute on buffer i has finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # outputs of buffer i are on the host
 
-    def e2e_step():
-        q_dev.copy_(q_host, non_blocking=True)
+    def stage_in(i):
+        copy_stream.wait_event(ev_done[i])
+        with torch.cuda.stream(copy_stream):
+            q_dev[i].copy_(q_host, non_blocking=True)
+        ev_in[i].record(copy_stream)
+
+    def e2e_step(k):
+        i = k % 2
+        stage_in(1 - i)                  # next step's q, behind step k-1's compute
+        stream.wait_event(ev_in[i])
+        stream.wait_event(ev_out[i])     # step k-2's outputs have left out_dev[i]
         for l in range(cfg.layers):
-            call(l, q=q_dev[l])
-        out_host.copy_(outs, non_blocking=True)
+            call(l, q=q_dev[i][l], out=out_dev[i][l])
+        ev_done[i].record(stream)
+        copy_stream.wait_event(ev_done[i])
+        with torch.cuda.stream(copy_stream):
+            out_host[i].copy_(out_dev[i], non_blocking=True)
+        ev_out[i].record(copy_stream)
 
-    for _ in range(2):
-        e2e_step()
+    stage_in(0)
+    for k in range(2):
+        e2e_step(k)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     h0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    stage_in(0)
+    for k in range(e2e_steps):
+        e2e_step(k)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks((time.perf_counter() - h0) * 1e3 / e2e_steps, dist, dev)
     e2e_value = job_rate(bytes_job, e2e_ms)
@@ -474,7 +497,7 @@ def run_ours(args, rank, world):
                          "peak_source": f"{peak_kind} hbm_gbs", "mean_call_us": 1e3 * mean_call_ms},
             "e2e": {"value": e2e_value, "unit": "GB/s",
                     "h2d_bytes_per_step": int(q_host.numel() * 2),
-                    "d2h_bytes_per_step": int(out_host.numel() * 4)},
+                    "d2h_bytes_per_step": int(out_host[0].numel() * 4)},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "plan_host_us_per_layer": float(np.mean(plan_us)),
