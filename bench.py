@@ -733,7 +733,8 @@ def frame_churn(cfg, pools, stagings, dev, stream, peak, kvx, torch, steps, look
     rest; a sequence at the row limit drops its oldest block (Trim). One
     Frame commit per step seals the edits; the coalesced gather then moves
     the committed descriptor's blocks into the staging rows. Times the host
-    edits, the commit (host and device) and the gather."""
+    edits (one batched kvx_frame_edit call per step), the commit (host and
+    device) and the gather."""
     import time
     S, M, N = cfg.S, cfg.max_blocks, cfg.num_phys
     bt_tok = 16  # tokens per block of the gather workload
@@ -745,36 +746,46 @@ def frame_churn(cfg, pools, stagings, dev, stream, peak, kvx, torch, steps, look
     def need(t):
         return np.minimum(M, -(-t // bt_tok))
 
-    def grow(s):
+    def grow(s, ops):
         want = int(need(tokens[s]))
         if want > nbv[s]:
             c = int(min(M - nbv[s], max(want - nbv[s], lookahead)))
-            assert f.reserve(s, c)[0] == kvx.KVX_OK
+            ops.append((kvx.KVX_EDIT_RESERVE, s, c, 0, 0, 0))
             nbv[s] += c
 
+    def submit(ops):
+        if ops:
+            st = f.edit(np.asarray(ops, dtype=np.int32))
+            assert not st.any(), st
+
+    init = []
     for s in range(S):
-        grow(s)
+        grow(s, init)
+    submit(init)
 
     def edits():
+        ops = []
         eos = np.flatnonzero(g.random(S) < p_eos)
         tokens[:] += 1
         for s in eos:
-            assert f.trim(int(s), 0, 0) == kvx.KVX_OK
+            s = int(s)
+            ops.append((kvx.KVX_EDIT_TRIM, s, 0, 0, 0, 0))
             nbv[s] = 0
             tokens[s] = int(g.integers(512, M * bt_tok - 512))
             if g.random() < p_share:
                 r = int(g.integers(0, S))
                 k = int(min(nbv[r], need(tokens[s]) // 2))
                 if r != s and k > 0:
-                    assert f.alias(int(s), 0, r, 0, k) == kvx.KVX_OK
+                    ops.append((kvx.KVX_EDIT_ALIAS, s, 0, r, 0, k))
                     nbv[s] = k
-        full = np.flatnonzero(tokens > M * bt_tok)
-        for s in full:
-            assert f.trim(int(s), 1, int(nbv[s])) == kvx.KVX_OK
+        for s in np.flatnonzero(tokens > M * bt_tok):
+            s = int(s)
+            ops.append((kvx.KVX_EDIT_TRIM, s, 1, int(nbv[s]), 0, 0))
             nbv[s] -= 1
             tokens[s] -= bt_tok
         for s in np.flatnonzero(need(tokens) > nbv):
-            grow(int(s))
+            grow(int(s), ops)
+        submit(ops)
 
     for _ in range(warm):
         edits()
@@ -827,7 +838,8 @@ def frame_churn(cfg, pools, stagings, dev, stream, peak, kvx, torch, steps, look
             "commit_host_us": t_commit / steps * 1e6 - wait_us,
             "commit_wait_us": wait_us,
             "commit_device_us": commit_us, "records_per_step": records / steps,
-            "h2d_bytes_per_step": 8 * records / steps, "apply_launches_per_step": launches / steps,
+            "record_bytes_per_step": 8 * records / steps,
+            "apply_launches_per_step": launches / steps,
             "gather_ms": gather_ms, "gather_gbs": moved / gather_ms / 1e6,
             "gather_frac": moved / gather_ms / 1e6 / peak,
             "blocks_per_seq": blocks / steps / S, "runs_per_seq": runs / S,

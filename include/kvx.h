@@ -327,10 +327,10 @@ int kvx_gather_read_runs(const void *workspace, int32_t S, int32_t max_blocks,
  *     block_table int32 [S][max_blocks], entries past num_blocks[s] are -1;
  *     num_blocks  int32 [S].
  * Two device descriptors are kept (active and shadow). kvx_frame_commit
- * enqueues on `stream` one host-to-device copy of the entries and lengths
- * that changed since the shadow was last current (this frame and the one
- * before) and one kernel that writes them into the shadow, then makes the
- * shadow active. Work that reads a descriptor must be ordered before the
+ * writes the entries and lengths that changed since the shadow was last
+ * current (this frame and the one before) as records in mapped pinned host
+ * memory and enqueues on `stream` one kernel that reads them and writes them
+ * into the shadow, then makes the shadow active. Work that reads a descriptor must be ordered before the
  * commit after the one that made it active (it becomes the shadow that
  * commit writes); on one stream this holds by construction.
  *
@@ -352,7 +352,7 @@ typedef struct {
   int64_t pending_entries; /* table entries edited since the last commit */
   int64_t pending_rows;    /* view lengths changed since the last commit */
   int64_t last_records;    /* (index, value) records the last commit uploaded */
-  int64_t last_bytes;      /* bytes it copied host -> device */
+  int64_t last_bytes;      /* bytes of those records (read by the device from host memory) */
   int64_t launches;        /* apply-kernel launches so far */
   int64_t wait_ns;         /* host time commits spent waiting for the record
                               buffers of the commit before last (stream work
@@ -379,8 +379,21 @@ int kvx_frame_alias(kvx_frame *frame, int32_t dst, int32_t dst_block, int32_t sr
  * (0 <= begin <= end <= nb[seq]); the others are released. Trim(s, 0, 0)
  * ends a sequence; Trim(s, k, nb) drops its k oldest blocks. */
 int kvx_frame_trim(kvx_frame *frame, int32_t seq, int32_t begin_block, int32_t end_block);
-/* Frame commit (see above). Asynchronous on `stream`; the host record
- * buffers of a commit are reused two commits later, after its copy ended. */
+/* Several edits in one call, applied in order exactly as the single-edit
+ * calls would apply them: ops [n][6] int32, one of
+ *     {KVX_EDIT_RESERVE, seq, count, 0, 0, 0}
+ *     {KVX_EDIT_ALIAS, dst, dst_block, src, src_block, count}
+ *     {KVX_EDIT_TRIM, seq, begin_block, end_block, 0, 0}
+ * status [n] (may be NULL) receives each edit's status (KVX_EINVAL for an
+ * unknown kind). A failed edit changes nothing and the later ones are still
+ * applied. Returns KVX_OK, or the status of the first failed edit. */
+#define KVX_EDIT_RESERVE 0
+#define KVX_EDIT_ALIAS 1
+#define KVX_EDIT_TRIM 2
+int kvx_frame_edit(kvx_frame *frame, const int32_t *ops, int32_t n, int32_t *status);
+/* Frame commit (see above). Asynchronous on `stream`: the apply kernel reads
+ * the commit's records from mapped pinned host memory, which is reused two
+ * commits later, after that kernel ended. */
 int kvx_frame_commit(kvx_frame *frame, void *stream);
 /* Device pointers of the active descriptor (valid until the frame is
  * destroyed; their contents change with the second commit after this one). */

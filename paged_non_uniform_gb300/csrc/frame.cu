@@ -15,12 +15,12 @@
 // O(log(N/64)) plus one word scan. Every edited table entry and row is
 // stamped with the frame it changed in.
 //
-// Device side: two descriptors (active, shadow). A commit uploads, as one
-// array of (index, value) records, every entry and row length that changed
-// in this frame or the one before -- the shadow was last current two frames
-// ago -- and one small kernel scatters them into the shadow, which then
-// becomes active. A commit is one host-to-device copy and one launch, or
-// nothing when no entry changed in two frames.
+// Device side: two descriptors (active, shadow). A commit writes, as one
+// array of (index, value) records in mapped pinned host memory, every entry
+// and row length that changed in this frame or the one before -- the shadow
+// was last current two frames ago -- and one small kernel reads them in
+// place and scatters them into the shadow, which then becomes active. A
+// commit is one launch, or nothing when no entry changed in two frames.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -39,11 +39,12 @@ namespace {
 constexpr int kApplyThreads = 256;
 
 // Records [0, ne) set block_table[rec.x] = rec.y; records [ne, ne + nr) set
-// num_blocks[rec.x] = rec.y. Indices are built by the host in range; the
+// num_blocks[rec.x] = rec.y. The records live in mapped pinned host memory
+// (plain loads). Indices are built by the host in range; the
 // checks only keep a damaged record list from writing outside the buffers.
 __global__ void __launch_bounds__(kApplyThreads)
     frame_apply_kernel(int32_t *__restrict__ bt, int32_t *__restrict__ nb,
-                       const int2 *__restrict__ rec, int32_t ne, int32_t nr, int64_t bt_len,
+                       const int2 *rec, int32_t ne, int32_t nr, int64_t bt_len,
                        int32_t S) {
   const int64_t i = (int64_t)blockIdx.x * kApplyThreads + threadIdx.x;
   if (i >= (int64_t)ne + nr) return;
@@ -164,8 +165,8 @@ struct kvx_frame {
   int32_t *d_bt[2] = {nullptr, nullptr};
   int32_t *d_nb[2] = {nullptr, nullptr};
   int active = 0;
-  int2 *h_rec[2] = {nullptr, nullptr};  // pinned
-  int2 *d_rec[2] = {nullptr, nullptr};
+  int2 *h_rec[2] = {nullptr, nullptr};  // pinned, mapped: the apply kernel reads them in place
+  int2 *d_rec[2] = {nullptr, nullptr};  // device address of h_rec
   int64_t rec_cap[2] = {0, 0};
   cudaEvent_t ev[2] = {nullptr, nullptr};
   bool ev_used[2] = {false, false};
@@ -222,7 +223,6 @@ void kvx_frame::free_device() {
     }
     if (d_bt[i]) cudaFree(d_bt[i]);
     if (d_nb[i]) cudaFree(d_nb[i]);
-    if (d_rec[i]) cudaFree(d_rec[i]);
     if (h_rec[i]) cudaFreeHost(h_rec[i]);
     ev[i] = nullptr;
     d_bt[i] = d_nb[i] = nullptr;
@@ -342,6 +342,24 @@ extern "C" int kvx_frame_trim(kvx_frame *f, int32_t seq, int32_t begin_block,
   return KVX_OK;
 }
 
+extern "C" int kvx_frame_edit(kvx_frame *f, const int32_t *ops, int32_t n, int32_t *status) {
+  if (!f || n < 0 || (n > 0 && !ops)) return KVX_EINVAL;
+  int first = KVX_OK;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t *o = ops + 6 * (size_t)i;
+    int rc;
+    switch (o[0]) {
+      case KVX_EDIT_RESERVE: rc = kvx_frame_reserve(f, o[1], o[2], nullptr); break;
+      case KVX_EDIT_ALIAS: rc = kvx_frame_alias(f, o[1], o[2], o[3], o[4], o[5]); break;
+      case KVX_EDIT_TRIM: rc = kvx_frame_trim(f, o[1], o[2], o[3]); break;
+      default: rc = KVX_EINVAL;
+    }
+    if (status) status[i] = rc;
+    if (rc != KVX_OK && first == KVX_OK) first = rc;
+  }
+  return first;
+}
+
 extern "C" int kvx_frame_commit(kvx_frame *f, void *stream) {
   if (!f) return KVX_EINVAL;
   int rc = f->ensure_device();
@@ -367,14 +385,18 @@ extern "C" int kvx_frame_commit(kvx_frame *f, void *stream) {
     if (f->rec_cap[slot] < n) {
       int64_t cap = std::max<int64_t>(4096, f->rec_cap[slot]);
       while (cap < n) cap *= 2;
-      if (f->d_rec[slot]) cudaFree(f->d_rec[slot]);
       if (f->h_rec[slot]) cudaFreeHost(f->h_rec[slot]);
       f->d_rec[slot] = nullptr;
       f->h_rec[slot] = nullptr;
       f->rec_cap[slot] = 0;
-      cudaError_t e = cudaMallocHost(&f->h_rec[slot], sizeof(int2) * (size_t)cap);
-      if (e == cudaSuccess) e = cudaMalloc(&f->d_rec[slot], sizeof(int2) * (size_t)cap);
+      void *hp = nullptr, *dp = nullptr;
+      cudaError_t e = cudaHostAlloc(&hp, sizeof(int2) * (size_t)cap, cudaHostAllocMapped);
+      if (e == cudaSuccess) {
+        f->h_rec[slot] = (int2 *)hp;
+        e = cudaHostGetDevicePointer(&dp, hp, 0);
+      }
       if (e != cudaSuccess) return set_cuda_error(e);
+      f->d_rec[slot] = (int2 *)dp;
       f->rec_cap[slot] = cap;
     }
     int2 *h = f->h_rec[slot];
@@ -386,14 +408,11 @@ extern "C" int kvx_frame_commit(kvx_frame *f, void *stream) {
     for (int32_t s : f->prev_rows)
       if (f->row_stamp[s] != f->frame) h[k++] = make_int2(s, f->nb[s]);
     const int sh = 1 - f->active;
-    cudaError_t e = cudaMemcpyAsync(f->d_rec[slot], h, sizeof(int2) * (size_t)n,
-                                    cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return set_cuda_error(e);
     const int64_t blocks = (n + kApplyThreads - 1) / kApplyThreads;
     frame_apply_kernel<<<(unsigned)blocks, kApplyThreads, 0, st>>>(
         f->d_bt[sh], f->d_nb[sh], f->d_rec[slot], (int32_t)ne, (int32_t)nr,
         (int64_t)f->S * f->M, f->S);
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) e = cudaEventRecord(f->ev[slot], st);
     if (e != cudaSuccess) return set_cuda_error(e);
     f->ev_used[slot] = true;

@@ -25,6 +25,9 @@ KVX_EUNSUPPORTED = -5
 KVX_ESTATE = -6
 KVX_ESCRATCH = -7
 KVX_ENOBLOCKS = -8
+KVX_EDIT_RESERVE = 0
+KVX_EDIT_ALIAS = 1
+KVX_EDIT_TRIM = 2
 
 KVX_DEV_BAD_PAGE = 1
 KVX_DEV_BAD_BUDGET = 2
@@ -124,6 +127,7 @@ lib.kvx_frame_destroy.argtypes = [_vp]
 lib.kvx_frame_reserve.argtypes = [_vp, _c.c_int32, _c.c_int32, _vp]
 lib.kvx_frame_alias.argtypes = [_vp] + [_c.c_int32] * 5
 lib.kvx_frame_trim.argtypes = [_vp, _c.c_int32, _c.c_int32, _c.c_int32]
+lib.kvx_frame_edit.argtypes = [_vp, _vp, _c.c_int32, _vp]
 lib.kvx_frame_commit.argtypes = [_vp, _vp]
 lib.kvx_frame_active.argtypes = [_vp, _c.POINTER(_vp), _c.POINTER(_vp)]
 lib.kvx_frame_view.argtypes = [_vp, _vp, _vp, _vp]
@@ -397,6 +401,14 @@ class Frame:
 
     def trim(self, seq: int, begin_block: int, end_block: int) -> int:
         return lib.kvx_frame_trim(self.handle, int(seq), int(begin_block), int(end_block))
+
+    def edit(self, ops) -> np.ndarray:
+        """Applies ops ([n][6] int32, KVX_EDIT_* rows) in order; returns the
+        status of every edit."""
+        ops = np.ascontiguousarray(ops, dtype=np.int32).reshape(-1, 6)
+        st = np.zeros(max(len(ops), 1), dtype=np.int32)
+        lib.kvx_frame_edit(self.handle, ops.ctypes.data, len(ops), st.ctypes.data)
+        return st[:len(ops)]
 
     def commit(self, stream=None) -> None:
         _check(lib.kvx_frame_commit(self.handle, _stream(stream)), "kvx_frame_commit")

@@ -114,3 +114,27 @@ def test_frame_create_errors():
     assert f.reserve(0, 5)[0] == kvx.KVX_ERANGE
     assert f.alias(0, 1, 1, 0, 1) == kvx.KVX_ERANGE  # src view empty; dst_block past nb
     assert f.trim(0, 1, 0) == kvx.KVX_ERANGE
+
+
+def test_batch_edit_matches_single_edits():
+    """kvx_frame_edit applies a batch exactly as the single-edit calls would,
+    failed edits included (they change nothing and report their status)."""
+    gen = synth.rng(31)
+    S, M, N = 10, 40, 300
+    a, b = kvx.Frame(S, M, N), kvx.Frame(S, M, N)
+    for it in range(40):
+        ops = []
+        for _ in range(25):
+            _, nb, _ = b.state()
+            op, args = random_edits(gen, S, M, nb)
+            kind = {"reserve": kvx.KVX_EDIT_RESERVE, "alias": kvx.KVX_EDIT_ALIAS,
+                    "trim": kvx.KVX_EDIT_TRIM}[op]
+            ops.append([kind, *args] + [0] * (5 - len(args)))
+            single = b.reserve(*args)[0] if op == "reserve" else getattr(b, op)(*args)
+            ops[-1].append(single)
+        ops = np.array(ops, np.int32)
+        st = a.edit(ops[:, :6])
+        assert np.array_equal(st, ops[:, 6]), it
+        for x, y in zip(a.state(), b.state()):
+            assert np.array_equal(x, y), it
+    assert a.edit(np.array([[7, 0, 0, 0, 0, 0]], np.int32))[0] == kvx.KVX_EINVAL
