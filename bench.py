@@ -482,7 +482,7 @@ def run_ours(args, rank, world):
             "config": {"workload": describe(cfg),
                        "l2": "inputs larger than L2: each step streams "
                              f"{bytes_step / 1e9:.1f} GB of distinct KV pages",
-                       "plan": "balanced ahead-of-time split, one persistent block per SM",
+                       "plan": "balanced ahead-of-time split, two persistent blocks per SM",
                        "sms": sms},
             "frac_of_hbm": value / world / peak,
             "seq_heads_per_s": world * cfg.B * cfg.Hq * cfg.layers / (ms_step * 1e-3),

@@ -159,8 +159,10 @@ int kvx_device_sm_count(int32_t *sms);
  *   head_group   int32 [Hkv], group of each KV head, in [0, num_groups); every
  *                group non-empty (host). Within a group, heads take page-slot
  *                rows 0, 1, ... in ascending head order.
- *   num_ctas     thread blocks for KVX_PLAN_BALANCED; 0 = one per SM of the
- *                current device (ignored by the other policies).
+ *   num_ctas     thread blocks for KVX_PLAN_BALANCED; 0 = as many as stay
+ *                resident on the current device (2 per SM for the
+ *                tensor-core kernel, 1 for the CUDA-core kernel); ignored by
+ *                the other policies.
  *   policy       KVX_PLAN_*.   kernel  KVX_KERNEL_*.
  *   out          receives the plan (owned by the caller; kvx_plan_destroy).
  * Errors: KVX_EINVAL, KVX_EUNSUPPORTED, KVX_ENOMEM; *out is NULL on error.
