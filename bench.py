@@ -163,6 +163,68 @@ def cpu_baseline(cfg, seconds):
                       f"one sequence per call, OpenMP over its KV heads)"}
 
 
+def host_cpu() -> dict:
+    """CPU model and logical CPU count of the host."""
+    model = ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            key = line.split(":", 1)[0].strip().lower()
+            if key in ("model name", "cpu part", "hardware"):
+                model = line.split(":", 1)[1].strip()
+                if key != "model name":
+                    model = f"{key} {model}"
+                break
+    except OSError:
+        pass
+    return {"model": model or "unknown", "nproc": os.cpu_count()}
+
+
+def cpu_gather_baseline(S=32, num_phys=65536):
+    """The oracle's block-by-block gather (memcpy per block, OpenMP over rows)
+    on a sample of the KV-RM workload: S sequences of the same length mix
+    over a randomly permuted pool of num_phys 32 KB blocks per tensor (K and
+    V), timed on the host cores. Values are irrelevant to a copy; the
+    buffers are touched before timing."""
+    import oracle
+    orc = oracle.load()
+    cfg = synth.gather_config(seed=0, S=S, num_phys=num_phys)
+    moved, secs = 0, 0.0
+    for _ in range(2):  # K and V
+        pool = np.empty((cfg.num_phys, cfg.block_bytes), np.uint8)
+        pool.fill(1)
+        staging = np.empty((cfg.S, cfg.row_bytes), np.uint8)
+        staging.fill(0)
+        t0 = time.perf_counter()
+        orc.gather(cfg.bt, cfg.nb, pool, staging)
+        secs += time.perf_counter() - t0
+        moved += 2 * int(cfg.nb.sum()) * cfg.block_bytes
+    return {"value": moved / secs / 1e9, "unit": "GB/s moved (read+write)",
+            "cores": orc.num_threads(), "kind": "oracle",
+            "sample": f"{S} sequences, {int(cfg.nb.sum())} live 32 KB blocks per tensor, K and V "
+                      f"pools of {num_phys} blocks each ({moved / 1e9:.2f} GB moved)"}
+
+
+def copy_ceiling(dev, stream, torch, gib=4, reps=10) -> float:
+    """Practical ceiling: device-to-device copy of a buffer larger than L2 with
+    the CUDA runtime (cudaMemcpyAsync through torch), GB/s read + write."""
+    a = torch.empty(gib << 30, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    a.fill_(1)
+    for _ in range(2):
+        b.copy_(a)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        b.copy_(a)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    gbs = 2 * (gib << 30) * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del a, b
+    torch.cuda.empty_cache()
+    return gbs
+
+
 def host_group_pages(cfg):
     """Pages each group needs (for the oracle-only arm, computed like the
     page tables the GPU arm builds: ceil of the group's longest head / P)."""
@@ -391,8 +453,10 @@ def run_ours(args, rank, world):
     call_ms = [[ev[s][l].elapsed_time(ev[s][l + 1]) for l in range(cfg.layers)]
                for s in range(args.steps)]
     mean_call_ms = float(np.mean(call_ms))
-    achieved = float(np.mean([bytes_layer[l] / (call_ms[s][l] * 1e-3)
-                              for s in range(args.steps) for l in range(cfg.layers)])) / 1e9
+    rates = np.array([bytes_layer[l] / (call_ms[s][l] * 1e-3)
+                      for s in range(args.steps) for l in range(cfg.layers)]) / 1e9
+    achieved = float(rates.mean())
+    rate_pct = {f"p{q}": float(np.percentile(rates, q)) for q in (10, 50, 90)}
     peak, peak_kind = peaks()
     prof = profiled_traffic()
     # ncu traffic of the profiled launch (layer 0), scaled to the mean launch
@@ -470,8 +534,11 @@ def run_ours(args, rank, world):
         gather = bench_gather(args, dev, stream, peak, dist, world, rank)
 
     cpu = None
+    ceiling = copy_ceiling(dev, stream, torch)
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(cfg, args.cpu_seconds)
+        cpu["host"] = host_cpu()
+        cpu["gather"] = cpu_gather_baseline()
 
     if rank == 0:
         line = {
@@ -494,7 +561,9 @@ def run_ours(args, rank, world):
                                          "kernel changed since the committed capture",
                          "kernel": "attn_mma_kernel<128> (one launch per layer call)",
                          "timing": "second pass of K steps, CUDA events around every launch",
-                         "peak_source": f"{peak_kind} hbm_gbs", "mean_call_us": 1e3 * mean_call_ms},
+                         "peak_source": f"{peak_kind} hbm_gbs", "mean_call_us": 1e3 * mean_call_ms,
+                         "per_launch_gbs": rate_pct,
+                         "copy_ceiling_gbs": ceiling},
             "e2e": {"value": e2e_value, "unit": "GB/s",
                     "h2d_bytes_per_step": int(q_host.numel() * 2),
                     "d2h_bytes_per_step": int(out_host[0].numel() * 4)},
