@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kScoreThreads) select_score_kernel(const Selec
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kBucketCap = 8192;       // (key, position) pairs kept per head
 constexpr int kBucketThreads = 512;
-constexpr int kBucketSpan = 16384;     // positions per bucket block (8 float4 per thread)
+constexpr int kBucketSpan = 32768;     // positions per bucket block
+constexpr int kBucketUC = 4;           // float4 per thread in each of its sub-spans
 constexpr int kBlockBucketCap = 4096;  // bucket entries one bucket block stages in shared memory
 constexpr int kMaxSelectLmax = 1 << 18;
 
@@ -228,7 +229,8 @@ __device__ __forceinline__ HeadSel head_sel(const SelectParams &p, int bh) {
 
 // Bucket pass, grid (position spans, heads). Every block finds the cut's
 // first digit d0 from the score kernel's histogram, then reads its span of
-// scores once (float4 per lane): positions whose first digit is above d0 go
+// scores once (float4 per lane, the next sub-span loading while the current
+// one is sorted): positions whose first digit is above d0 go
 // into the above-cut bitmask (word j of a warp's 128 positions is collected
 // from lanes 8j..8j+7), positions in the bucket d0 are appended to the head's
 // (key, position) list: staged in shared memory (one shared atomic per warp)
@@ -249,12 +251,14 @@ __global__ void __launch_bounds__(kBucketThreads, 2) select_bucket_kernel(const 
   const float4 *sc4 = reinterpret_cast<const float4 *>(p.scores + (size_t)bh * p.ldsc);
   uint32_t *gtw = p.bgt + (size_t)bh * p.wstride;
   uint2 *list = p.blist + (size_t)bh * kBucketCap;
-  constexpr int UA = kBucketSpan / 4 / kBucketThreads;
+  constexpr int SUB4 = kBucketThreads * kBucketUC;  // float4 per sub-span
+  constexpr int NSUB = kBucketSpan / 4 / SUB4;
   const int i0 = t_begin / 4, n4 = (n + 3) >> 2;
-  // the span's scores are loaded while the cut's first digit is found
-  float4 v[UA];
+  // the first sub-span's scores are loaded while the cut's first digit is
+  // found; each later sub-span is loaded while the previous one is sorted
+  float4 v[kBucketUC];
 #pragma unroll
-  for (int j = 0; j < UA; ++j) {
+  for (int j = 0; j < kBucketUC; ++j) {
     const int i4 = i0 + j * kBucketThreads + tid;
     v[j] = i4 < n4 ? __ldcg(sc4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -269,40 +273,53 @@ __global__ void __launch_bounds__(kBucketThreads, 2) select_bucket_kernel(const 
   // few scores in the bucket. Elsewhere every score's key is compared.
   const bool fast = d0 >= 4 && d0 <= 2043 && d0 != 1023 && d0 != 1024;
   const float lo = key_float(d0 << 21), hi = key_float((d0 + 1) << 21);
+#pragma unroll 1
+  for (int c = 0; c < NSUB; ++c) {
+    const int b4 = i0 + c * SUB4;
+    if (4 * b4 >= n) break;  // block-uniform
+    float4 nx[kBucketUC];
 #pragma unroll
-  for (int j = 0; j < UA; ++j) {
-    const int t = 4 * (i0 + j * kBucketThreads + tid);
-    if (t - 4 * lane >= n) break;  // warp-uniform: the warp's 128 positions start past n
-    const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-    uint32_t ng = 0, nb = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const bool in = t + e < n;
-      bool above, inb;
-      if (fast) {
-        above = f[e] >= hi;
-        inb = f[e] >= lo && !above;
-      } else {
-        const uint32_t dg = order_key(f[e]) >> 21;
-        above = dg > d0;
-        inb = dg == d0;
-      }
-      ng |= (uint32_t)(in && above) << e;
-      nb |= (uint32_t)(in && inb) << e;
+    for (int j = 0; j < kBucketUC; ++j) {
+      const int i4 = b4 + SUB4 + j * kBucketThreads + tid;
+      nx[j] = (c + 1 < NSUB && i4 < n4) ? __ldcg(sc4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    uint32_t wg = ng << (4 * (lane & 7));
 #pragma unroll
-    for (int sh = 1; sh < 8; sh <<= 1) wg |= __shfl_xor_sync(0xffffffffu, wg, sh);
-    if ((lane & 7) == 0 && (t >> 5) < nwords) gtw[t >> 5] = wg;
-    if (nb) {
-      int off = atomicAdd(&s_cnt, __popc(nb));
+    for (int j = 0; j < kBucketUC; ++j) {
+      const int t = 4 * (b4 + j * kBucketThreads + tid);
+      if (t - 4 * lane >= n) break;  // warp-uniform: the warp's 128 positions start past n
+      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+      uint32_t ng = 0, nb = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if ((nb >> e) & 1u) {
-          if (off < kBlockBucketCap) sl[off] = make_uint2(order_key(f[e]), (uint32_t)(t + e));
-          ++off;
+      for (int e = 0; e < 4; ++e) {
+        const bool in = t + e < n;
+        bool above, inb;
+        if (fast) {
+          above = f[e] >= hi;
+          inb = f[e] >= lo && !above;
+        } else {
+          const uint32_t dg = order_key(f[e]) >> 21;
+          above = dg > d0;
+          inb = dg == d0;
         }
+        ng |= (uint32_t)(in && above) << e;
+        nb |= (uint32_t)(in && inb) << e;
+      }
+      uint32_t wg = ng << (4 * (lane & 7));
+#pragma unroll
+      for (int sh = 1; sh < 8; sh <<= 1) wg |= __shfl_xor_sync(0xffffffffu, wg, sh);
+      if ((lane & 7) == 0 && (t >> 5) < nwords) gtw[t >> 5] = wg;
+      if (nb) {
+        int off = atomicAdd(&s_cnt, __popc(nb));
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((nb >> e) & 1u) {
+            if (off < kBlockBucketCap) sl[off] = make_uint2(order_key(f[e]), (uint32_t)(t + e));
+            ++off;
+          }
+      }
     }
+#pragma unroll
+    for (int j = 0; j < kBucketUC; ++j) v[j] = nx[j];
   }
   __syncthreads();
   const int c = s_cnt;
