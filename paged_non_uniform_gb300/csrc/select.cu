@@ -75,10 +75,10 @@ struct SelectParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kScoreThreads) select_score_kernel(const SelectParams p) {
+__global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const SelectParams p) {
   constexpr int LPT = D / 8;          // lanes per token row (16 bytes each)
   constexpr int TPW = 32 / LPT;       // token rows per warp and step
-  constexpr int U = 4;                // steps in flight per lane
+  constexpr int U = 8;                // steps in flight per lane
   __shared__ float Q[D];
   __shared__ int hist[2048];
   __shared__ float s_sc[kScoreTokensPerBlock];
