@@ -10,7 +10,7 @@ import torch
 import oracle
 import synth
 from synth.device import TableLayer, ValueTable
-from paged_non_uniform_gb300 import kvx
+from paged_non_uniform_gb300 import kvx, pages
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-3
@@ -123,3 +123,63 @@ def test_full_size_gpu_selection_sampled_heads(table):
         bh = b * Hkv + h
         kh = table.host_rows(4242, bh * L + np.arange(L, dtype=np.int64))
         check_head(orc, q[b, h * g:(h + 1) * g], kh, top, recent, kept[bh])
+
+
+def test_full_size_select_pack_attend(table):
+    """The benchmark's sparse pipeline at full size (Llama-3-8B shapes, batch 8
+    x 122k, one layer): GPU selection, packing of the kept rows into
+    head-group pages, attention over them. Sampled heads: packed slots equal
+    the dense rows bit for bit, and the output equals the oracle's attention
+    over the same kept set."""
+    cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
+    B, Hq, Hkv, D, L, P = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, int(cfg.seq_len[0]), cfg.P
+    top, recent = 2048, 128
+    keys = torch.empty((B, Hkv, L, D), dtype=torch.bfloat16, device="cuda")
+    vals = torch.empty_like(keys)
+    table.fill(keys, 777)
+    table.fill(vals, 31337)
+    q = synth.normal(synth.rng(98), (B, Hq, D), "bf16")
+    qd = torch.from_numpy(synth.f32_to_bf16_bits(q).view(np.int16)).view(torch.bfloat16).cuda()
+    kept = torch.zeros((B * Hkv, top + recent), dtype=torch.int32, device="cuda")
+    cnt = torch.zeros(B * Hkv, dtype=torch.int32, device="cuda")
+    sl = torch.from_numpy(cfg.seq_len).cuda()
+    ws = torch.zeros(kvx.kvx_select_workspace_bytes(B, Hkv, L) // 4 + 64, dtype=torch.int32,
+                     device="cuda")
+    kvx.kvx_select_topk(keys, qd, sl, B, Hq, Hkv, D, L, top, recent, kept, cnt, ws)
+    torch.cuda.synchronize()
+    n = cnt.cpu().numpy().reshape(B, Hkv)
+    assert np.all(n == top + recent)
+    hg = np.zeros(Hkv, np.int32)
+    plan = kvx.kvx_plan_create(B, Hq, Hkv, D, P, 1, kvx.KVX_BF16, n, cfg.seq_len, hg, 0)
+    kvx.kvx_plan_upload(plan)
+    gp = plan.group_pages()
+    tables, npages = pages.assign_pages(gp, [synth.page_permutation(7, int(gp[0].sum()) + 2)], 2)
+    kp = torch.zeros((npages[0], Hkv, P, D), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    pt = torch.from_numpy(tables[0]).cuda()
+    aws = torch.zeros(plan.workspace_bytes() // 4 + 64, dtype=torch.int32, device="cuda")
+    kvx.kvx_pack_kept(plan, keys, vals, L, kept, top + recent, [kp], [vp], npages, [pt],
+                      [tables[0].shape[1]], aws)
+    out = torch.full((B, Hq, D), float("nan"), device="cuda")
+    kvx.kvx_decode_attn(plan, qd, [kp], [vp], npages, [pt], [tables[0].shape[1]],
+                        torch.from_numpy(n.reshape(-1).copy()).cuda(), sl, 0.0, out, aws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(aws) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    kept_h = kept.cpu().numpy()
+    orc = oracle.load()
+    g = Hq // Hkv
+    for b, h in [(0, 0), (4, 3), (7, 7)]:
+        bh = b * Hkv + h
+        idx = kept_h[bh]
+        rows = bh * L + idx.astype(np.int64)
+        kh = table.host_rows(777, rows)
+        vh = table.host_rows(31337, rows)
+        # packed slots: token i of head h at page tables[0][b, i // P], slot row h
+        t = np.arange(idx.size)
+        pg = tables[0][b, t // P]
+        slots = kp[torch.from_numpy(pg).cuda(), h, torch.from_numpy(t % P).cuda()]
+        assert np.array_equal(slots.float().cpu().numpy(), kh), (b, h)
+        ref = orc.attn_head(q[b, h * g:(h + 1) * g], kh, vh, np.arange(idx.size, dtype=np.int32),
+                            1.0 / math.sqrt(D))
+        assert float(np.abs(got[b, h * g:(h + 1) * g] - ref).max()) <= TOL, (b, h)
