@@ -65,6 +65,24 @@ def test_full_size_sampled_heads(name, table):
         assert err <= TOL, (b, h, err)
 
 
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_full_size_group_sweep_sampled_heads(G, table):
+    """The head-group sweep's configurations (Qwen3-4B layer 0 regrouped into
+    groups of G KV heads; G = 8 is the unified page): sampled heads against
+    the oracle, as the benchmark's group sweep runs them."""
+    cfg = synth.regroup(synth.decode_config("qwen3_4b", seed=0, layers=1), G)
+    plan = _plan(cfg, 0)
+    lay = TableLayer(cfg, 0, table, plan.group_pages(), seed=0)
+    got = _run(plan, lay, cfg)
+    orc = oracle.load()
+    g = cfg.Hq // cfg.Hkv
+    for b, h in _sample_heads(cfg, 0, 4, seed=G):
+        k, v = lay.host_kv(b, h)
+        ref = orc.attn_head(lay.q_host[b, h * g:(h + 1) * g], k, v,
+                            np.arange(k.shape[0], dtype=np.int32), 1.0 / math.sqrt(cfg.D))
+        assert float(np.abs(got[b, h * g:(h + 1) * g] - ref).max()) <= TOL, (G, b, h)
+
+
 def test_full_size_sparse_with_selected_tokens(table):
     """Llama-3-8B shapes, batch 8 x 122k: sampled heads keep the top 2048
     tokens by score plus the 128 most recent, selected from dense keys."""
