@@ -388,11 +388,16 @@ int kvx_frame_trim(kvx_frame *frame, int32_t seq, int32_t begin_block, int32_t e
  *     {KVX_EDIT_TRIM, seq, begin_block, end_block, 0, 0}
  * status [n] (may be NULL) receives each edit's status (KVX_EINVAL for an
  * unknown kind). A failed edit changes nothing and the later ones are still
- * applied. Returns KVX_OK, or the status of the first failed edit. */
+ * applied. ids (may be NULL) receives the block ids of every successful
+ * Reserve, concatenated in edit order; a Reserve whose ids would not fit in
+ * ids_cap entries fails with KVX_ERANGE. *ids_written (may be NULL) gets the
+ * number of ids written. Returns KVX_OK, or the status of the first failed
+ * edit. */
 #define KVX_EDIT_RESERVE 0
 #define KVX_EDIT_ALIAS 1
 #define KVX_EDIT_TRIM 2
-int kvx_frame_edit(kvx_frame *frame, const int32_t *ops, int32_t n, int32_t *status);
+int kvx_frame_edit(kvx_frame *frame, const int32_t *ops, int32_t n, int32_t *status,
+                   int32_t *ids, int64_t ids_cap, int64_t *ids_written);
 /* Frame commit (see above). Asynchronous on `stream`: the apply kernel reads
  * the commit's records from mapped pinned host memory, which is reused two
  * commits later, after that kernel ended. */

@@ -342,14 +342,23 @@ extern "C" int kvx_frame_trim(kvx_frame *f, int32_t seq, int32_t begin_block,
   return KVX_OK;
 }
 
-extern "C" int kvx_frame_edit(kvx_frame *f, const int32_t *ops, int32_t n, int32_t *status) {
-  if (!f || n < 0 || (n > 0 && !ops)) return KVX_EINVAL;
+extern "C" int kvx_frame_edit(kvx_frame *f, const int32_t *ops, int32_t n, int32_t *status,
+                              int32_t *ids, int64_t ids_cap, int64_t *ids_written) {
+  if (!f || n < 0 || (n > 0 && !ops) || ids_cap < 0) return KVX_EINVAL;
   int first = KVX_OK;
+  int64_t written = 0;
   for (int32_t i = 0; i < n; ++i) {
     const int32_t *o = ops + 6 * (size_t)i;
     int rc;
     switch (o[0]) {
-      case KVX_EDIT_RESERVE: rc = kvx_frame_reserve(f, o[1], o[2], nullptr); break;
+      case KVX_EDIT_RESERVE:
+        if (ids && o[2] > 0 && written + o[2] > ids_cap) {
+          rc = KVX_ERANGE;  // no room for its ids: the edit is not applied
+        } else {
+          rc = kvx_frame_reserve(f, o[1], o[2], ids ? ids + written : nullptr);
+          if (rc == KVX_OK && ids) written += o[2];
+        }
+        break;
       case KVX_EDIT_ALIAS: rc = kvx_frame_alias(f, o[1], o[2], o[3], o[4], o[5]); break;
       case KVX_EDIT_TRIM: rc = kvx_frame_trim(f, o[1], o[2], o[3]); break;
       default: rc = KVX_EINVAL;
@@ -357,6 +366,7 @@ extern "C" int kvx_frame_edit(kvx_frame *f, const int32_t *ops, int32_t n, int32
     if (status) status[i] = rc;
     if (rc != KVX_OK && first == KVX_OK) first = rc;
   }
+  if (ids_written) *ids_written = written;
   return first;
 }
 

@@ -127,7 +127,8 @@ lib.kvx_frame_destroy.argtypes = [_vp]
 lib.kvx_frame_reserve.argtypes = [_vp, _c.c_int32, _c.c_int32, _vp]
 lib.kvx_frame_alias.argtypes = [_vp] + [_c.c_int32] * 5
 lib.kvx_frame_trim.argtypes = [_vp, _c.c_int32, _c.c_int32, _c.c_int32]
-lib.kvx_frame_edit.argtypes = [_vp, _vp, _c.c_int32, _vp]
+lib.kvx_frame_edit.argtypes = [_vp, _vp, _c.c_int32, _vp, _vp, _c.c_int64,
+                               _c.POINTER(_c.c_int64)]
 lib.kvx_frame_commit.argtypes = [_vp, _vp]
 lib.kvx_frame_active.argtypes = [_vp, _c.POINTER(_vp), _c.POINTER(_vp)]
 lib.kvx_frame_view.argtypes = [_vp, _vp, _vp, _vp]
@@ -402,13 +403,22 @@ class Frame:
     def trim(self, seq: int, begin_block: int, end_block: int) -> int:
         return lib.kvx_frame_trim(self.handle, int(seq), int(begin_block), int(end_block))
 
-    def edit(self, ops) -> np.ndarray:
+    def edit(self, ops, want_ids: bool = False):
         """Applies ops ([n][6] int32, KVX_EDIT_* rows) in order; returns the
-        status of every edit."""
+        status of every edit (and, with want_ids, the reserved block ids in
+        edit order)."""
         ops = np.ascontiguousarray(ops, dtype=np.int32).reshape(-1, 6)
         st = np.zeros(max(len(ops), 1), dtype=np.int32)
-        lib.kvx_frame_edit(self.handle, ops.ctypes.data, len(ops), st.ctypes.data)
-        return st[:len(ops)]
+        if not want_ids:
+            lib.kvx_frame_edit(self.handle, ops.ctypes.data, len(ops), st.ctypes.data, None, 0,
+                               None)
+            return st[:len(ops)]
+        cap = int(np.maximum(ops[ops[:, 0] == KVX_EDIT_RESERVE, 2], 0).sum())
+        ids = np.zeros(max(cap, 1), dtype=np.int32)
+        nw = _c.c_int64(0)
+        lib.kvx_frame_edit(self.handle, ops.ctypes.data, len(ops), st.ctypes.data,
+                           ids.ctypes.data, cap, _c.byref(nw))
+        return st[:len(ops)], ids[:nw.value]
 
     def commit(self, stream=None) -> None:
         _check(lib.kvx_frame_commit(self.handle, _stream(stream)), "kvx_frame_commit")

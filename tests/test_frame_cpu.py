@@ -123,18 +123,40 @@ def test_batch_edit_matches_single_edits():
     S, M, N = 10, 40, 300
     a, b = kvx.Frame(S, M, N), kvx.Frame(S, M, N)
     for it in range(40):
-        ops = []
+        ops, want = [], []
         for _ in range(25):
             _, nb, _ = b.state()
             op, args = random_edits(gen, S, M, nb)
             kind = {"reserve": kvx.KVX_EDIT_RESERVE, "alias": kvx.KVX_EDIT_ALIAS,
                     "trim": kvx.KVX_EDIT_TRIM}[op]
             ops.append([kind, *args] + [0] * (5 - len(args)))
-            single = b.reserve(*args)[0] if op == "reserve" else getattr(b, op)(*args)
+            if op == "reserve":
+                single, got_ids = b.reserve(*args)
+                want.extend(got_ids.tolist())
+            else:
+                single = getattr(b, op)(*args)
             ops[-1].append(single)
         ops = np.array(ops, np.int32)
-        st = a.edit(ops[:, :6])
+        if it % 2:
+            st, ids = a.edit(ops[:, :6], want_ids=True)
+            assert ids.tolist() == want, it
+        else:
+            st = a.edit(ops[:, :6])
         assert np.array_equal(st, ops[:, 6]), it
         for x, y in zip(a.state(), b.state()):
             assert np.array_equal(x, y), it
     assert a.edit(np.array([[7, 0, 0, 0, 0, 0]], np.int32))[0] == kvx.KVX_EINVAL
+
+
+def test_batch_edit_ids_capacity():
+    f = kvx.Frame(2, 16, 64)
+    ops = np.array([[kvx.KVX_EDIT_RESERVE, 0, 3, 0, 0, 0],
+                    [kvx.KVX_EDIT_RESERVE, 1, 4, 0, 0, 0]], np.int32)
+    ids = np.zeros(5, np.int32)
+    st = np.zeros(2, np.int32)
+    nw = kvx._c.c_int64(0)
+    rc = kvx.lib.kvx_frame_edit(f.handle, ops.ctypes.data, 2, st.ctypes.data, ids.ctypes.data,
+                                5, kvx._c.byref(nw))
+    # the second Reserve does not fit in the id buffer: refused, nothing applied
+    assert rc == kvx.KVX_ERANGE and list(st) == [kvx.KVX_OK, kvx.KVX_ERANGE] and nw.value == 3
+    assert list(ids[:3]) == [0, 1, 2] and list(f.state()[1]) == [3, 0]
