@@ -68,51 +68,70 @@ static void finish_splits(kvx_plan *p) {
       p->cta_tokens[c] += p->items[i].end - p->items[i].begin;
 }
 
-// Balanced: lay the heads' kept tokens end to end, charge each item its
-// tokens plus a fixed overhead, and cut the stream into num_ctas spans of
-// equal cost at stage boundaries.
-static void plan_balanced(kvx_plan *p, int num_ctas) {
-  const int H = p->shape.B * p->shape.Hkv;
+// Greedy fill of `heads` (in order) into blocks of cost at most `cap` each
+// (tokens + c0 per item), cutting at stage boundaries; returns the number of
+// blocks used, or max_ctas + 1 if they do not suffice (out is then partial).
+static int fill_blocks(const kvx_plan *p, const std::vector<int> &heads, double cap, double c0,
+                       int max_ctas, std::vector<std::vector<Item>> *out) {
   const int T = kStageTokens;
-  const double c0 = item_overhead_tokens();
-  // Every block boundary can cut one head, adding one item (and its overhead).
-  double total = c0 * (num_ctas - 1);
-  for (int bh = 0; bh < H; ++bh) total += p->n[bh] + c0;
-  const double per = std::max(total / num_ctas, c0 + T);
-  p->num_ctas = num_ctas;
-  p->cta_off.assign(1, 0);
-  int cta = 0;
+  int c = 0;
   double used = 0;
-  auto close_cta = [&]() {
-    p->cta_off.push_back((int32_t)p->items.size());
-    ++cta;
-  };
-  for (int bh = 0; bh < H; ++bh) {
+  if (out) out->assign(max_ctas, {});
+  for (int bh : heads) {
     const int n = p->n[bh];
     int pos = 0;
     while (pos < n) {
+      if (c >= max_ctas) return max_ctas + 1;
       const int rem = n - pos;
-      const double cap = (cta + 1) * per - used;
-      if (cta == num_ctas - 1 || cap >= rem + c0) {
-        p->items.push_back(Item{bh, pos, n, -1, -1, 0, 0, 0});
+      const double left = cap - used;
+      if (left >= rem + c0) {
+        if (out) (*out)[c].push_back(Item{bh, pos, n, -1, -1, 0, 0, 0});
         used += rem + c0;
         pos = n;
         continue;
       }
-      int k = (int)std::floor((cap - c0) / T) * T;
-      if (k >= T) {
-        if (rem - k < T) k = rem;  // never leave a sliver behind
-        p->items.push_back(Item{bh, pos, pos + k, -1, -1, 0, 0, 0});
-        used += k + c0;
+      int k = (int)std::floor((left - c0) / T) * T;
+      if (k >= T && rem - k >= T) {
+        if (out) (*out)[c].push_back(Item{bh, pos, pos + k, -1, -1, 0, 0, 0});
         pos += k;
-        if (pos < n) close_cta();
-      } else {
-        close_cta();
       }
+      ++c;  // the block is full
+      used = 0;
     }
   }
-  while ((int)p->cta_off.size() < num_ctas + 1)
+  return used > 0 ? c + 1 : c;
+}
+
+// Balanced: lay the heads' kept tokens end to end, charge each item its
+// tokens plus a fixed overhead, and cut the stream into at most num_ctas
+// blocks whose cost is at most a common cap, at stage boundaries; the cap is
+// the smallest (to a token) with which the stream fits.
+static void plan_balanced(kvx_plan *p, int num_ctas) {
+  const int H = p->shape.B * p->shape.Hkv;
+  const double c0 = item_overhead_tokens();
+  std::vector<int> heads(H);
+  double total = 0;
+  for (int bh = 0; bh < H; ++bh) {
+    heads[bh] = bh;
+    total += p->n[bh] + c0;
+  }
+  double lo = std::max(total / num_ctas, c0 + kStageTokens), hi = lo;
+  while (fill_blocks(p, heads, hi, c0, num_ctas, nullptr) > num_ctas) hi += c0 + kStageTokens;
+  while (hi - lo > 1.0) {
+    const double mid = 0.5 * (lo + hi);
+    if (fill_blocks(p, heads, mid, c0, num_ctas, nullptr) <= num_ctas)
+      hi = mid;
+    else
+      lo = mid;
+  }
+  std::vector<std::vector<Item>> cta;
+  fill_blocks(p, heads, hi, c0, num_ctas, &cta);
+  p->num_ctas = num_ctas;
+  p->cta_off.assign(1, 0);
+  for (int i = 0; i < num_ctas; ++i) {
+    for (const Item &it : cta[i]) p->items.push_back(it);
     p->cta_off.push_back((int32_t)p->items.size());
+  }
 }
 
 // One block per head, no split.
@@ -251,8 +270,9 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
         pg = std::max(pg, (p->n[(size_t)b * Hkv + h] + P - 1) / P);
       }
     if (policy == KVX_PLAN_BALANCED)
-      plan_balanced(p, num_ctas > 0 ? num_ctas
-                                    : sms * (resolved == KVX_KERNEL_MMA ? attn_mma_ctas_per_sm() : 1));
+      plan_balanced(p, num_ctas > 0
+                           ? num_ctas
+                           : sms * (resolved == KVX_KERNEL_MMA ? attn_mma_ctas_per_sm() : 1));
     else if (policy == KVX_PLAN_PER_HEAD)
       plan_per_head(p);
     else
