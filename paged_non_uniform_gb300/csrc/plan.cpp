@@ -69,8 +69,9 @@ static void finish_splits(kvx_plan *p) {
 }
 
 // Greedy fill of `heads` (in order) into blocks of cost at most `cap` each
-// (tokens + c0 per item), cutting at stage boundaries; returns the number of
-// blocks used, or max_ctas + 1 if they do not suffice (out is then partial).
+// (tokens + c0 per item; a head's last sliver under one stage may pass the
+// cap), cutting at stage boundaries; returns the number of blocks used, or
+// max_ctas + 1 if they do not suffice (out is then partial).
 static int fill_blocks(const kvx_plan *p, const std::vector<int> &heads, double cap, double c0,
                        int max_ctas, std::vector<std::vector<Item>> *out) {
   const int T = kStageTokens;
@@ -91,9 +92,14 @@ static int fill_blocks(const kvx_plan *p, const std::vector<int> &heads, double 
         continue;
       }
       int k = (int)std::floor((left - c0) / T) * T;
-      if (k >= T && rem - k >= T) {
+      if (k >= T) {
+        if (rem - k < T) k = rem;  // take a sliver along (the cap is passed by < T)
         if (out) (*out)[c].push_back(Item{bh, pos, pos + k, -1, -1, 0, 0, 0});
         pos += k;
+        if (pos == n) {
+          used += k + c0;
+          continue;
+        }
       }
       ++c;  // the block is full
       used = 0;

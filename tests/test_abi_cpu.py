@@ -214,3 +214,35 @@ def test_select_and_pack_reject_bad_arguments(kvx):
                                np.array([4, 4], np.int64).ctypes.data, p,
                                np.array([8, 8], np.int32).ctypes.data, 256, 256, None)
     assert rc == kvx.KVX_ESTATE
+
+
+@pytest.mark.parametrize("name", ["qwen3_4b", "llama3_sparse", "qwen25_32b"])
+@pytest.mark.parametrize("num_ctas", [152, 304, 1000])
+def test_balanced_plan_cap(kvx, name, num_ctas):
+    """Every block of the balanced plan costs (tokens + item charge per item)
+    at most one item charge plus two stages above the ideal share (stage
+    rounding and the no-sliver rule leave less than a stage each, and a block
+    may close one item short); pieces are
+    whole stages except a head's last piece; at most one head is cut at each
+    block boundary."""
+    cfg = synth.decode_config(name, seed=0, layers=1)
+    plan = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                               kvx.KVX_BF16, cfg.budget[0], cfg.seq_len, cfg.head_group[0],
+                               num_ctas)
+    st = plan.stats()
+    c0 = st["item_overhead"]
+    items, off = plan.items()
+    n = cfg.n[0].reshape(-1)
+    cost = [int((items[off[c]:off[c + 1], 2] - items[off[c]:off[c + 1], 1]).sum())
+            + c0 * int(off[c + 1] - off[c]) for c in range(num_ctas)]
+    # ideal share: tokens, an item charge per head, and one more per block
+    # boundary (where a head can be cut)
+    ideal = (int(n.sum()) + c0 * n.size + c0 * (num_ctas - 1)) / num_ctas
+    assert max(cost) <= ideal + c0 + 2 * 32 + 1, (max(cost), ideal)
+    for bh, b, e in items[:, :3]:
+        assert b % 32 == 0 and (e % 32 == 0 or e == n[bh]), (bh, b, e)
+    # a head cut across blocks: its pieces sit in consecutive blocks
+    cta_of = np.repeat(np.arange(num_ctas), np.diff(off))
+    for bh in np.unique(items[:, 0]):
+        ctas = np.sort(cta_of[items[:, 0] == bh])
+        assert np.all(np.diff(ctas) == 1), (bh, ctas)
