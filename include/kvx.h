@@ -1,6 +1,7 @@
 /*
  * kvx.h -- C ABI of the kvx library: decode-step attention over a paged KV
- * cache with non-uniform per-head budgets, and the coalesced KV gather.
+ * cache with non-uniform per-head budgets, the coalesced KV gather and the
+ * block pager behind it, and kept-set selection for sparse decode.
  *
  * Sources of the operations:
  *  - "Tangram: Unlocking Non-Uniform KV Cache for Efficient Multi-turn LLM
@@ -10,19 +11,24 @@
  *    Figs. 4(c), 5 and 13).
  *  - "KV-RM: Regularizing KV-Cache Movement for Static-Graph LLM Serving":
  *    descriptor merging of fragmented block mappings into a few large
- *    transfers that fill a fixed-shape staging buffer (Figs. 2 and 3).
+ *    transfers that fill a fixed-shape staging buffer (Figs. 2 and 3), and
+ *    mapping edits sealed by a Frame commit (Fig. 3).
+ *  - "KVDrive": decode over each head's top-K critical KV entries (Fig. 7,
+ *    Fig. 16).
  *
  * Conventions for every entry point:
  *  - Every function returns an int status: KVX_OK (0) or a negative code
  *    (kvx_status_string() names it). Nothing throws across the ABI.
  *  - The caller owns all device memory (inputs, outputs, workspaces) and all
- *    host arrays passed in. The library owns only the opaque plan (host
- *    arrays plus a device copy made by kvx_plan_upload), freed by
- *    kvx_plan_destroy.
+ *    host arrays passed in. The library owns only its opaque objects: the
+ *    plan (host arrays plus a device copy made by kvx_plan_upload, freed by
+ *    kvx_plan_destroy) and the frame (host view, two device descriptors and
+ *    record buffers, freed by kvx_frame_destroy).
  *  - Device calls are asynchronous on the stream passed as `void *stream`
  *    (a cudaStream_t; NULL = the legacy default stream). They never
- *    synchronise and never allocate device memory. Argument errors are
- *    found on the host, before anything is launched.
+ *    synchronise and never allocate device memory on the hot path (a frame
+ *    allocates its descriptors on first use). Argument errors are found on
+ *    the host, before anything is launched.
  *  - Errors found on the device (a page id outside its pool, a budget that
  *    disagrees with the plan, a block id outside the pool, a wait that ran
  *    out) set bits in a status word at the start of the caller's workspace
