@@ -218,13 +218,16 @@ __device__ __forceinline__ void consume_stage(
   }
 }
 
-template <int D>
+// VM: float4 groups of a head's g x D outputs that each consumer thread owns
+// in the split merge (one kernel per VM keeps a single merge inlined).
+template <int D, int VM>
 __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     attn_mma_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem =
-      (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  // 1024-byte alignment by pointer arithmetic on the shared array, so that
+  // every pointer derived from it stays in the shared state space
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   float *merge = (float *)(smem + kStages * C::kStage);
   uint64_t *bars = (uint64_t *)(merge + kMergeBufs * kCons * C::kMW);
   volatile int *abort_flag = (volatile int *)(bars + 2 * kStages);
@@ -476,22 +479,17 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       if (item.slot >= 0) {
         // Publish this piece; the block that finishes the head's last piece
         // merges all of them and rearms the counter for the next call. After
-        // the barrier, one thread's fence before the ticket releases every
-        // partial write of the block (the fence is cumulative over writes the
-        // barrier ordered before it), and the last block's fence after the
-        // ticket acquires the other blocks' partials for all its threads
-        // through the second barrier.
+        // the barrier, one thread's acquire-release ticket releases every
+        // partial write of the block (release is cumulative over the writes
+        // the barrier ordered before it), and in the last block it acquires
+        // the other blocks' partials for all its threads through the second
+        // barrier.
         consumer_sync(kCons * 32);
-        if (tid == 0) {
-          __threadfence();
-          const bool last =
-              atomicAdd(p.counters + item.split, 1) == p.split[item.split].count - 1;
-          if (last) __threadfence();
-          *last_flag = last;
-        }
+        if (tid == 0)
+          *last_flag = ticket_acq_rel(p.counters + item.split) == p.split[item.split].count - 1;
         consumer_sync(kCons * 32);
         if (*last_flag) {
-          merge_split<D, kCons * 32>(p, p.split[item.split], tid);
+          merge_split<D, kCons * 32, VM, 12>(p, p.split[item.split], tid);
           if (tid == 0) p.counters[item.split] = 0;
         }
       }
@@ -511,13 +509,13 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   }
 }
 
-template <int D>
-cudaError_t launch_d(const AttnParams &p, int num_ctas, cudaStream_t st) {
+template <int D, int VM>
+cudaError_t launch_dv(const AttnParams &p, int num_ctas, cudaStream_t st) {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, VM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<D>::kSmem);
     if (e != cudaSuccess) return e;
@@ -533,9 +531,23 @@ cudaError_t launch_d(const AttnParams &p, int num_ctas, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_mma_kernel<D>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, VM>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const AttnParams &p, int num_ctas, cudaStream_t st) {
+  constexpr int NT = kCons * 32;
+  static_assert(KVX_MAX_GQA * D / 4 <= 3 * NT, "split merge: at most three groups per thread");
+  const int n4 = p.g * D / 4;
+  constexpr int VMAX = (KVX_MAX_GQA * D / 4 + NT - 1) / NT;
+  if (n4 <= NT) return launch_dv<D, 1>(p, num_ctas, st);
+  if constexpr (VMAX >= 2) {
+    if (n4 <= 2 * NT) return launch_dv<D, 2>(p, num_ctas, st);
+  }
+  if constexpr (VMAX >= 3) return launch_dv<D, 3>(p, num_ctas, st);
+  return cudaErrorInvalidValue;  // unreachable: g <= KVX_MAX_GQA
 }
 
 }  // namespace

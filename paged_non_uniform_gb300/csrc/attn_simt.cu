@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(kWarps * 32)
       __syncthreads();
       if (last_flag) {
         __threadfence();
-        merge_split<D, kWarps * 32>(p, p.split[item.split], threadIdx.x);
+        constexpr int NT = kWarps * 32, VM = (KVX_MAX_GQA * D / 4 + NT - 1) / NT;
+        merge_split<D, NT, VM, 4>(p, p.split[item.split], threadIdx.x);
         if (threadIdx.x == 0) p.counters[item.split] = 0;
       }
     }

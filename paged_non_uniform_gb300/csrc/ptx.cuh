@@ -163,6 +163,17 @@ __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Ticket of a split head's piece: adds one to the counter and returns its
+// old value, in one acquire-release atomic at GPU scope. Release: the
+// piece's partial, written by the block's threads before a barrier that this
+// thread passed, is visible before the count is; acquire: the partials of the
+// pieces counted before are visible after it.
+__device__ __forceinline__ int ticket_acq_rel(int *counter) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }

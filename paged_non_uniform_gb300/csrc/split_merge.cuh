@@ -20,20 +20,17 @@
 
 namespace kvx {
 
-// Called by the NT merging threads of a block (tid in [0, NT)). Each thread
-// owns up to V float4 groups of the head's g x D outputs and keeps R = V *
-// BATCH (slot, group) loads in flight per L2 round trip: BATCH slots of each
-// of its V groups, or, when the outputs need only one group per thread,
-// R slots of that group. Partials are folded in slot order with a running
-// maximum.
-template <int D, int NT>
+// One merging thread of NT (tid in [0, NT)) owns the float4 groups q4 = tid,
+// tid + NT, ... (V of them) of the head's g x D outputs. It issues the loads
+// of S = PAIRS / V slots of every group it owns before folding any of them,
+// so that a head of up to S pieces costs one L2 round trip. Each group folds
+// its slots in slot order with a running maximum. The caller picks V so that
+// V * NT float4 groups cover g x D.
+template <int D, int NT, int V, int PAIRS>
 __device__ __forceinline__ void merge_split(const AttnParams &p, const SplitHead &sh, int tid) {
-  constexpr int V = (KVX_MAX_GQA * D / 4 + NT - 1) / NT;
-  constexpr int BATCH = V == 1 ? 4 : 2;
-  constexpr int R = V * BATCH;
+  static_assert(V >= 1 && V <= 3 && PAIRS >= V, "merge: one to three groups per thread");
+  constexpr int S = (PAIRS + V - 1) / V;  // slots per round trip
   const int g = p.g, cnt = sh.count, n4 = g * D / 4;
-  const bool one = n4 <= NT;      // one float4 group per thread
-  const int per = one ? R : BATCH;  // slots per round trip
   const int b = sh.bh / p.Hkv, h = sh.bh - b * p.Hkv;
   const float2 *ml = p.part_ml + (size_t)sh.slot_begin * g;
   const float4 *po = reinterpret_cast<const float4 *>(p.part_o + (size_t)sh.slot_begin * g * D);
@@ -45,33 +42,33 @@ __device__ __forceinline__ void merge_split(const AttnParams &p, const SplitHead
     L[k] = 0.f;
     O[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int s0 = 0; s0 < cnt; s0 += per) {
-    float2 mv[R];
-    float4 ov[R];
+  for (int s0 = 0; s0 < cnt; s0 += S) {
+    float2 mv[S][V];
+    float4 ov[S][V];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int k = one ? 0 : r % V, j = one ? r : r / V;
-      const int q4 = tid + k * NT;
-      if (s0 + j < cnt && q4 < n4) {
-        mv[r] = __ldcg(ml + (size_t)(s0 + j) * g + (4 * q4) / D);
-        ov[r] = __ldcg(po + (size_t)(s0 + j) * n4 + q4);
+    for (int j = 0; j < S; ++j) {
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int q4 = tid + k * NT;
+        if (s0 + j < cnt && q4 < n4) {
+          mv[j][k] = __ldcg(ml + (size_t)(s0 + j) * g + (4 * q4) / D);
+          ov[j][k] = __ldcg(po + (size_t)(s0 + j) * n4 + q4);
+        }
       }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
+    for (int j = 0; j < S; ++j) {
 #pragma unroll
       for (int k = 0; k < V; ++k) {
-        const bool mine = one ? (k == 0) : (r % V == k);
-        const int j = one ? r : r / V;
         const int q4 = tid + k * NT;
-        if (mine && s0 + j < cnt && q4 < n4) {
-          const float mn = fmaxf(M[k], mv[r].x);
-          const float a = ex2(M[k] - mn), f = ex2(mv[r].x - mn);
-          L[k] = L[k] * a + f * mv[r].y;
-          O[k].x = O[k].x * a + f * ov[r].x;
-          O[k].y = O[k].y * a + f * ov[r].y;
-          O[k].z = O[k].z * a + f * ov[r].z;
-          O[k].w = O[k].w * a + f * ov[r].w;
+        if (s0 + j < cnt && q4 < n4) {
+          const float mn = fmaxf(M[k], mv[j][k].x);
+          const float a = ex2(M[k] - mn), f = ex2(mv[j][k].x - mn);
+          L[k] = L[k] * a + f * mv[j][k].y;
+          O[k].x = O[k].x * a + f * ov[j][k].x;
+          O[k].y = O[k].y * a + f * ov[j][k].y;
+          O[k].z = O[k].z * a + f * ov[j][k].z;
+          O[k].w = O[k].w * a + f * ov[j][k].w;
           M[k] = mn;
         }
       }
