@@ -137,13 +137,14 @@ __global__ void __launch_bounds__(kWarps * 32)
       }
     }
     if (item.slot >= 0) {
-      __threadfence();
+      // publish the piece: the ticket after the barrier releases the block's
+      // partial writes and, in the block that counts last, acquires the
+      // other pieces' partials for all threads through the second barrier
       __syncthreads();
       if (threadIdx.x == 0)
-        last_flag = atomicAdd(p.counters + item.split, 1) == p.split[item.split].count - 1;
+        last_flag = ticket_acq_rel(p.counters + item.split) == p.split[item.split].count - 1;
       __syncthreads();
       if (last_flag) {
-        __threadfence();
         constexpr int NT = kWarps * 32, VM = (KVX_MAX_GQA * D / 4 + NT - 1) / NT;
         merge_split<D, NT, VM, 4>(p, p.split[item.split], threadIdx.x);
         if (threadIdx.x == 0) p.counters[item.split] = 0;

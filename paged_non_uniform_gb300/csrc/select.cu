@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
   __shared__ float Q[D];
   __shared__ int hist[2048];
   __shared__ float s_sc[kScoreTokensPerBlock];
+  pdl_launch_dependents();  // the bucket pass may launch; it waits for this grid
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, h = bh - b * p.Hkv;
   const int g = p.Hq / p.Hkv;
@@ -242,6 +243,8 @@ __global__ void __launch_bounds__(kBucketThreads, 2) select_bucket_kernel(const 
   __shared__ uint32_t s_digit;
   __shared__ int s_k, s_cnt, s_base;
   __shared__ int wsum[kBucketThreads / 32];
+  pdl_launch_dependents();
+  pdl_wait();  // scores and histograms of the score pass
   const int bh = blockIdx.y;
   const HeadSel hs = head_sel(p, bh);
   const int t_begin = blockIdx.x * kBucketSpan;
@@ -351,6 +354,7 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectP
   __shared__ int wsum[kTopkWarps];
   __shared__ uint32_t s_digit;
   __shared__ int s_k;
+  pdl_wait();  // bucket lists and bitmasks of the bucket pass
   const int bh = blockIdx.x;
   const HeadSel hs = head_sel(p, bh);
   const int L = hs.L, n = hs.n, ksel = hs.ksel;
@@ -659,10 +663,25 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
       configured[dev] = 1;
     }
   }
-  const dim3 bgrid((Lmax + kBucketSpan - 1) / kBucketSpan, B * Hkv);
-  select_bucket_kernel<<<bgrid, kBucketThreads, 0, st>>>(p);
-  select_topk_kernel<<<B * Hkv, kTopkThreads, topk_smem_bytes(Lmax), st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // The bucket and top-k passes are launched as programmatic dependents: each
+  // starts while the grid before it drains and waits on the device for it.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((Lmax + kBucketSpan - 1) / kBucketSpan, B * Hkv);
+  cfg.blockDim = dim3(kBucketThreads);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, select_bucket_kernel, p);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  cfg.gridDim = dim3(B * Hkv);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = topk_smem_bytes(Lmax);
+  e = cudaLaunchKernelEx(&cfg, select_topk_kernel, p);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);
   return KVX_OK;
 }
