@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
 }
 
 constexpr int kTopkWarps = kTopkThreads / 32;
+static_assert(2048 % kTopkThreads == 0, "top-k: the first-digit histogram splits evenly");
 constexpr int kBucketCap = 8192;       // (key, position) pairs kept per head
 constexpr int kBucketThreads = 512;
 constexpr int kBucketSpan = 32768;     // positions per bucket block
@@ -364,21 +365,62 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectP
   const float *sc = p.scores + (size_t)bh * p.ldsc;
   int32_t *out = p.kept_idx + (size_t)bh * p.stride;
   const bool take_all = ksel >= n;
-  const int cnt = hs.search ? min(p.bcnt[bh], kBucketCap + 1) : 0;
+  // The first chunk of every input (bucket size, above-cut bitmask words,
+  // bucket list, histogram) is loaded before any of it is stored, so that
+  // the loads share one L2 round trip; list entries past the bucket's size
+  // are read (inside the list's capacity) and dropped. Longer inputs finish
+  // in plain loops.
+  constexpr int CW = 4, CL = 4, CH = 2048 / kTopkThreads;
+  const uint32_t *ggt = p.bgt + (size_t)bh * p.wstride;
+  const uint2 *glist = p.blist + (size_t)bh * kBucketCap;
+  const int32_t *ghist = p.hist0 + (size_t)bh * 2048;
+  const int cnt_raw = hs.search ? __ldcg(p.bcnt + bh) : 0;
+  uint32_t wv[CW];
+  uint2 lv[CL];
+  int hv[CH];
+#pragma unroll
+  for (int j = 0; j < CW; ++j) {
+    const int w = tid + j * kTopkThreads;
+    wv[j] = hs.search && w < nwords ? __ldcg(ggt + w) : 0u;
+  }
+#pragma unroll
+  for (int j = 0; j < CL; ++j) {
+    const int i = tid + j * kTopkThreads;
+    lv[j] = hs.search && i < kBucketCap ? __ldcg(glist + i) : make_uint2(0u, 0u);
+  }
+#pragma unroll
+  for (int j = 0; j < CH; ++j) hv[j] = hs.search ? __ldcg(ghist + tid + j * kTopkThreads) : 0;
+  const int cnt = hs.search ? min(cnt_raw, kBucketCap + 1) : 0;
   const bool in_smem = cnt <= kBucketCap;
   // bitmasks: above-cut from the bucket pass (or all / none), at-cut empty
-  const uint32_t *ggt = p.bgt + (size_t)bh * p.wstride;
-  for (int w = tid; w < nwords; w += kTopkThreads) {
+  auto word0 = [&](int w, uint32_t loaded) {
     const int rem = n - 32 * w;
-    gtw[w] = hs.search ? (in_smem ? __ldcg(ggt + w) : 0u)
-                       : (take_all ? (rem >= 32 ? 0xffffffffu : (1u << rem) - 1u) : 0u);
+    return hs.search ? (in_smem ? loaded : 0u)
+                     : (take_all ? (rem >= 32 ? 0xffffffffu : (1u << rem) - 1u) : 0u);
+  };
+#pragma unroll
+  for (int j = 0; j < CW; ++j) {
+    const int w = tid + j * kTopkThreads;
+    if (w < nwords) {
+      gtw[w] = word0(w, wv[j]);
+      eqw[w] = 0u;
+    }
+  }
+  for (int w = tid + CW * kTopkThreads; w < nwords; w += kTopkThreads) {
+    gtw[w] = word0(w, hs.search && in_smem ? __ldcg(ggt + w) : 0u);
     eqw[w] = 0u;
   }
   if (hs.search) {
-    if (in_smem)
-      for (int i = tid; i < cnt; i += kTopkThreads)
-        list[i] = __ldcg(p.blist + (size_t)bh * kBucketCap + i);
-    for (int i = tid; i < 2048; i += kTopkThreads) hist[i] = p.hist0[(size_t)bh * 2048 + i];
+    if (in_smem) {
+#pragma unroll
+      for (int j = 0; j < CL; ++j) {
+        const int i = tid + j * kTopkThreads;
+        if (i < cnt) list[i] = lv[j];
+      }
+      for (int i = tid + CL * kTopkThreads; i < cnt; i += kTopkThreads) list[i] = __ldcg(glist + i);
+    }
+#pragma unroll
+    for (int j = 0; j < CH; ++j) hist[tid + j * kTopkThreads] = hv[j];
   }
   __syncthreads();
   uint32_t prefix = 0;
