@@ -153,6 +153,7 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 static_assert(2048 % kTopkThreads == 0, "top-k: the first-digit histogram splits evenly");
 constexpr int kBucketCap = 8192;       // (key, position) pairs kept per head
 constexpr int kBucketThreads = 512;
+static_assert(2048 % kBucketThreads == 0, "bucket: the first-digit histogram splits evenly");
 constexpr int kBucketSpan = 32768;     // positions per bucket block
 constexpr int kBucketUC = 4;           // float4 per thread in each of its sub-spans
 constexpr int kBlockBucketCap = 4096;  // bucket entries one bucket block stages in shared memory
@@ -266,7 +267,15 @@ __global__ void __launch_bounds__(kBucketThreads, 2) select_bucket_kernel(const 
     const int i4 = i0 + j * kBucketThreads + tid;
     v[j] = i4 < n4 ? __ldcg(sc4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  for (int i = tid; i < 2048; i += kBucketThreads) hist[i] = p.hist0[(size_t)bh * 2048 + i];
+  {
+    // the histogram's loads are all issued before the first store
+    constexpr int CH = 2048 / kBucketThreads;
+    int hv[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) hv[j] = __ldcg(p.hist0 + (size_t)bh * 2048 + tid + j * kBucketThreads);
+#pragma unroll
+    for (int j = 0; j < CH; ++j) hist[tid + j * kBucketThreads] = hv[j];
+  }
   if (tid == 0) s_cnt = 0;
   __syncthreads();
   find_digit_block<kBucketThreads>(hist, 2048, hs.ksel, &s_digit, &s_k, wsum);
