@@ -258,6 +258,11 @@ void kvx_plan_destroy(kvx_plan *plan);
  *   out               device fp32 [B][Hq][D].
  *   workspace         device, >= kvx_plan_workspace_bytes, 256-byte aligned.
  * Padding slots of partly filled pages are never read into the result.
+ * Launch: one kernel, as a programmatic dependent of the kernel before it on
+ * the stream. It may start while that kernel drains. It reads no input but
+ * the plan's device copy until that kernel has completed, except that a plan
+ * of short blocks prefetches its first K/V pages into L2, which changes no
+ * data.
  * Errors: KVX_EINVAL, KVX_ERANGE, KVX_ESTATE, KVX_ECUDA (nothing launched on
  * argument errors).
  * ------------------------------------------------------------------------- */
@@ -447,6 +452,10 @@ int kvx_frame_get_stats(const kvx_frame *frame, kvx_frame_stats *out);
  *               list of up to 8192 candidates near the cut and a bitmask).
  * The cut is decided on fp32 scores: positions whose scores lie within fp32
  * rounding of the cut may be exchanged with respect to an exact selection.
+ * Launch: a memset of the workspace's counters, the score pass, then the
+ * bucket and top-k passes. The last two are programmatic dependents of the
+ * pass before them, which they wait for on the device before reading its
+ * results.
  * ------------------------------------------------------------------------- */
 int kvx_select_workspace_bytes(int32_t B, int32_t Hkv, int32_t Lmax, size_t *bytes);
 
