@@ -193,6 +193,45 @@ def test_selection_bucket_overflow_and_ragged():
                        kept[bh, :cnt[bh]])
 
 
+def test_selection_longest_rows():
+    """Rows at the library's maximum length (262144) and just past 131072:
+    a head's above-cut bitmask then has more words than the top-k kernel
+    loads in its first chunk, so the remainder of the bitmask is read in
+    the kernel's second loop."""
+    g = synth.rng(9)
+    L = np.array([262144, 131200], np.int32)
+    q = synth.normal(g, (2, 4, 128), "bf16")
+    k = synth.normal(g, (2, 1, int(L.max()), 128), "bf16")
+    top, recent = 2048, 128
+    kept, cnt = gpu_select(q, k, L, top, recent)
+    orc = oracle.load()
+    for b in range(2):
+        assert cnt[b] == top + recent
+        check_head(orc, q[b], k[b, 0, :L[b]], top, recent, kept[b, :cnt[b]])
+
+
+def test_selection_cut_bucket_beyond_first_chunk():
+    """Every candidate score lies in one first-digit bucket, with more
+    entries (6436) than the top-k kernel loads in its first chunk (4096)
+    but fewer than the list holds (8192), so the rest of the list is read in
+    the kernel's second loop. The scores 4 (1 + m/128) are exact in fp32 and
+    fp64, so the kept set is unique: the top 2048 with ties at the lower
+    position, then the recent window."""
+    B, Hq, Hkv, D, L = 1, 8, 2, 128, 6500
+    top, recent = 2048, 64
+    g = synth.rng(12)
+    q = np.zeros((B, Hq, D), np.float32)
+    q[:, :, 0] = 1.0
+    k = np.zeros((B, Hkv, L, D), np.float32)
+    k[..., 0] = 1.0 + g.integers(0, 26, size=(B, Hkv, L)) / 128.0
+    kept, cnt = gpu_select(q, k, np.array([L], np.int32), top, recent)
+    orc = oracle.load()
+    for h in range(Hkv):
+        ref = orc.select_topk(q[0, 4 * h:4 * h + 4], k[0, h], top, recent)
+        assert cnt[h] == ref.size == top + recent
+        assert np.array_equal(kept[h, :cnt[h]], ref)
+
+
 def test_selection_bad_length_flagged():
     """A length above Lmax selects nothing for its sequence and sets the
     status bit; the other sequences are unaffected."""
