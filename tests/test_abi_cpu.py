@@ -246,3 +246,52 @@ def test_balanced_plan_cap(kvx, name, num_ctas):
     for bh in np.unique(items[:, 0]):
         ctas = np.sort(cta_of[items[:, 0] == bh])
         assert np.all(np.diff(ctas) == 1), (bh, ctas)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_balanced_plan_random_shapes(kvx, orc, seed):
+    """Seeded random shapes, budgets, groupings and block counts, down to
+    heads shorter than a stage and more blocks than stages. The balanced plan
+    covers every kept token once (oracle count array) and resolves budgets as
+    the oracle does. Pieces are whole stages except a head's last. A cut
+    head's pieces sit in consecutive blocks and run before the block's whole
+    heads. No block costs more than one item charge plus two stages above
+    the ideal share. Every piece of a cut head holds at least one stage.
+    """
+    g = np.random.default_rng(1000 + seed)
+    Hkv = int(g.choice([1, 2, 3, 4, 8]))
+    gqa = int(g.choice([1, 2, 4, 8]))
+    B = int(g.integers(1, 7))
+    P = int(g.choice([8, 16, 32, 64, 128]))
+    L = g.integers(1, 6001, size=B).astype(np.int32)
+    budget = g.integers(1, 8001, size=(B, Hkv)).astype(np.int32)
+    G = int(g.integers(1, min(Hkv, 4) + 1))
+    hg = np.concatenate([np.arange(G), g.integers(0, G, size=Hkv - G)]).astype(np.int32)
+    g.shuffle(hg)
+    num_ctas = int(g.choice([1, 2, 3, 7, 50, 152, 304, 900]))
+    plan = kvx.kvx_plan_create(B, gqa * Hkv, Hkv, 128, P, G, kvx.KVX_BF16, budget, L, hg,
+                               num_ctas)
+    n = orc.resolve_budget(budget, L).reshape(-1)
+    assert np.array_equal(plan.kept().reshape(-1), n)
+    items, off = plan.items()
+    assert len(off) == num_ctas + 1 and off[0] == 0 and off[-1] == len(items)
+    bad, _ = orc.plan_coverage(n, items)
+    assert bad == 0
+    T, c0 = 32, plan.stats()["item_overhead"]
+    for bh, b, e in items[:, :3]:
+        assert b % T == 0 and (e % T == 0 or e == n[bh]), (bh, b, e)
+    pieces = np.bincount(items[:, 0], minlength=n.size)
+    cta_of = np.repeat(np.arange(num_ctas), np.diff(off))
+    for bh in np.flatnonzero(pieces > 1):
+        mine = items[:, 0] == bh
+        assert np.all(np.diff(np.sort(cta_of[mine])) == 1), bh
+        # no sliver: every piece of a cut head holds at least one stage
+        assert np.all(items[mine, 2] - items[mine, 1] >= T), (bh, items[mine])
+    cost = []
+    for c in range(num_ctas):
+        blk = items[off[c]:off[c + 1]]
+        split = pieces[blk[:, 0]] > 1
+        assert not np.any(split[1:] & ~split[:-1]), (c, blk)  # split pieces first
+        cost.append(int((blk[:, 2] - blk[:, 1]).sum()) + c0 * len(blk))
+    ideal = (int(n.sum()) + c0 * n.size + c0 * (num_ctas - 1)) / num_ctas
+    assert max(cost) <= ideal + c0 + 2 * T + 1, (max(cost), ideal)
