@@ -206,6 +206,26 @@ int kvx_plan_items(const kvx_plan *plan, int32_t *items, int32_t *cta_off);
 /* Per-block token loads, int64 [num_ctas] (host). */
 int kvx_plan_cta_tokens(const kvx_plan *plan, int64_t *tokens);
 
+/* Token coverage of the plan (host only). The ahead-of-time split must read
+ * every kept token of every head exactly once (Tangram, AOT Load Balancing,
+ * Fig. 13: the static plan cuts each head's kept tokens across thread blocks;
+ * the cut changes where tokens are read, never which). Fills
+ *     count int32 [B*Hkv][max_n],  max_n = max(1, max over heads of n[b][h]),
+ *     count[bh*max_n + t] = number of work items containing token t of head bh,
+ * so a correct plan gives 1 for t < n[bh] and 0 from n[bh] on.
+ * Errors: KVX_EINVAL (null argument). */
+int kvx_plan_coverage(const kvx_plan *plan, int32_t *count);
+
+/* Device coverage record (test hook; no effect unless set). dev_count is a
+ * device buffer of int32 [B*Hkv][stride], stride >= max_n above, zeroed by
+ * the caller. Every subsequent kvx_decode_attn with this plan adds 1 to
+ * dev_count[bh*stride + t] for each kept token t of head bh at the point
+ * where a consumer warp feeds it to the softmax (after its K/V data has
+ * arrived; counted from what the kernel consumed, not from the plan). A
+ * correct launch leaves exactly kvx_plan_coverage's array. NULL turns the
+ * record off. Errors: KVX_EINVAL, KVX_ERANGE (stride too small). */
+int kvx_plan_set_coverage_record(kvx_plan *plan, int32_t *dev_count, int32_t stride);
+
 /* Optional per-block timing trace: dev_trace is a device buffer of int64
  * [num_ctas][4] = {SM id, start ns, end ns, tokens}, written by every
  * subsequent kvx_decode_attn with this plan; NULL turns it off. */
@@ -242,7 +262,7 @@ void kvx_plan_destroy(kvx_plan *plan);
  * the token-major layout (same for V).
  *
  *   plan              an uploaded plan built for these shapes and budgets.
- *   q                 [B][Hq][D] of the plan's dtype (device).
+ *   q                 [B][Hq][D] of the plan's dtype (device), 16-byte aligned.
  *   k_pools, v_pools  host arrays [num_groups] of device pointers, each a
  *                     pool of pool_pages[G] pages, [|G|][P][D] (head-major)
  *                     or [P][|G|][D] (token-major) of the plan's dtype,
@@ -505,8 +525,12 @@ int kvx_pack_kept(const kvx_plan *plan, const void *keys, const void *values,
  *    errors (KVX_DEV_BAD_BLOCK, KVX_DEV_BAD_LENGTH) are OR-ed; the caller
  *    zeroes it. With NULL they are not reported.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    (cudaGetSymbolAddress) with that device current, and a call looks it
+ *    up again when the device's CUDA context has changed since (after
+ *    cudaDeviceReset, the array may sit elsewhere in the new context). Make
+ *    that first call before any stream capture. A call with S = 0 does only
+ *    this set-up (plus the header clear below) and copies nothing: use it to
+ *    prepare a device ahead of time.
  *  - Every call shares the one array and clears its header on `stream` first;
  *    calls whose work overlaps on the GPU (different streams, different
  *    threads) race on it and must be ordered by the caller.

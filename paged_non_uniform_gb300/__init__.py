@@ -6,7 +6,6 @@ coalesced KV gather, as a C-ABI library (libkvx.so) with a thin binding.
     kvx.kvx_decode_attn(plan, q, k_pools, v_pools, ...)
     kvx.kvx_gather_coalesce(block_table, num_blocks, ...)
 
-`pages` holds host helpers that lay out head-group page tables and pools.
 Importing `kvx` raises ImportError if the library is not built; nothing falls
 back to another implementation.
 """

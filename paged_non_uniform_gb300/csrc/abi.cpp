@@ -113,7 +113,7 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   if (workspace_bytes < need || !aligned(workspace, 256)) return KVX_EINVAL;
   if (!std::isfinite(scale) || scale < 0.f) return KVX_EINVAL;
   const size_t es = s.dtype == KVX_BF16 ? 2 : 4;
-  if (!aligned(q, 4) || !aligned(out, 16)) return KVX_EINVAL;
+  if (!aligned(q, 16) || !aligned(out, 16)) return KVX_EINVAL;
 
   AttnParams p;
   std::memset(&p, 0, sizeof(p));
@@ -162,6 +162,8 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   p.part_ml = (float2 *)(ws + lay.part_ml);
   p.part_o = (float *)(ws + lay.part_o);
   p.trace = plan->d_trace;
+  p.cover = plan->d_cover;
+  p.cover_stride = plan->cover_stride;
   p.B = B;
   p.Hq = s.Hq;
   p.Hkv = s.Hkv;

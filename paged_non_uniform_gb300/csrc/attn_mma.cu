@@ -425,9 +425,14 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
           dead = true;
           continue;
         }
-        const int valid = min(kStageTokens, item.end - (item.begin + st * kStageTokens));
+        const int t0 = item.begin + st * kStageTokens;
+        const int valid = min(kStageTokens, item.end - t0);
         const uint32_t kb = stage0 + slot * C::kStage;
         consume_stage<D>(kb, kb + C::kTile, la, valid, qf, o, m0, m1, l0, l1, sl2, lane);
+        // Coverage record (test hook): one count per token this warp has
+        // just fed to the softmax, taken here rather than from the plan.
+        if (p.cover && lane < valid)
+          atomicAdd(p.cover + (size_t)item.bh * p.cover_stride + t0 + lane, 1);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * slot);
       }

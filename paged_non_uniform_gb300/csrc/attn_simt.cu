@@ -3,13 +3,16 @@
 //
 // Same work items, partial format and output as the tensor-core kernel
 // ("Tangram: Unlocking Non-Uniform KV Cache for Efficient Multi-turn LLM
-// Serving", Fig. 8(b) page addressing, Fig. 13 ahead-of-time split): four
-// warps per block; warp w takes tokens begin+w, begin+w+4, ... of an item;
-// the 32 lanes of a warp split the head dimension, reduce the g dot products
-// with shuffles and run the online softmax per query head. The warps' states
-// are merged in shared memory at the end of each item; split heads are merged
-// by the block that finishes their last piece. Page ids outside the
-// pool read as zero rows and set KVX_DEV_BAD_PAGE.
+// Serving", Fig. 8(b) page addressing, Fig. 13 ahead-of-time split). Four
+// warps per block. A token row of K (or V) is read with 16-byte vector loads:
+// LPT = D * sizeof(T) / 16 lanes cover one row, so one warp step covers
+// TPW = 32 / LPT tokens (lane group j of warp w takes tokens
+// begin + w*TPW + j, then every kWarps*TPW further). Each lane group reduces
+// its g dot products with shuffles inside the group and keeps its own online
+// softmax state; the groups of a warp are merged by shuffles, the warps in
+// shared memory at the end of each item, and split heads by the block that
+// finishes their last piece. Page ids outside the pool read as zero rows and
+// set KVX_DEV_BAD_PAGE.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -22,25 +25,52 @@ namespace {
 
 constexpr int kWarps = 4;
 
+// Sixteen bytes of a row (one vector load) as EPL floats.
 template <typename T>
-__device__ __forceinline__ float to_f(T x);
+struct Vec16;
 template <>
-__device__ __forceinline__ float to_f<float>(float x) {
-  return x;
-}
+struct Vec16<float> {
+  static constexpr int kN = 4;
+  __device__ __forceinline__ static void load(const float *src, float (&f)[4]) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+    f[0] = v.x;
+    f[1] = v.y;
+    f[2] = v.z;
+    f[3] = v.w;
+  }
+};
 template <>
-__device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
-  return __bfloat162float(x);
+struct Vec16<__nv_bfloat16> {
+  static constexpr int kN = 8;
+  __device__ __forceinline__ static void load(const __nv_bfloat16 *src, float (&f)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+// Scale of a state with maximum m when the merged maximum is M (a state that
+// has seen no token has m = -inf and contributes nothing).
+__device__ __forceinline__ float rescale(float m, float M) {
+  return m == -INFINITY ? 0.f : ex2(m - M);
 }
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
     attn_simt_kernel(const __grid_constant__ AttnParams p) {
-  constexpr int DL = D / 32;
-  constexpr int MW = 8 * D + 16;  // floats per warp record
+  constexpr int EPL = Vec16<T>::kN;  // elements per lane per 16-byte load
+  constexpr int LPT = D / EPL;       // lanes per token row
+  constexpr int TPW = 32 / LPT;      // tokens per warp step
+  static_assert(LPT >= 1 && LPT <= 32 && 32 % LPT == 0, "a row must tile the warp");
+  constexpr int MW = 8 * D + 16;     // floats per warp record
   __shared__ float merge[2][kWarps][MW];
   __shared__ int last_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / LPT, gl = lane % LPT;  // token of the step, lane within the row
   const int it0 = p.cta_off[blockIdx.x], it1 = p.cta_off[blockIdx.x + 1];
   const int g = p.g, P = p.P;
   uint64_t t_start = p.trace ? globaltimer_ns() : 0;
@@ -58,62 +88,87 @@ __global__ void __launch_bounds__(kWarps * 32)
       const int L = __ldg(p.seq_len + b), bud = __ldg(p.head_budget + item.bh);
       if (min(L, bud) != __ldg(p.n_plan + item.bh)) atomicOr(p.status, KVX_DEV_BAD_BUDGET);
     }
-    float qv[KVX_MAX_GQA][DL], o[KVX_MAX_GQA][DL], m[KVX_MAX_GQA], l[KVX_MAX_GQA];
-    const T *qb = (const T *)p.q + ((size_t)b * p.Hq + (size_t)h * g) * D;
+    float qv[KVX_MAX_GQA][EPL], o[KVX_MAX_GQA][EPL], m[KVX_MAX_GQA], l[KVX_MAX_GQA];
+    const T *qb = (const T *)p.q + ((size_t)b * p.Hq + (size_t)h * g) * D + gl * EPL;
 #pragma unroll
     for (int j = 0; j < KVX_MAX_GQA; ++j) {
       m[j] = -INFINITY;
       l[j] = 0.f;
 #pragma unroll
-      for (int i = 0; i < DL; ++i) {
-        qv[j][i] = j < g ? to_f(qb[(size_t)j * D + lane + 32 * i]) : 0.f;
-        o[j][i] = 0.f;
-      }
+      for (int e = 0; e < EPL; ++e) o[j][e] = qv[j][e] = 0.f;
+      if (j < g) Vec16<T>::load(qb + (size_t)j * D, qv[j]);
     }
-    for (int t = item.begin + warp; t < item.end; t += kWarps) {
-      const int32_t page = __ldg(pt + t / P);
-      float kv[DL], vv[DL];
-      if (page < 0 || (int64_t)page >= gd.num_pages) {
-        if (lane == 0) atomicOr(p.status, KVX_DEV_BAD_PAGE);
+    for (int t0 = item.begin + warp * TPW; t0 < item.end; t0 += kWarps * TPW) {
+      const int t = t0 + grp;
+      const bool active = t < item.end;
+      float kv[EPL], vv[EPL];
 #pragma unroll
-        for (int i = 0; i < DL; ++i) kv[i] = vv[i] = 0.f;
-      } else {
-        const size_t rr = p.layout == KVX_LAYOUT_HEAD_MAJOR
-                              ? ((size_t)page * gd.size + row) * P + (t & (P - 1))
-                              : ((size_t)page * P + (t & (P - 1))) * gd.size + row;
-#pragma unroll
-        for (int i = 0; i < DL; ++i) {
-          kv[i] = to_f(kp[rr * D + lane + 32 * i]);
-          vv[i] = to_f(vp[rr * D + lane + 32 * i]);
+      for (int e = 0; e < EPL; ++e) kv[e] = vv[e] = 0.f;
+      if (active) {
+        const int32_t page = __ldg(pt + t / P);
+        if (page < 0 || (int64_t)page >= gd.num_pages) {
+          if (gl == 0) atomicOr(p.status, KVX_DEV_BAD_PAGE);
+        } else {
+          const size_t rr = p.layout == KVX_LAYOUT_HEAD_MAJOR
+                                ? ((size_t)page * gd.size + row) * P + (t & (P - 1))
+                                : ((size_t)page * P + (t & (P - 1))) * gd.size + row;
+          Vec16<T>::load(kp + rr * D + gl * EPL, kv);
+          Vec16<T>::load(vp + rr * D + gl * EPL, vv);
         }
+        // Coverage record (test hook): one count per token fed to the softmax.
+        if (p.cover && gl == 0) atomicAdd(p.cover + (size_t)item.bh * p.cover_stride + t, 1);
       }
 #pragma unroll
       for (int j = 0; j < KVX_MAX_GQA; ++j) {
         if (j >= g) break;
         float dot = 0.f;
 #pragma unroll
-        for (int i = 0; i < DL; ++i) dot = fmaf(qv[j][i], kv[i], dot);
+        for (int e = 0; e < EPL; ++e) dot = fmaf(qv[j][e], kv[e], dot);
 #pragma unroll
-        for (int sh = 16; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
-        const float x = dot * p.scale_log2;
-        const float mn = fmaxf(m[j], x);
-        const float al = ex2(m[j] - mn), pw = ex2(x - mn);
-        l[j] = l[j] * al + pw;
+        for (int sh = LPT / 2; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+        if (active) {
+          const float x = dot * p.scale_log2;
+          const float mn = fmaxf(m[j], x);
+          const float al = ex2(m[j] - mn), pw = ex2(x - mn);
+          l[j] = l[j] * al + pw;
 #pragma unroll
-        for (int i = 0; i < DL; ++i) o[j][i] = fmaf(o[j][i], al, pw * vv[i]);
-        m[j] = mn;
+          for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(o[j][e], al, pw * vv[e]);
+          m[j] = mn;
+        }
+      }
+    }
+    // merge the lane groups of this warp (lanes gl of every group hold the
+    // same dimensions)
+#pragma unroll
+    for (int sh = LPT; sh < 32; sh <<= 1) {
+#pragma unroll
+      for (int j = 0; j < KVX_MAX_GQA; ++j) {
+        if (j >= g) break;
+        const float mo = __shfl_xor_sync(0xffffffffu, m[j], sh);
+        const float lo = __shfl_xor_sync(0xffffffffu, l[j], sh);
+        const float M = fmaxf(m[j], mo);
+        const float a = rescale(m[j], M), c = rescale(mo, M);
+        l[j] = l[j] * a + lo * c;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+          const float oo = __shfl_xor_sync(0xffffffffu, o[j][e], sh);
+          o[j][e] = o[j][e] * a + oo * c;
+        }
+        m[j] = M;
       }
     }
     float *buf = &merge[(it - it0) & 1][0][0];
     float *mw = buf + warp * MW;
+    if (grp == 0) {
 #pragma unroll
-    for (int j = 0; j < KVX_MAX_GQA; ++j) {
-      if (j >= g) break;
+      for (int j = 0; j < KVX_MAX_GQA; ++j) {
+        if (j >= g) break;
 #pragma unroll
-      for (int i = 0; i < DL; ++i) mw[j * D + lane + 32 * i] = o[j][i];
-      if (lane == 0) {
-        mw[8 * D + j] = m[j];
-        mw[8 * D + 8 + j] = l[j];
+        for (int e = 0; e < EPL; ++e) mw[j * D + gl * EPL + e] = o[j][e];
+        if (lane == 0) {
+          mw[8 * D + j] = m[j];
+          mw[8 * D + 8 + j] = l[j];
+        }
       }
     }
     __syncthreads();
@@ -125,7 +180,7 @@ __global__ void __launch_bounds__(kWarps * 32)
       float Ls = 0.f, O = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float f = ex2(buf[w * MW + 8 * D + qi] - M);
+        const float f = rescale(buf[w * MW + 8 * D + qi], M);
         Ls += f * buf[w * MW + 8 * D + 8 + qi];
         O += f * buf[w * MW + qi * D + d];
       }

@@ -73,6 +73,8 @@ struct alignas(128) AttnParams {
   float2 *part_ml;             // [slots][g] = (max in log2 units, sum)
   uint32_t *status;
   int64_t *trace;
+  int32_t *cover;              // coverage record [B*Hkv][cover_stride], or null
+  int32_t cover_stride;
   int32_t B, Hq, Hkv, D, g, P, num_groups, layout;
   float scale_log2;            // scale * log2(e)
   int32_t stall_block;         // failure-detection test: block whose first stage gets no loads (-1: none)
@@ -146,6 +148,8 @@ struct kvx_plan {
   int32_t *d_n;
   kvx::SplitHead *d_split;
   int64_t *d_trace;
+  int32_t *d_cover;     // kvx_plan_set_coverage_record
+  int32_t cover_stride;
   int32_t stall_block;  // kvx_plan_inject_stall
   uint64_t wait_ns;
   int32_t pf_tokens;    // tokens per block warmed into L2 before the dependency wait

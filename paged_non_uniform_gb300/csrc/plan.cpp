@@ -250,6 +250,8 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
     p->d_n = nullptr;
     p->d_split = nullptr;
     p->d_trace = nullptr;
+    p->d_cover = nullptr;
+    p->cover_stride = 0;
     p->stall_block = -1;
     p->wait_ns = 2000000000ull;
     p->pf_tokens = 0;
@@ -425,6 +427,33 @@ extern "C" int kvx_plan_cta_tokens(const kvx_plan *p, int64_t *tokens) {
 extern "C" int kvx_plan_set_trace(kvx_plan *p, int64_t *dev_trace) {
   if (!p) return KVX_EINVAL;
   p->d_trace = dev_trace;
+  return KVX_OK;
+}
+
+static int32_t plan_max_n(const kvx_plan *p) {
+  int32_t mx = 1;
+  for (int32_t v : p->n) mx = std::max(mx, v);
+  return mx;
+}
+
+extern "C" int kvx_plan_coverage(const kvx_plan *p, int32_t *count) {
+  if (!p || !count) return KVX_EINVAL;
+  const int32_t mx = plan_max_n(p);
+  std::memset(count, 0, sizeof(int32_t) * p->n.size() * (size_t)mx);
+  for (const Item &it : p->items) {
+    if (it.bh < 0 || (size_t)it.bh >= p->n.size() || it.begin < 0 || it.end > mx)
+      return KVX_ERANGE;  // not reachable for a plan built by kvx_plan_create
+    int32_t *row = count + (size_t)it.bh * mx;
+    for (int32_t t = it.begin; t < it.end; ++t) row[t] += 1;
+  }
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_set_coverage_record(kvx_plan *p, int32_t *dev_count, int32_t stride) {
+  if (!p) return KVX_EINVAL;
+  if (dev_count && stride < plan_max_n(p)) return KVX_ERANGE;
+  p->d_cover = dev_count;
+  p->cover_stride = dev_count ? stride : 0;
   return KVX_OK;
 }
 

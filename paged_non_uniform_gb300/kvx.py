@@ -95,6 +95,8 @@ lib.kvx_plan_group_pages.argtypes = [_vp, _vp]
 lib.kvx_plan_items.argtypes = [_vp, _vp, _vp]
 lib.kvx_plan_cta_tokens.argtypes = [_vp, _vp]
 lib.kvx_plan_set_trace.argtypes = [_vp, _vp]
+lib.kvx_plan_coverage.argtypes = [_vp, _vp]
+lib.kvx_plan_set_coverage_record.argtypes = [_vp, _vp, _c.c_int32]
 lib.kvx_plan_inject_stall.argtypes = [_vp, _c.c_int32, _c.c_uint64]
 lib.kvx_plan_destroy.argtypes = [_vp]
 lib.kvx_plan_destroy.restype = None
@@ -229,6 +231,18 @@ class Plan:
 
     def set_trace(self, dev_trace) -> None:
         _check(lib.kvx_plan_set_trace(self.handle, _dptr(dev_trace)), "kvx_plan_set_trace")
+
+    def coverage(self) -> np.ndarray:
+        """kvx_plan_coverage: int32 [B*Hkv][max_n] count of items per token."""
+        mx = max(1, int(self.kept().max()))
+        c = np.zeros((self.shape.B * self.shape.Hkv, mx), dtype=np.int32)
+        _check(lib.kvx_plan_coverage(self.handle, c.ctypes.data), "kvx_plan_coverage")
+        return c
+
+    def set_coverage_record(self, dev_count, stride: int = 0) -> None:
+        """kvx_plan_set_coverage_record (None turns it off)."""
+        _check(lib.kvx_plan_set_coverage_record(self.handle, _dptr(dev_count), int(stride)),
+               "kvx_plan_set_coverage_record")
 
     def inject_stall(self, block: int, wait_limit_ns: int) -> None:
         """Failure-detection test hook: see kvx_plan_inject_stall."""

@@ -234,7 +234,18 @@ def decode_config(name: str, seed: int = 0, layers: int | None = None,
     llama3_sparse 32 layers, 32/8 heads, D 128, bf16, batch 8, L = 122000,
                   every head keeps 2176 tokens (top 2048 by score + 128 recent);
                   one group; page 16.
+    tiny          1 layer, 4/2 heads, D 64, fp32, batch 2, L {37, 100}; KV head 0
+                  keeps everything, KV head 1 keeps 20 tokens (4 sink + 16
+                  recent); groups {h0}, {h1}; page 16 (the shapes of tiny()).
     """
+    if name == "tiny":
+        L = np.array([37, 100], dtype=np.int32)
+        n = np.array([[[37, 20], [100, 20]]], dtype=np.int32)
+        budget = np.array([[[FULL, 20], [FULL, 20]]], dtype=np.int32)
+        hg = np.array([[0, 1]], dtype=np.int32)
+        if layers and layers > 1:
+            n, budget, hg = (np.repeat(a, layers, axis=0) for a in (n, budget, hg))
+        return DecodeConfig("tiny", layers or 1, 2, 4, 2, 64, 16, "f32", L, n, budget, hg, 2)
     g = rng(seed)
     if name in ("qwen3_4b", "qwen3_4b_32k"):
         nl, B, Hq, Hkv, D, P = 36, 16, 32, 8, 128, 16
@@ -371,16 +382,3 @@ def block_stamp_pool(num_phys: int, block_bytes: int, seed: int = 0) -> np.ndarr
     ids = np.arange(num_phys, dtype=np.int64).view(np.uint8).reshape(num_phys, 8)
     pool[:, :8] = ids
     return pool
-
-
-def select_top_recent(q_heads: np.ndarray, k: np.ndarray, top: int = 2048,
-                      recent: int = 128) -> np.ndarray:
-    """Kept set of one KV head for the sparse long-context workload: the last
-    `recent` positions plus the `top` positions of [0, L - recent) with the
-    largest score sum_j <q_j, k_t> over the head's query heads (float64; ties
-    go to the lower position). Returns ascending positions."""
-    L = k.shape[0]
-    cut = max(0, L - recent)
-    score = k[:cut].astype(np.float64) @ q_heads.astype(np.float64).sum(0)
-    order = np.lexsort((np.arange(cut), -score))[:min(top, cut)]
-    return np.sort(np.concatenate([order, np.arange(cut, L)])).astype(np.int32)

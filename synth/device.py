@@ -19,6 +19,7 @@ class ValueTable:
     def __init__(self, seed: int, rows: int, D: int, dtype: str = "bf16", device="cuda"):
         self.rows, self.D, self.dtype = rows, D, dtype
         vals = synth.value_table(seed, rows * D, dtype)
+        self.host_raw = vals.reshape(rows, D)  # bf16 bit patterns (uint16) or float32
         if dtype == "bf16":
             self.host = synth.bf16_bits_to_f32(vals).reshape(rows, D)
             t = torch.from_numpy(vals.view(np.int16)).view(torch.bfloat16)
@@ -42,6 +43,10 @@ class ValueTable:
     def host_rows(self, shift: int, row_ids: np.ndarray) -> np.ndarray:
         """float32 values of pool rows `row_ids` of a pool filled with `shift`."""
         return self.host[(shift + np.asarray(row_ids, dtype=np.int64)) % self.rows]
+
+    def host_raw_rows(self, shift: int, row_ids: np.ndarray) -> np.ndarray:
+        """Stored element patterns (uint16 for bf16) of pool rows `row_ids`."""
+        return self.host_raw[(shift + np.asarray(row_ids, dtype=np.int64)) % self.rows]
 
 
 def torch_dtype(dtype: str):

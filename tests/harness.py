@@ -13,7 +13,8 @@ import torch
 
 import oracle
 import synth
-from paged_non_uniform_gb300 import kvx, pages
+from paged_non_uniform_gb300 import kvx
+import pages
 
 
 def num_groups(case) -> int:
@@ -86,3 +87,34 @@ def oracle_out(case, scale=None) -> np.ndarray:
 
 def max_abs(a, b) -> float:
     return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+
+
+def oracle_layer(orc, cfg, lay, max_rows=1 << 19) -> np.ndarray:
+    """The oracle's output for every (sequence, query head) of one layer held
+    by a synth.device.TableLayer: each head's kept K/V rows are rebuilt on
+    the host from the value table, compacted to positions 0..n-1, and the
+    oracle runs over groups of sequences (at most max_rows rows per tensor
+    per call, so that its OpenMP loop spans many heads)."""
+    B, Hq, Hkv, D = cfg.B, cfg.Hq, cfg.Hkv, cfg.D
+    n = cfg.n[lay.layer]
+    out = np.zeros((B, Hq, D))
+    scale = 1.0 / math.sqrt(D)
+    b0 = 0
+    while b0 < B:
+        b1 = b0 + 1
+        while b1 < B and (b1 + 1 - b0) * Hkv * int(n[b0:b1 + 1].max()) <= max_rows:
+            b1 += 1
+        nmax = int(n[b0:b1].max())
+        k = np.zeros((b1 - b0, Hkv, nmax, D))
+        v = np.zeros_like(k)
+        kept = []
+        for b in range(b0, b1):
+            for h in range(Hkv):
+                kh, vh = lay.host_kv(b, h)
+                k[b - b0, h, :kh.shape[0]] = kh
+                v[b - b0, h, :vh.shape[0]] = vh
+                kept.append(np.arange(kh.shape[0], dtype=np.int32))
+        out[b0:b1] = orc.decode_attn(lay.q_host[b0:b1].astype(np.float64), k, v,
+                                     np.full(b1 - b0, nmax, np.int32), kept, scale)
+        b0 = b1
+    return out

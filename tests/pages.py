@@ -1,4 +1,4 @@
-"""Host-side head-group page management for the kvx decode path.
+"""Test input preparation: lays dense kept rows out in head-group pages.
 
 Layout ("Tangram: Unlocking Non-Uniform KV Cache for Efficient Multi-turn LLM
 Serving", Fig. 8(b), Head Group Page): each head group G has its own pool of
@@ -13,8 +13,9 @@ past a head's kept count are padding and are never read.
 
 These helpers assign physical pages to sequences (any permutation of a group's
 pages is valid: the result does not depend on where pages sit) and pack dense
-kept rows into pools. They run on the host with NumPy; the kernels only read
-the result.
+kept rows into pools, following the page layout that the kvx C ABI documents
+for kvx_decode_attn. They prepare GPU inputs for tests only: the library never
+imports them, and the oracle never sees pages.
 """
 from __future__ import annotations
 

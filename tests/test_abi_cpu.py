@@ -77,6 +77,7 @@ def test_plan_coverage_matches_oracle(kvx, orc, name, policy, num_ctas):
     items, off = plan.items()
     bad, count = orc.plan_coverage(n_oracle.reshape(-1), items)
     assert bad == 0
+    assert np.array_equal(plan.coverage(), count)  # kvx_plan_coverage, bit for bit
     st = plan.stats()
     assert off[0] == 0 and off[-1] == len(items) and np.all(np.diff(off) >= 0)
     assert st["total_tokens"] == int(n_oracle.sum())
@@ -275,8 +276,9 @@ def test_balanced_plan_random_shapes(kvx, orc, seed):
     assert np.array_equal(plan.kept().reshape(-1), n)
     items, off = plan.items()
     assert len(off) == num_ctas + 1 and off[0] == 0 and off[-1] == len(items)
-    bad, _ = orc.plan_coverage(n, items)
+    bad, count = orc.plan_coverage(n, items)
     assert bad == 0
+    assert np.array_equal(plan.coverage(), count)
     T, c0 = 32, plan.stats()["item_overhead"]
     for bh, b, e in items[:, :3]:
         assert b % T == 0 and (e % T == 0 or e == n[bh]), (bh, b, e)
@@ -295,3 +297,16 @@ def test_balanced_plan_random_shapes(kvx, orc, seed):
         cost.append(int((blk[:, 2] - blk[:, 1]).sum()) + c0 * len(blk))
     ideal = (int(n.sum()) + c0 * n.size + c0 * (num_ctas - 1)) / num_ctas
     assert max(cost) <= ideal + c0 + 2 * T + 1, (max(cost), ideal)
+
+
+def test_coverage_record_stride_is_checked(kvx):
+    """kvx_plan_set_coverage_record needs a row per head at least as long as
+    the longest kept set; no device memory is touched by the call."""
+    case = synth.tiny(0)
+    plan = _plan(kvx, case, num_ctas=2)
+    assert int(plan.kept().max()) == 100
+    with pytest.raises(kvx.KvxError) as e:
+        plan.set_coverage_record(1 << 20, 99)
+    assert e.value.status == kvx.KVX_ERANGE
+    plan.set_coverage_record(1 << 20, 100)
+    plan.set_coverage_record(None)

@@ -1,6 +1,8 @@
 """Full-size workloads in the launch configuration the benchmark times
-(balanced plan, one persistent block per SM, tensor-core kernel), checked on
-sampled heads against the fp64 oracle one head at a time."""
+(balanced plan over two persistent blocks per SM, tensor-core kernel): every
+(sequence, query head) of the layer against the fp64 oracle, and the tokens
+the kernel actually consumed (its coverage record) against the oracle's
+count array of the plan."""
 import math
 
 import numpy as np
@@ -9,8 +11,10 @@ import torch
 
 import oracle
 import synth
+from harness import oracle_layer
 from synth.device import TableLayer, ValueTable
-from paged_non_uniform_gb300 import kvx, pages
+from paged_non_uniform_gb300 import kvx
+import pages
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-3
@@ -21,66 +25,78 @@ def table():
     return ValueTable(seed=11, rows=1 << 19, D=128, dtype="bf16")
 
 
-def _plan(cfg, layer):
+def _plan(cfg, layer, policy=kvx.KVX_PLAN_BALANCED):
     plan = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
                                kvx.KVX_BF16, cfg.budget[layer], cfg.seq_len,
-                               cfg.head_group[layer])
+                               cfg.head_group[layer], 0, policy)
     kvx.kvx_plan_upload(plan)
     return plan
 
 
-def _run(plan, lay, cfg):
+def _run(plan, lay, cfg, cover=None):
     out = torch.full((cfg.B, cfg.Hq, cfg.D), float("nan"), device="cuda")
     ws = torch.zeros(plan.workspace_bytes() // 4 + 64, dtype=torch.int32, device="cuda")
+    if cover is not None:
+        plan.set_coverage_record(cover, cover.shape[1])
     kvx.kvx_decode_attn(plan, lay.q, lay.k_pools, lay.v_pools, lay.pool_pages, lay.pt,
                         lay.strides, lay.budget, lay.seq_len, 0.0, out, ws)
     torch.cuda.synchronize()
+    if cover is not None:
+        plan.set_coverage_record(None)
     assert kvx.kvx_workspace_status(ws) == 0
     return out.cpu().numpy().astype(np.float64)
 
 
-def _sample_heads(cfg, layer, k, seed):
-    g = synth.rng(seed)
-    heads = {tuple(int(x) for x in np.unravel_index(np.argmax(cfg.n[layer]), cfg.n[layer].shape)),
-             tuple(int(x) for x in np.unravel_index(np.argmin(cfg.n[layer]), cfg.n[layer].shape))}
-    while len(heads) < k:
-        heads.add((int(g.integers(cfg.B)), int(g.integers(cfg.Hkv))))
-    return sorted(heads)
+def check_coverage(plan, cover):
+    """The kernel's count of consumed tokens equals, bit for bit, the oracle's
+    count array of the plan's items, and that array has no violation (every
+    kept token once, nothing past n)."""
+    items, _ = plan.items()
+    n = plan.kept().reshape(-1)
+    bad, count = oracle.load().plan_coverage(n, items)
+    assert bad == 0
+    got = cover.cpu().numpy()
+    assert got.shape == count.shape
+    assert np.array_equal(got, count)
+    assert int(got.sum()) == int(n.sum())
 
 
-@pytest.mark.parametrize("name", ["qwen3_4b", "qwen3_4b_32k", "qwen25_32b"])
-def test_full_size_sampled_heads(name, table):
-    cfg = synth.decode_config(name, seed=0, layers=1)
-    plan = _plan(cfg, 0)
+def every_head(name, table, policy=kvx.KVX_PLAN_BALANCED, cfg=None):
+    cfg = cfg or synth.decode_config(name, seed=0, layers=1)
+    plan = _plan(cfg, 0, policy)
     lay = TableLayer(cfg, 0, table, plan.group_pages(), seed=0)
-    got = _run(plan, lay, cfg)
+    cover = torch.zeros((cfg.B * cfg.Hkv, max(1, int(cfg.n[0].max()))), dtype=torch.int32,
+                        device="cuda")
+    got = _run(plan, lay, cfg, cover)
+    check_coverage(plan, cover)
     assert np.all(np.isfinite(got))
-    orc = oracle.load()
-    g = cfg.Hq // cfg.Hkv
-    for b, h in _sample_heads(cfg, 0, 6, seed=1):
-        k, v = lay.host_kv(b, h)
-        ref = orc.attn_head(lay.q_host[b, h * g:(h + 1) * g], k, v,
-                            np.arange(k.shape[0], dtype=np.int32), 1.0 / math.sqrt(cfg.D))
-        err = float(np.abs(got[b, h * g:(h + 1) * g] - ref).max())
-        assert err <= TOL, (b, h, err)
+    ref = oracle_layer(oracle.load(), cfg, lay)
+    err = float(np.abs(got - ref).max())
+    st = plan.stats()
+    print(f"{cfg.name} layer 0, policy {policy}: {st['num_ctas']} blocks, "
+          f"{st['num_items']} items, {st['num_split_heads']} split heads; "
+          f"{cfg.B * cfg.Hq} (sequence, query head) outputs, max abs err {err:.3e}")
+    assert err <= TOL, err
+    return plan, lay, cfg
+
+
+@pytest.mark.parametrize("name", ["qwen3_4b", "qwen3_4b_32k", "qwen25_32b", "llama3_sparse"])
+def test_full_size_every_head_and_coverage(name, table):
+    every_head(name, table)
+
+
+def test_full_size_uniform_split_every_head_and_coverage(table):
+    """The uniform-split plan (Tangram, Fig. 4(c)) on the same layer."""
+    every_head("qwen3_4b", table, kvx.KVX_PLAN_UNIFORM)
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-def test_full_size_group_sweep_sampled_heads(G, table):
+def test_full_size_group_sweep_every_head(G, table):
     """The head-group sweep's configurations (Qwen3-4B layer 0 regrouped into
-    groups of G KV heads; G = 8 is the unified page): sampled heads against
-    the oracle, as the benchmark's group sweep runs them."""
-    cfg = synth.regroup(synth.decode_config("qwen3_4b", seed=0, layers=1), G)
-    plan = _plan(cfg, 0)
-    lay = TableLayer(cfg, 0, table, plan.group_pages(), seed=0)
-    got = _run(plan, lay, cfg)
-    orc = oracle.load()
-    g = cfg.Hq // cfg.Hkv
-    for b, h in _sample_heads(cfg, 0, 4, seed=G):
-        k, v = lay.host_kv(b, h)
-        ref = orc.attn_head(lay.q_host[b, h * g:(h + 1) * g], k, v,
-                            np.arange(k.shape[0], dtype=np.int32), 1.0 / math.sqrt(cfg.D))
-        assert float(np.abs(got[b, h * g:(h + 1) * g] - ref).max()) <= TOL, (G, b, h)
+    groups of G KV heads; G = 8 is the unified page), as the benchmark's group
+    sweep runs them: every head against the oracle, coverage exact."""
+    every_head(None, table, cfg=synth.regroup(synth.decode_config("qwen3_4b", seed=0, layers=1),
+                                              G))
 
 
 def test_full_size_sparse_with_selected_tokens(table):
@@ -97,7 +113,7 @@ def test_full_size_sparse_with_selected_tokens(table):
         K = synth.normal(gen, (L, cfg.D), "bf16")
         V = synth.normal(gen, (L, cfg.D), "bf16")
         qh = lay.q_host[b, h * g:(h + 1) * g]
-        kept = synth.select_top_recent(qh, K, 2048, 128)
+        kept = oracle.load().select_topk(qh, K, 2048, 128)
         assert kept.size == cfg.n[0][b, h] == 2176
         ids = torch.from_numpy(lay.pool_row_ids(b, h)).cuda()
         gi = int(cfg.head_group[0][h])
@@ -114,9 +130,9 @@ def test_full_size_sparse_with_selected_tokens(table):
         assert err <= TOL, (b, h, err)
 
 
-def test_full_size_gpu_selection_sampled_heads(table):
+def test_full_size_gpu_selection_every_head(table):
     """Batch 8 x 122k dense keys (Llama-3-8B shapes, one layer, tiled from the
-    value table): the GPU kept set of sampled heads against the oracle's
+    value table): the GPU kept set of every head against the oracle's
     selection, outside the fp32 error band around the cut."""
     from test_select_gpu import check_head
     cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
@@ -137,7 +153,7 @@ def test_full_size_gpu_selection_sampled_heads(table):
     assert np.all(cnt == top + recent)
     orc = oracle.load()
     g = Hq // Hkv
-    for b, h in [(0, 0), (2, 5), (7, 7)]:
+    for b, h in [(b, h) for b in range(B) for h in range(Hkv)]:
         bh = b * Hkv + h
         kh = table.host_rows(4242, bh * L + np.arange(L, dtype=np.int64))
         check_head(orc, q[b, h * g:(h + 1) * g], kh, top, recent, kept[bh])
@@ -146,9 +162,9 @@ def test_full_size_gpu_selection_sampled_heads(table):
 def test_full_size_select_pack_attend(table):
     """The benchmark's sparse pipeline at full size (Llama-3-8B shapes, batch 8
     x 122k, one layer): GPU selection, packing of the kept rows into
-    head-group pages, attention over them. Sampled heads: packed slots equal
-    the dense rows bit for bit, and the output equals the oracle's attention
-    over the same kept set."""
+    head-group pages, attention over them. Every head: packed slots equal the
+    dense rows bit for bit, and the output equals the oracle's attention over
+    the same kept set."""
     cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
     B, Hq, Hkv, D, L, P = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, int(cfg.seq_len[0]), cfg.P
     top, recent = 2048, 128
@@ -187,7 +203,7 @@ def test_full_size_select_pack_attend(table):
     kept_h = kept.cpu().numpy()
     orc = oracle.load()
     g = Hq // Hkv
-    for b, h in [(0, 0), (4, 3), (7, 7)]:
+    for b, h in [(b, h) for b in range(B) for h in range(Hkv)]:
         bh = b * Hkv + h
         idx = kept_h[bh]
         rows = bh * L + idx.astype(np.int64)

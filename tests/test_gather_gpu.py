@@ -99,14 +99,26 @@ def test_gather_flags_bad_entries_and_copies_the_rest():
     assert np.array_equal(got, ref)
 
 
+def _row_blocks_u8(table, shift, ids, block_bytes):
+    """Host copy of pool blocks `ids` of a pool filled from `table` with
+    `shift` whose first 8 bytes were stamped with the block id: the bytes the
+    gather must copy, uint8 [len(ids)][block_bytes]."""
+    rows_per_block = block_bytes // 256
+    blk = table.host_raw_rows(shift, (ids[:, None].astype(np.int64) * rows_per_block
+                                      + np.arange(rows_per_block)).reshape(-1))
+    blk = np.ascontiguousarray(blk).reshape(ids.size, block_bytes // 2)
+    blk.view(np.int64)[:, 0] = ids
+    return blk.view(np.uint8).reshape(ids.size, block_bytes)
+
+
 @pytest.mark.parametrize("extents", [False, True])
-def test_full_size_gather_sampled_rows(extents):
+def test_full_size_gather_every_row(extents):
     """256 sequences, 16..16k tokens, 32 KB blocks, 40 GB fragmented K+V pool,
-    two 8 GiB staging tensors: sampled rows bit-exact, run list exact."""
+    two 8 GiB staging tensors: all 512 staging rows (256 per tensor) bit-exact
+    against the oracle's gather of the same blocks, and the run list exact."""
     cfg = synth.gather_config(seed=0, extents=extents)
     orc = oracle.load()
     table = ValueTable(seed=21, rows=1 << 18, D=128, dtype="bf16")
-    rows_per_block = cfg.block_bytes // 256
     pools, stagings, shifts = [], [], [12345, 777777]
     for t in range(2):
         p = torch.empty((cfg.num_phys, cfg.block_bytes // 2), dtype=torch.bfloat16, device="cuda")
@@ -122,21 +134,18 @@ def test_full_size_gather_sampled_rows(extents):
     assert np.array_equal(gcnt, cnt) and int(gcnt.sum()) == total
     for s in range(cfg.S):
         assert np.array_equal(gruns[s, :cnt[s]], runs[s, :cnt[s]])
-    sample = sorted({0, cfg.S - 1, int(np.argmax(cfg.nb)), int(np.argmin(cfg.nb)), 17, 101})
+    checked = 0
     for t in range(2):
-        for s in sample:
+        for s in range(cfg.S):
             ids = cfg.bt[s, :cfg.nb[s]]
-            # host copy of the blocks this row needs: table rows + id stamp
-            blk = table.host_rows(shifts[t], (ids[:, None].astype(np.int64) * rows_per_block
-                                              + np.arange(rows_per_block)).reshape(-1))
-            blk = synth.f32_to_bf16_bits(blk).reshape(ids.size, cfg.block_bytes // 2).copy()
-            blk.view(np.int64)[:, 0] = ids
-            mini = blk.view(np.uint8).reshape(ids.size, cfg.block_bytes)
-            st = np.zeros((1, cfg.row_bytes), np.uint8)
+            mini = _row_blocks_u8(table, shifts[t], ids, cfg.block_bytes)
+            ref = np.zeros((1, cfg.row_bytes), np.uint8)
             orc.gather(np.arange(ids.size, dtype=np.int32)[None, :],
-                       np.array([ids.size], np.int32), mini, st)
+                       np.array([ids.size], np.int32), mini, ref)
             got = stagings[t][s].view(torch.uint8).cpu().numpy()
-            assert np.array_equal(got, st[0]), (t, s)
+            assert np.array_equal(got, ref[0]), (t, s)
+            checked += 1
+    assert checked == 2 * cfg.S == 512
 
 
 def test_medium_gather_all_rows():
@@ -145,7 +154,6 @@ def test_medium_gather_all_rows():
     cfg = synth.gather_config(seed=7, S=32, num_phys=32768)
     orc = oracle.load()
     table = ValueTable(seed=23, rows=1 << 18, D=128, dtype="bf16")
-    rows_per_block = cfg.block_bytes // 256
     pools, stagings, shifts = [], [], [5, 99991]
     for t in range(2):
         p = torch.empty((cfg.num_phys, cfg.block_bytes // 2), dtype=torch.bfloat16, device="cuda")
@@ -160,11 +168,7 @@ def test_medium_gather_all_rows():
         got = stagings[t].view(torch.uint8).cpu().numpy()
         for s in range(cfg.S):
             ids = cfg.bt[s, :cfg.nb[s]]
-            blk = table.host_rows(shifts[t], (ids[:, None].astype(np.int64) * rows_per_block
-                                              + np.arange(rows_per_block)).reshape(-1))
-            blk = synth.f32_to_bf16_bits(blk).reshape(ids.size, cfg.block_bytes // 2).copy()
-            blk.view(np.int64)[:, 0] = ids
-            mini = blk.view(np.uint8).reshape(ids.size, cfg.block_bytes)
+            mini = _row_blocks_u8(table, shifts[t], ids, cfg.block_bytes)
             init = np.full((1, cfg.row_bytes // 2), 0x4040, np.uint16)  # bf16 3.0
             ref = orc.gather(np.arange(ids.size, dtype=np.int32)[None, :],
                              np.array([ids.size], np.int32), mini,

@@ -7,7 +7,8 @@ import torch
 
 import synth
 from harness import DeviceCase, make_plan
-from paged_non_uniform_gb300 import kvx, pages
+from paged_non_uniform_gb300 import kvx
+import pages
 
 pytestmark = pytest.mark.gpu
 BAND = 4096  # bytes on each side

@@ -17,7 +17,8 @@ import torch
 
 import oracle
 import synth
-from paged_non_uniform_gb300 import kvx, pages
+from paged_non_uniform_gb300 import kvx
+import pages
 
 pytestmark = pytest.mark.gpu
 U = 2.0 ** -24
