@@ -294,12 +294,46 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_gather_scratch[KVX_GATHER_STATIC_SCRATCH_BYTES];
 
-// Device address of g_gather_scratch on the current device, looked up once
-// per device (the array's host-side name is only a stand-in, not a device
-// address). Returns nullptr and sets *err if the lookup fails.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Process-unique id of the CUDA context current on this thread, or 0 when
+// there is none yet (or the driver cannot tell).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = (CtxGetCurrentFn)f;
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = (CtxGetIdFn)f;
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_gather_scratch in the current device's context. The
+// array's host-side name is only a stand-in, not a device address, so the
+// address is looked up with cudaGetSymbolAddress the first time a context
+// of the device calls, and again whenever the current context is not the one
+// the cached address belongs to (a device reset destroys the context, and
+// the array may land elsewhere in the next one). Returns nullptr and sets
+// *err if the lookup fails.
 void *static_scratch(cudaError_t *err) {
   static std::mutex mu;
   static void *addr[64] = {nullptr};
+  static unsigned long long ctx_of[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= 64) {
@@ -307,7 +341,8 @@ void *static_scratch(cudaError_t *err) {
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (!addr[dev] || ctx == 0 || ctx != ctx_of[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_gather_scratch);
     if (e != cudaSuccess) {
@@ -315,6 +350,7 @@ void *static_scratch(cudaError_t *err) {
       return nullptr;
     }
     addr[dev] = p;
+    ctx_of[dev] = current_context_id();  // the lookup made the context current
   }
   *err = cudaSuccess;
   return addr[dev];

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from paged_non_uniform_gb300 import kvx
 
@@ -49,8 +50,12 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
                  for t in range(2)]
         ref, got, ws_status, status = _both(cfg, pools, 0)
         assert ws_status == 0 and status == 0, call
+        init = synth.rng(5).integers(0, 256, size=(cfg.S, cfg.row_bytes), dtype=np.uint8)
         for t in range(2):
             assert np.array_equal(ref[t], got[t]), (call, t)
+            # and on its own against the oracle's brute-force gather
+            exp = oracle.load().gather(cfg.bt, cfg.nb, pools[t], init.copy())
+            assert np.array_equal(got[t], exp), (call, t)
 
 
 def test_noalloc_zero_tail_and_error_bits():
@@ -70,3 +75,49 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     with pytest.raises(kvx.KvxError) as e:
         kvx.kvx_gather_coalesce_noalloc(p, p, 4096, 4096, [p], 1, 16, [p], 16 * 4096, 0)
     assert e.value.status == kvx.KVX_ESCRATCH
+
+
+def _largest_fitting_max_blocks(S):
+    cap = 8 << 20  # KVX_GATHER_NOALLOC_SCRATCH_BYTES
+    lo, hi = 1, 1 << 16
+    assert kvx.kvx_gather_workspace_bytes(S, lo) <= cap < kvx.kvx_gather_workspace_bytes(S, hi)
+    while hi - lo > 1:
+        mid = (lo + hi) // 2
+        if kvx.kvx_gather_workspace_bytes(S, mid) <= cap:
+            lo = mid
+        else:
+            hi = mid
+    return lo
+
+
+def test_noalloc_at_the_scratch_limit():
+    """S = 256 (the KV-RM shape) with the largest table the 8 MiB scratch
+    holds, short rows: equal to the workspace entry point and to the oracle.
+    One more block per row is rejected with KVX_ESCRATCH before any launch."""
+    S = 256
+    mb = _largest_fitting_max_blocks(S)
+    assert mb >= 1024  # the KV-RM workload's table (16k tokens / 16) fits
+    g = synth.rng(17)
+    num_phys, bb = 4096, 16
+    nb = g.integers(0, 9, size=S).astype(np.int32)
+    bt = np.full((S, mb), -1, np.int32)
+    for s in range(S):
+        bt[s, :nb[s]] = g.choice(num_phys, size=nb[s], replace=False)
+    cfg = synth.GatherConfig("limit", S, mb, nb, bt, num_phys, bb, 8 * bb, nb * 16)
+    pools = [synth.block_stamp_pool(num_phys, bb, seed=21)]
+    ref, got, ws_status, status = _both(cfg, pools, 0)
+    assert ws_status == status == 0
+    assert np.array_equal(ref[0], got[0])
+    init = synth.rng(5).integers(0, 256, size=(S, 8 * bb), dtype=np.uint8)
+    assert np.array_equal(got[0], oracle.load().gather(bt, nb, pools[0], init.copy()))
+    p = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvx.KvxError) as e:
+        kvx.kvx_gather_coalesce_noalloc(p, p, S, mb + 1, [p], num_phys, bb, [p], 8 * bb, 0)
+    assert e.value.status == kvx.KVX_ESCRATCH
+
+
+def test_noalloc_setup_call_with_no_rows():
+    """S = 0 only prepares the device (address lookup, header clear)."""
+    p = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    kvx.kvx_gather_coalesce_noalloc(p, p, 0, 0, [p], 1, 16, [p], 16, 0)
+    torch.cuda.synchronize()
