@@ -3,9 +3,11 @@
 
 One step = one decode step of the Qwen3-4B-shaped workload: for each of its 36
 layers, split decode attention over that layer's head-group paged KV cache
-(plus the log-sum-exp merge of split heads). The KV-RM gather (256 sequences,
-fragmented 40 GB pool, fixed-shape staging) is timed in its own loop and
-reported in the same line.
+(the log-sum-exp merge of split heads runs in the same launch). The other
+decode workloads (the 32k-context step, the Qwen2.5-32B step, the Llama-3-8B
+sparse step and the tiny fp32 case) are timed the same way and reported under
+`workloads`; the KV-RM gather (256 sequences, fragmented 40 GB pool,
+fixed-shape staging) is timed in its own loop. All in one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -33,6 +35,7 @@ import synth  # noqa: E402
 
 METRIC = "decode-attn KV GB/s and % of GB300 HBM roofline; gather GB/s"
 FALLBACK_HBM = 6800.0
+EXTRA_WORKLOADS = ["qwen3_4b_32k", "qwen25_32b", "llama3_sparse", "tiny"]
 
 
 def parse():
@@ -48,7 +51,9 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-group-sweep", action="store_true")
     ap.add_argument("--no-sparse", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-workloads", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=3.0,
+                    help="oracle time per workload in the CPU baseline")
     return ap.parse_args()
 
 
@@ -64,7 +69,7 @@ def peaks():
 
 KERNEL_SOURCES = ["attn_mma.cu", "ptx.cuh", "split_merge.cuh", "kvx_internal.h", "abi.cpp",
                   "plan.cpp"]
-PROFILE = os.path.join(ROOT, "profiles", "attn_mma_qwen3_4b.md")
+PROFILE = os.path.join(ROOT, "profiles", "attn_mma_qwen3_4b.json")
 
 
 def kernel_source_hash() -> str:
@@ -80,16 +85,13 @@ def kernel_source_hash() -> str:
 
 def profiled_traffic():
     """(dram bytes per launch, algorithmic bytes of that launch) from the
-    committed ncu summary, or None if the kernel has changed since."""
+    committed ncu figures, or None if the kernel has changed since."""
     try:
-        kv = {}
-        for line in open(PROFILE):
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                kv[k.strip()] = v.strip().strip("`")
-        if kv.get("kernel_source_sha256") != kernel_source_hash():
+        with open(PROFILE) as f:
+            d = json.load(f)
+        if d.get("kernel_source_sha256") != kernel_source_hash():
             return None
-        return float(kv["dram_bytes_per_launch"]), float(kv["algorithmic_bytes_per_launch"])
+        return float(d["dram_bytes_per_launch"]), float(d["algorithmic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
 
@@ -101,66 +103,98 @@ def describe(cfg) -> str:
             f"kept tokens/step {int(cfg.n.sum())}")
 
 
+def config_of(cfg) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": describe(cfg),
+            "l2": "inputs larger than L2: each step streams "
+                  f"{cfg.kv_bytes_step() / 1e9:.1f} GB of distinct KV pages",
+            "plan": "balanced ahead-of-time split, two persistent blocks per SM"}
+
+
 # ------------------------------------------------------------ CPU oracle
-def host_sequences(cfg, table_seed=11):
-    """Yields, sequence by sequence and layer by layer, the oracle's inputs for
-    all KV heads of one sequence: (q [1][Hq][D], k, v [1][Hkv][nmax][D],
-    [nmax], kept sets, KV bytes), rebuilt on the host from the seeded value
-    table and page tables the GPU arm uses."""
+def host_group_pages(cfg, layer):
+    """Pages each group needs (ceil of the group's longest head / P), as the
+    library reports them; used to rebuild the GPU arm's page tables."""
+    hg = cfg.head_group[layer]
+    gp = np.zeros((cfg.num_groups, cfg.B), dtype=np.int64)
+    for h in range(cfg.Hkv):
+        gp[hg[h]] = np.maximum(gp[hg[h]], (cfg.n[layer][:, h] + cfg.P - 1) // cfg.P)
+    return gp
+
+
+def host_batch(cfg, layer=0, b0=0, max_rows=1 << 20, table_seed=11):
+    """The oracle's inputs for sequences b0..b1-1 of one layer, rebuilt on the
+    host from the seeded value table and page tables the GPU arm uses
+    (synth.device.TableLayer with seed 0): q [nb][Hq][D], dense k and v
+    [nb][Hkv][nmax][D] holding each head's kept rows at positions 0..n-1,
+    lengths, kept sets, and the KV bytes (storage type) they stand for. As
+    many sequences as fit in max_rows rows per tensor (at least one)."""
     from synth.device import page_tables_for, rows_in_group
     table_rows = 1 << 19
-    vals = synth.bf16_bits_to_f32(synth.value_table(table_seed, table_rows * cfg.D, "bf16"))
-    vals = vals.reshape(table_rows, cfg.D)
-    gpf = host_group_pages(cfg)
-    for layer in range(cfg.layers):
-        tables, _ = page_tables_for(gpf(layer), 0 * 131 + layer, 0)
-        hg = cfg.head_group[layer]
-        rows, gsize = rows_in_group(hg), np.bincount(hg, minlength=cfg.num_groups)
-        gen = synth.rng(0 * 1009 + layer)
-        sh = gen.integers(0, table_rows, size=(cfg.num_groups, 2)).astype(np.int64)
-        q = synth.normal(gen, (cfg.B, cfg.Hq, cfg.D), cfg.dtype)
-        for b in range(cfg.B):
-            n = cfg.n[layer][b]
-            nmax = int(n.max())
-            k = np.zeros((1, cfg.Hkv, nmax, cfg.D))
-            v = np.zeros((1, cfg.Hkv, nmax, cfg.D))
-            for h in range(cfg.Hkv):
-                gi = int(hg[h])
-                t = np.arange(int(n[h]), dtype=np.int64)
-                ids = (tables[gi][b, t // cfg.P].astype(np.int64) * int(gsize[gi]) +
-                       int(rows[h])) * cfg.P + t % cfg.P
-                k[0, h, :n[h]] = vals[(sh[gi, 0] + ids) % table_rows]
-                v[0, h, :n[h]] = vals[(sh[gi, 1] + ids) % table_rows]
-            kept = [np.arange(int(n[h]), dtype=np.int32) for h in range(cfg.Hkv)]
-            qb = np.ascontiguousarray(q[b:b + 1], dtype=np.float64)
-            yield qb, k, v, np.array([nmax], np.int32), kept, int(n.sum()) * 2 * cfg.D * 2
+    vals = synth.value_table(table_seed, table_rows * cfg.D, cfg.dtype)
+    vals = (synth.bf16_bits_to_f32(vals) if cfg.dtype == "bf16" else vals).reshape(table_rows,
+                                                                                   cfg.D)
+    n = cfg.n[layer]
+    b1 = b0 + 1
+    while b1 < cfg.B and (b1 + 1 - b0) * cfg.Hkv * int(n[b0:b1 + 1].max()) <= max_rows:
+        b1 += 1
+    tables, _ = page_tables_for(host_group_pages(cfg, layer), 0 * 131 + layer, 0)
+    hg = cfg.head_group[layer]
+    rows, gsize = rows_in_group(hg), np.bincount(hg, minlength=cfg.num_groups)
+    gen = synth.rng(0 * 1009 + layer)
+    sh = gen.integers(0, table_rows, size=(cfg.num_groups, 2)).astype(np.int64)
+    q = synth.normal(gen, (cfg.B, cfg.Hq, cfg.D), cfg.dtype)
+    nmax = int(n[b0:b1].max())
+    k = np.zeros((b1 - b0, cfg.Hkv, nmax, cfg.D))
+    v = np.zeros_like(k)
+    kept = []
+    for b in range(b0, b1):
+        for h in range(cfg.Hkv):
+            gi = int(hg[h])
+            t = np.arange(int(n[b, h]), dtype=np.int64)
+            ids = (tables[gi][b, t // cfg.P].astype(np.int64) * int(gsize[gi]) +
+                   int(rows[h])) * cfg.P + t % cfg.P
+            k[b - b0, h, :t.size] = vals[(sh[gi, 0] + ids) % table_rows]
+            v[b - b0, h, :t.size] = vals[(sh[gi, 1] + ids) % table_rows]
+            kept.append(np.arange(t.size, dtype=np.int32))
+    es = 2 if cfg.dtype == "bf16" else 4
+    nbytes = int(n[b0:b1].sum()) * 2 * cfg.D * es
+    qb = np.ascontiguousarray(q[b0:b1], dtype=np.float64)
+    return (qb, k, v, np.full(b1 - b0, nmax, np.int32), kept), nbytes, b1 - b0
 
 
-def oracle_sample(cfg, seconds):
-    """Times the fp64 oracle (OpenMP over the KV heads of one sequence per
-    call) on the workload's sequences in order until `seconds` of oracle time
-    have been spent. Returns (kv bytes, seconds, heads, threads)."""
+def oracle_timing(cfg, seconds):
+    """Times oracle_decode_attn, as it stands, on one batch of the workload's
+    layer-0 sequences (OpenMP over the batch's (sequence, KV head) pairs),
+    repeated until `seconds` of oracle time. Returns (GB/s of KV, threads
+    used, description)."""
     import oracle
     orc = oracle.load()
+    args, nbytes, nseq = host_batch(cfg)
     scale = 1.0 / math.sqrt(cfg.D)
-    spent, nbytes, heads = 0.0, 0, 0
-    for item in host_sequences(cfg):
+    spent, reps = 0.0, 0
+    while spent < seconds or reps == 0:
         t0 = time.perf_counter()
-        orc.decode_attn(*item[:5], scale)
+        orc.decode_attn(*args, scale)
         spent += time.perf_counter() - t0
-        nbytes += item[5]
-        heads += cfg.Hkv
-        if spent >= seconds:
-            break
-    return nbytes, spent, heads, min(orc.num_threads(), cfg.Hkv)
+        reps += 1
+    heads = nseq * cfg.Hkv
+    cores = min(orc.num_threads(), heads)
+    return (nbytes * reps / spent / 1e9, cores,
+            f"{nseq} sequences x {cfg.Hkv} KV heads of {cfg.name} layer 0 ({nbytes / 1e9:.3f} "
+            f"GB of {cfg.dtype} KV per call), {reps} calls in {spent:.1f} s of fp64 oracle "
+            f"time, OpenMP over the {heads} (sequence, KV head) pairs")
 
 
-def cpu_baseline(cfg, seconds):
-    nbytes, secs, heads, cores = oracle_sample(cfg, seconds)
-    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{heads} (sequence, KV head) pairs of {cfg.name}, from layer 0 on "
-                      f"({nbytes / 1e9:.3f} GB of bf16 KV, {secs:.1f} s of fp64 oracle time; "
-                      f"one sequence per call, OpenMP over its KV heads)"}
+def cpu_baseline(cfg, seconds, extra=()):
+    value, cores, sample = oracle_timing(cfg, seconds)
+    out = {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+           "workloads": {}}
+    for name in extra:
+        c = synth.decode_config(name, seed=0, layers=1)
+        v, cr, smp = oracle_timing(c, seconds)
+        out["workloads"][name] = {"value": v, "unit": "GB/s", "cores": cr, "sample": smp}
+    return out
 
 
 def host_cpu() -> dict:
@@ -225,61 +259,44 @@ def copy_ceiling(dev, stream, torch, gib=4, reps=10) -> float:
     return gbs
 
 
-def host_group_pages(cfg):
-    """Pages each group needs (for the oracle-only arm, computed like the
-    page tables the GPU arm builds: ceil of the group's longest head / P)."""
-    def fn(layer):
-        hg = cfg.head_group[layer]
-        gp = np.zeros((cfg.num_groups, cfg.B), dtype=np.int64)
-        for h in range(cfg.Hkv):
-            gp[hg[h]] = np.maximum(gp[hg[h]], (cfg.n[layer][:, h] + cfg.P - 1) // cfg.P)
-        return gp
-    return fn
-
-
 def run_reference(args, rank, world):
     """The oracle as it stands, on the host cores: each step runs it over the
-    same bounded sample of the workload (the first sequences of layer 0),
-    sized so that warm-up plus timed steps take about a minute."""
+    same bounded sample of the workload (the first sequences of layer 0, one
+    call with OpenMP over all their (sequence, KV head) pairs), repeated so
+    that warm-up plus timed steps take about half a minute."""
     import oracle
-    cfg = synth.decode_config(args.workload, seed=0)
     if rank != 0:
         return
+    cfg = synth.decode_config(args.workload, seed=0)
     orc = oracle.load()
     total_steps = max(args.steps + args.warmup, 1)
-    target = max(0.02, 60.0 / total_steps)
-    sample = []  # (q, k, v, L, kept, bytes) per sequence
+    target = max(0.02, 30.0 / total_steps)
+    call, nbytes, nseq = host_batch(cfg)
     scale = 1.0 / math.sqrt(cfg.D)
-    spent, held = 0.0, 0
-    for item in host_sequences(cfg):
-        t0 = time.perf_counter()
-        orc.decode_attn(*item[:5], scale)
-        spent += time.perf_counter() - t0
-        sample.append(item)
-        held += item[1].nbytes + item[2].nbytes
-        if spent >= target or held >= (4 << 30):
-            break
+    t0 = time.perf_counter()
+    orc.decode_attn(*call, scale)
+    reps = max(1, int(round(target / max(time.perf_counter() - t0, 1e-6))))
     secs = []
     for i in range(total_steps):
         t0 = time.perf_counter()
-        for it in sample:
-            orc.decode_attn(*it[:5], scale)
+        for _ in range(reps):
+            orc.decode_attn(*call, scale)
         if i >= args.warmup:
             secs.append(time.perf_counter() - t0)
-    nbytes = sum(it[5] for it in sample)
     sec = sum(secs)
-    value = nbytes * len(secs) / sec / 1e9
-    cores = min(orc.num_threads(), cfg.Hkv)
+    value = nbytes * reps * len(secs) / sec / 1e9
+    cores = min(orc.num_threads(), nseq * cfg.Hkv)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * sec / max(len(secs), 1), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(cfg)},
+            "config": config_of(cfg),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": f"each step: the fp64 oracle over the first {len(sample)} "
-                                       f"sequences of the step in layer order "
-                                       f"({nbytes / 1e9:.3f} GB of bf16 KV), "
-                                       f"OpenMP over each sequence's KV heads"},
+                             "sample": f"each step: the fp64 oracle over the first {nseq} "
+                                       f"sequences of layer 0 ({nbytes / 1e9:.3f} GB of bf16 "
+                                       f"KV), {reps} times, OpenMP over their "
+                                       f"{nseq * cfg.Hkv} (sequence, KV head) pairs",
+                             "host": host_cpu()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -367,12 +384,147 @@ class Clocks:
 
 
 # -------------------------------------------------------------- GPU arm
+class DecodeSetup:
+    """Plans (balanced, default block count) and head-group pools of every
+    layer of one decode workload, filled on the GPU from a seeded value
+    table; one shared workspace and an output per layer."""
+
+    def __init__(self, cfg, table, dev, kvx, torch):
+        from synth.device import TableLayer
+        self.cfg, self.kvx = cfg, kvx
+        dtype = kvx.KVX_BF16 if cfg.dtype == "bf16" else kvx.KVX_F32
+        self.plans, self.layers, self.plan_us = [], [], []
+        for l in range(cfg.layers):
+            p = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups, dtype,
+                                    cfg.budget[l], cfg.seq_len, cfg.head_group[l], 0)
+            kvx.kvx_plan_upload(p)
+            self.plan_us.append(p.stats()["plan_us"])
+            self.plans.append(p)
+            self.layers.append(TableLayer(cfg, l, table, p.group_pages(), seed=0, device=dev))
+        ws_bytes = max(p.workspace_bytes() for p in self.plans)
+        self.ws = torch.zeros(max(ws_bytes, 256) // 4 + 64, dtype=torch.int32, device=dev)
+        self.outs = torch.empty((cfg.layers, cfg.B, cfg.Hq, cfg.D), dtype=torch.float32,
+                                device=dev)
+        self.bytes_layer = [cfg.kv_bytes_layer(l) for l in range(cfg.layers)]
+        self.bytes_step = sum(self.bytes_layer)
+
+    def call(self, l, stream, q=None, out=None):
+        lay = self.layers[l]
+        self.kvx.kvx_decode_attn(self.plans[l], lay.q if q is None else q, lay.k_pools,
+                                 lay.v_pools, lay.pool_pages, lay.pt, lay.strides, lay.budget,
+                                 lay.seq_len, 0.0, self.outs[l] if out is None else out, self.ws,
+                                 stream=stream)
+
+    def step(self, stream):
+        for l in range(self.cfg.layers):
+            self.call(l, stream)
+
+    def status(self) -> int:
+        return self.kvx.kvx_workspace_status(self.ws)
+
+    def per_launch(self, stream, torch, steps):
+        """A second pass of `steps` steps with a CUDA event after every launch
+        (which serialises the programmatic dependent launches): the rate of
+        each launch on its own, GB/s mean and p10/p50/p90, and its mean
+        duration."""
+        L = self.cfg.layers
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
+        for s in range(steps):
+            ev[s][0].record(stream)
+            for l in range(L):
+                self.call(l, stream)
+                ev[s][l + 1].record(stream)
+        torch.cuda.synchronize()
+        call_ms = np.array([[ev[s][l].elapsed_time(ev[s][l + 1]) for l in range(L)]
+                            for s in range(steps)])
+        rates = np.array([[self.bytes_layer[l] / (call_ms[s, l] * 1e-3) for l in range(L)]
+                          for s in range(steps)]).reshape(-1) / 1e9
+        return {"mean_gbs": float(rates.mean()),
+                "p10_gbs": float(np.percentile(rates, 10)),
+                "p50_gbs": float(np.percentile(rates, 50)),
+                "p90_gbs": float(np.percentile(rates, 90)),
+                "mean_call_us": float(call_ms.mean() * 1e3)}
+
+
+def timed_steps(setup, stream, torch, steps, warmup, dist=None, dev=None, clocks=None):
+    """W untimed steps, then exactly K steps between two events on the
+    launching stream (barrier and synchronize on both sides). Returns
+    (ms per step as the max over ranks, clock record or None)."""
+    for _ in range(warmup):
+        setup.step(stream)
+    torch.cuda.synchronize()
+    assert setup.status() == 0, "device status set during warm-up"
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        setup.step(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop() if clocks else None
+    if dist:
+        dist.barrier()
+    assert setup.status() == 0, "device status set during the timed region"
+    return max_over_ranks(t0.elapsed_time(t1) / steps, dist, dev), clk
+
+
+def workload_line(setup, ms_step, peak, per_launch, note):
+    cfg = setup.cfg
+    value = setup.bytes_step / (ms_step * 1e-3) / 1e9
+    return {"workload": describe(cfg), "value": value, "unit": "GB/s", "frac": value / peak,
+            "ms_per_step": ms_step, "kv_bytes_per_step": setup.bytes_step,
+            "seq_heads_per_s": cfg.B * cfg.Hq * cfg.layers / (ms_step * 1e-3),
+            "launches_per_step": cfg.layers, "per_launch": per_launch,
+            "plan_host_us_per_layer": float(np.mean(setup.plan_us)), "l2": note}
+
+
+def bench_workload(name, table_for, dev, stream, peak, steps, warmup, kvx, torch):
+    """One extra decode workload in its own pools, freed afterwards."""
+    cfg = synth.decode_config(name, seed=0)
+    setup = DecodeSetup(cfg, table_for(cfg), dev, kvx, torch)
+    if name == "tiny":
+        # One layer of 90.6 KB: each timed call follows an L2 flush (a write
+        # of a buffer larger than L2), with events around the call alone.
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for _ in range(warmup):
+            setup.step(stream)
+        ms = []
+        for _ in range(steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            setup.step(stream)
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        assert setup.status() == 0
+        line = workload_line(setup, float(np.mean(ms)), peak, None,
+                             "each call after an L2 flush (256 MiB write); events around the "
+                             "call; fp32 K/V, CUDA-core kernel; launch-bound")
+        del flush
+    else:
+        ms, _ = timed_steps(setup, stream, torch, steps, warmup)
+        line = workload_line(setup, ms, peak, setup.per_launch(stream, torch, max(3, steps // 4)),
+                             f"inputs larger than L2: {setup.bytes_step / 1e9:.2f} GB of "
+                             "distinct KV pages per step")
+    del setup
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_ours(args, rank, world):
     import torch
     from paged_non_uniform_gb300 import build
     build.build()
     from paged_non_uniform_gb300 import kvx
-    from synth.device import TableLayer, ValueTable
+    from synth.device import ValueTable
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
@@ -381,103 +533,141 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.current_stream()
+    peak, peak_kind = peaks()
 
     cfg = synth.decode_config(args.workload, seed=rank_seed(rank))
-    table = ValueTable(seed=11 + rank_seed(rank), rows=1 << 19, D=cfg.D, dtype=cfg.dtype)
+    tables = {}
+
+    def table_for(c):
+        key = (c.dtype, c.D)
+        if key not in tables:
+            tables[key] = ValueTable(seed=11 + rank_seed(rank), rows=1 << 19, D=c.D,
+                                     dtype=c.dtype, device=dev)
+        return tables[key]
+
     sms = kvx.kvx_device_sm_count()
-    plans, layers = [], []
-    plan_us = []
-    for l in range(cfg.layers):
-        p = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
-                                kvx.KVX_BF16, cfg.budget[l], cfg.seq_len, cfg.head_group[l], 0)
-        kvx.kvx_plan_upload(p)
-        plan_us.append(p.stats()["plan_us"])
-        plans.append(p)
-        layers.append(TableLayer(cfg, l, table, p.group_pages(), seed=0))
-    ws_bytes = max(p.workspace_bytes() for p in plans)
-    ws = torch.zeros(ws_bytes // 4 + 64, dtype=torch.int32, device=dev)
-    outs = torch.empty((cfg.layers, cfg.B, cfg.Hq, cfg.D), dtype=torch.float32, device=dev)
-    launches_per_step = cfg.layers  # one kernel launch per decode-attention call
-    bytes_layer = [cfg.kv_bytes_layer(l) for l in range(cfg.layers)]
-    bytes_step = sum(bytes_layer)
-
-    def call(l, q=None, out=None):
-        lay = layers[l]
-        kvx.kvx_decode_attn(plans[l], lay.q if q is None else q, lay.k_pools, lay.v_pools,
-                            lay.pool_pages, lay.pt, lay.strides, lay.budget, lay.seq_len, 0.0,
-                            outs[l] if out is None else out, ws, stream=stream)
-
-    def step():
-        for l in range(cfg.layers):
-            call(l)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert kvx.kvx_workspace_status(ws) == 0, "device status set during warm-up"
+    setup = DecodeSetup(cfg, table_for(cfg), dev, kvx, torch)
+    bytes_step = setup.bytes_step
 
     # ---- timed region: K whole steps between two events
-    clocks = Clocks()
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for s in range(args.steps):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    if dist:
-        dist.barrier()
-    ms_total = t0.elapsed_time(t1)
-    assert kvx.kvx_workspace_status(ws) == 0, "device status set during the timed region"
-    ms_step = max_over_ranks(ms_total / args.steps, dist, dev)
+    ms_step, clk = timed_steps(setup, stream, torch, args.steps, args.warmup, dist, dev, Clocks())
     bytes_job = sum_over_ranks(bytes_step, dist, dev)
     value = job_rate(bytes_job, ms_step)
 
-    # ---- roofline of the attention kernel: a second pass of K steps with an
-    # event around every call (one kernel launch each); algorithmic KV bytes
-    # of the layer over that launch's duration, averaged over all launches
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(cfg.layers + 1)]
-          for _ in range(args.steps)]
-    for s in range(args.steps):
-        ev[s][0].record(stream)
-        for l in range(cfg.layers):
-            call(l)
-            ev[s][l + 1].record(stream)
-    torch.cuda.synchronize()
-    call_ms = [[ev[s][l].elapsed_time(ev[s][l + 1]) for l in range(cfg.layers)]
-               for s in range(args.steps)]
-    mean_call_ms = float(np.mean(call_ms))
-    rates = np.array([bytes_layer[l] / (call_ms[s][l] * 1e-3)
-                      for s in range(args.steps) for l in range(cfg.layers)]) / 1e9
-    achieved = float(rates.mean())
-    rate_pct = {f"p{q}": float(np.percentile(rates, q)) for q in (10, 50, 90)}
-    peak, peak_kind = peaks()
+    # ---- roofline of the attention kernel. The step launches nothing but
+    # this kernel, one launch per layer, so its mean duration inside the timed
+    # region is the step time over the launches; achieved = algorithmic KV
+    # bytes of the mean launch over that duration.
+    launches_per_step = cfg.layers
+    in_step_us = ms_step * 1e3 / launches_per_step
+    achieved = float(np.mean(setup.bytes_layer)) / (in_step_us * 1e-6) / 1e9
+    per_launch = setup.per_launch(stream, torch, args.steps)
     prof = profiled_traffic()
     # ncu traffic of the profiled launch (layer 0), scaled to the mean launch
-    traffic = (prof[0] * np.mean(bytes_layer) / prof[1]) if prof else None
+    traffic = (prof[0] * np.mean(setup.bytes_layer) / prof[1]) if prof else None
 
     # ---- load balance of layer 0 under the three plans (same kernel)
-    balance = measure_balance(cfg, layers[0], ws, stream, kvx, torch) if rank == 0 else None
+    balance = (measure_balance(cfg, setup.layers[0], setup.ws, stream, kvx, torch)
+               if rank == 0 else None)
 
     # ---- end to end through the public API with host buffers
-    g = cfg.Hq // cfg.Hkv
+    e2e = end_to_end(setup, dev, stream, dist, bytes_job, args.steps, torch)
+    plan_us = float(np.mean(setup.plan_us))
+
+    del setup
+    torch.cuda.empty_cache()
+
+    # ---- the other decode workloads, each in its own pools
+    workloads = None
+    if rank == 0 and not args.no_workloads:
+        workloads = {}
+        for name in EXTRA_WORKLOADS:
+            if name != args.workload:
+                workloads[name] = bench_workload(name, table_for, dev, stream, peak, args.steps,
+                                                 args.warmup, kvx, torch)
+
+    # ---- head-group size sweep (first layers of the same workload)
+    gsweep = None
+    if rank == 0 and not args.no_group_sweep:
+        gsweep = group_sweep(cfg, table_for(cfg), dev, stream, peak, kvx, torch)
+
+    sparse = None
+    if rank == 0 and not args.no_sparse:
+        sparse = sparse_select(dev, stream, peak, kvx, torch)
+
+    # ---- gather (KV-RM movement workload)
+    gather = None
+    if not args.no_gather:
+        tables.clear()
+        torch.cuda.empty_cache()
+        gather = bench_gather(args, dev, stream, peak, dist, world, rank)
+
+    cpu = None
+    ceiling = copy_ceiling(dev, stream, torch)
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(cfg, args.cpu_seconds,
+                           [w for w in ("qwen25_32b", "llama3_sparse", "tiny")
+                            if w != args.workload])
+        cpu["host"] = host_cpu()
+        cpu["gather"] = cpu_gather_baseline()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 K/V, fragmented page tables)",
+            "config": config_of(cfg), "sms": sms,
+            "frac_of_hbm": value / world / peak,
+            "seq_heads_per_s": world * cfg.B * cfg.Hq * cfg.layers / (ms_step * 1e-3),
+            "kv_bytes_per_step": bytes_job,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "traffic_note": "ncu dram read+write of the profiled layer-0 launch, "
+                                         "scaled to the mean launch by algorithmic bytes"
+                                         if prof else "kernel changed since the committed "
+                                                      "capture",
+                         "kernel": "attn_mma_kernel<128> (one launch per layer call; the only "
+                                   "kernel of the step)",
+                         "timing": "in-step: frac and achieved use the mean launch duration "
+                                   "inside the timed region (step time / launches per step)",
+                         "in_step_launch_us": in_step_us,
+                         "per_launch_events": dict(per_launch, frac=per_launch["mean_gbs"] / peak,
+                                                   timing="second pass of K steps with an "
+                                                          "event after every launch, which "
+                                                          "serialises the programmatic "
+                                                          "dependent launches"),
+                         "peak_source": f"{peak_kind} hbm_gbs", "copy_ceiling_gbs": ceiling},
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+            "plan_host_us_per_layer": plan_us,
+            "workloads": workloads,
+            "gather": gather,
+            "balance": balance,
+            "group_sweep": gsweep,
+            "sparse_select": sparse,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def end_to_end(setup, dev, stream, dist, bytes_job, steps, torch):
+    """The same step through the public API with host buffers: every step
+    copies its q from pinned host memory and reads its outputs back. The
+    copies run on a second stream, double-buffered: step k+1's q goes up and
+    step k-1's outputs come down while step k computes."""
+    cfg = setup.cfg
     q_host = torch.empty((cfg.layers, cfg.B, cfg.Hq, cfg.D), dtype=torch.bfloat16,
                          pin_memory=True)
     for l in range(cfg.layers):
-        q_host[l].copy_(layers[l].q.cpu())
-    e2e_steps = max(3, args.steps // 2)
-    # Every step copies its q from pinned host memory and reads its outputs
-    # back. The copies run on a second stream, double-buffered: step k+1's q
-    # goes up and step k-1's outputs come down while step k computes.
+        q_host[l].copy_(setup.layers[l].q.cpu())
+    e2e_steps = max(3, steps // 2)
     q_dev = [torch.empty_like(q_host, device=dev) for _ in range(2)]
-    out_dev = [torch.empty_like(outs) for _ in range(2)]
-    out_host = [torch.empty(tuple(outs.shape), dtype=torch.float32, pin_memory=True)
+    out_dev = [torch.empty_like(setup.outs) for _ in range(2)]
+    out_host = [torch.empty(tuple(setup.outs.shape), dtype=torch.float32, pin_memory=True)
                 for _ in range(2)]
     copy_stream = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]    # q of buffer i is on the device
@@ -496,7 +686,7 @@ def run_ours(args, rank, world):
         stream.wait_event(ev_in[i])
         stream.wait_event(ev_out[i])     # step k-2's outputs have left out_dev[i]
         for l in range(cfg.layers):
-            call(l, q=q_dev[i][l], out=out_dev[i][l])
+            setup.call(l, stream, q=q_dev[i][l], out=out_dev[i][l])
         ev_done[i].record(stream)
         copy_stream.wait_event(ev_done[i])
         with torch.cuda.stream(copy_stream):
@@ -515,70 +705,9 @@ def run_ours(args, rank, world):
         e2e_step(k)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks((time.perf_counter() - h0) * 1e3 / e2e_steps, dist, dev)
-    e2e_value = job_rate(bytes_job, e2e_ms)
-
-    # ---- head-group size sweep (first layers of the same workload)
-    gsweep = None
-    if rank == 0 and not args.no_group_sweep:
-        gsweep = group_sweep(cfg, table, dev, stream, peak, kvx, torch)
-
-    sparse = None
-    if rank == 0 and not args.no_sparse:
-        sparse = sparse_select(dev, stream, peak, kvx, torch)
-
-    # ---- gather (KV-RM movement workload)
-    gather = None
-    if not args.no_gather:
-        del layers, plans
-        torch.cuda.empty_cache()
-        gather = bench_gather(args, dev, stream, peak, dist, world, rank)
-
-    cpu = None
-    ceiling = copy_ceiling(dev, stream, torch)
-    if rank == 0 and not args.no_cpu:
-        cpu = cpu_baseline(cfg, args.cpu_seconds)
-        cpu["host"] = host_cpu()
-        cpu["gather"] = cpu_gather_baseline()
-
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) bf16 K/V, fragmented page tables)",
-            "config": {"workload": describe(cfg),
-                       "l2": "inputs larger than L2: each step streams "
-                             f"{bytes_step / 1e9:.1f} GB of distinct KV pages",
-                       "plan": "balanced ahead-of-time split, two persistent blocks per SM",
-                       "sms": sms},
-            "frac_of_hbm": value / world / peak,
-            "seq_heads_per_s": world * cfg.B * cfg.Hq * cfg.layers / (ms_step * 1e-3),
-            "kv_bytes_per_step": bytes_job,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "traffic_note": "ncu dram read+write of the profiled layer-0 launch, scaled "
-                                         "to the mean launch by algorithmic bytes" if prof else
-                                         "kernel changed since the committed capture",
-                         "kernel": "attn_mma_kernel<128> (one launch per layer call)",
-                         "timing": "second pass of K steps, CUDA events around every launch",
-                         "peak_source": f"{peak_kind} hbm_gbs", "mean_call_us": 1e3 * mean_call_ms,
-                         "per_launch_gbs": rate_pct,
-                         "copy_ceiling_gbs": ceiling},
-            "e2e": {"value": e2e_value, "unit": "GB/s",
-                    "h2d_bytes_per_step": int(q_host.numel() * 2),
-                    "d2h_bytes_per_step": int(out_host[0].numel() * 4)},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk,
-            "plan_host_us_per_layer": float(np.mean(plan_us)),
-            "gather": gather,
-            "balance": balance,
-            "group_sweep": gsweep,
-            "sparse_select": sparse,
-            "cpu_baseline": cpu,
-        }
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    return {"value": job_rate(bytes_job, e2e_ms), "unit": "GB/s",
+            "h2d_bytes_per_step": int(q_host.numel() * 2),
+            "d2h_bytes_per_step": int(out_host[0].numel() * 4)}
 
 
 def measure_balance(cfg, lay, ws, stream, kvx, torch):
