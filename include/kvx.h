@@ -75,7 +75,8 @@ extern "C" {
 /* ---- work-split policies (kvx_plan_create) ---------------------------- */
 /* Ahead-of-time balanced split (Tangram, AOT Load Balancing): the kept tokens
  * of all heads are laid end to end and cut into num_ctas spans of equal cost;
- * a head cut across spans is split into partials merged by log-sum-exp. */
+ * a head cut across spans is split into partials merged by log-sum-exp
+ * through the workspace. */
 #define KVX_PLAN_BALANCED 0
 /* One thread block per (sequence, KV head); no split (naive baseline). */
 #define KVX_PLAN_PER_HEAD 1
@@ -83,6 +84,18 @@ extern "C" {
  * covers the GPU twice; one block per piece (the uniform split of Tangram
  * Fig. 4(c), whose stragglers the balanced plan removes). */
 #define KVX_PLAN_UNIFORM 2
+/* Cluster layout (tensor-core kernel only), thread-block clusters of 2, 4 or 8
+ * blocks on this GPU: every head is either whole on one block or cut into
+ * pieces on blocks of one cluster, at most one piece per block, run as that
+ * block's last item; the pieces are merged through distributed shared memory
+ * by the block of the head's first piece, with no workspace partials. The
+ * cost cap per block is the smallest with which that placement fits (heads
+ * placed longest first). num_ctas must be a multiple of the cluster size;
+ * 0 = as many clusters as can be resident on the current device.
+ * KVX_EUNSUPPORTED if no placement fits. */
+#define KVX_PLAN_CLUSTER_2 3
+#define KVX_PLAN_CLUSTER_4 4
+#define KVX_PLAN_CLUSTER_8 5
 
 /* ---- kernel choice ----------------------------------------------------- */
 #define KVX_KERNEL_AUTO 0 /* tensor-core kernel for bf16, CUDA-core kernel for fp32 */
@@ -138,7 +151,9 @@ typedef struct kvx_plan_stats {
   int32_t item_overhead;     /* tokens the balanced plan charges per item on top of
                                 its tokens (the per-item cost of query load,
                                 cross-warp merge and partial write) */
-  int32_t pad_;
+  int32_t cluster;           /* blocks per thread-block cluster of the launch
+                                (1: no clusters, split heads merged through the
+                                workspace) */
 } kvx_plan_stats;
 
 /* Text for a status code. Never NULL. */
@@ -165,10 +180,10 @@ int kvx_device_sm_count(int32_t *sms);
  *   head_group   int32 [Hkv], group of each KV head, in [0, num_groups); every
  *                group non-empty (host). Within a group, heads take page-slot
  *                rows 0, 1, ... in ascending head order.
- *   num_ctas     thread blocks for KVX_PLAN_BALANCED; 0 = as many as stay
- *                resident on the current device (2 per SM for the
- *                tensor-core kernel, 1 for the CUDA-core kernel); ignored by
- *                the other policies.
+ *   num_ctas     thread blocks for KVX_PLAN_BALANCED and KVX_PLAN_CLUSTER_*;
+ *                0 = as many as stay resident on the current device (2 per SM
+ *                for the tensor-core kernel, 1 for the CUDA-core kernel);
+ *                ignored by the other policies.
  *   policy       KVX_PLAN_*.   kernel  KVX_KERNEL_*.
  *   out          receives the plan (owned by the caller; kvx_plan_destroy).
  * Errors: KVX_EINVAL, KVX_EUNSUPPORTED, KVX_ENOMEM; *out is NULL on error.
@@ -282,7 +297,9 @@ void kvx_plan_destroy(kvx_plan *plan);
  * the stream. It may start while that kernel drains. It reads no input but
  * the plan's device copy until that kernel has completed, except that a plan
  * of short blocks prefetches its first K/V pages into L2, which changes no
- * data.
+ * data. The call may be captured into a CUDA graph once the plan has made
+ * one call on the device (that call sets the kernel's shared-memory limit);
+ * the graph keeps the pointers, strides and scale of the captured call.
  * Errors: KVX_EINVAL, KVX_ERANGE, KVX_ESTATE, KVX_ECUDA (nothing launched on
  * argument errors).
  * ------------------------------------------------------------------------- */

@@ -172,6 +172,7 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   p.P = P;
   p.num_groups = G;
   p.layout = s.layout;
+  p.cluster = plan->cluster;
   p.stall_block = plan->stall_block;
   p.wait_ns = plan->wait_ns;
   p.pf_tokens = plan->pf_tokens;

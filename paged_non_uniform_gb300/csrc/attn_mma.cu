@@ -77,7 +77,61 @@ struct Cfg {
   static constexpr int kMW = 8 * kMS + 16;            // floats per warp record
   static constexpr int kSmem =
       1024 + kStages * kStage + kMergeBufs * kCons * kMW * 4 + 2 * kStages * 8 + 16;
+  // a launch in clusters also keeps its inbox barrier (cluster merge), after
+  // the rest
+  static constexpr int kSmemCluster = kSmem + 16;
 };
+
+// Merge of a head whose pieces ran on blocks of one thread-block cluster
+// (distributed shared memory, this GPU only). Every piece's block has left
+// its merged (m, l, o) in its own ring, which is idle once its last item is
+// done: o [g][D] floats from offset 0, then (m, l) [g] float2 (obox, the same
+// offset in every block). The block of piece 0, once all others have arrived
+// on its inbox barrier, reads the pieces through the cluster's shared window
+// and folds them in piece order, as merge_split does for workspace partials.
+template <int D, int NT, int V>
+__device__ __forceinline__ void merge_cluster(const AttnParams &p, const SplitHead &sh, int tid,
+                                              uint32_t obox) {
+  const int g = p.g, cnt = sh.count, n4 = g * D / 4;
+  const int b = sh.bh / p.Hkv, h = sh.bh - b * p.Hkv;
+  float4 *out = reinterpret_cast<float4 *>(p.out + ((size_t)b * p.Hq + (size_t)h * g) * D);
+  const uint32_t ml_off = (uint32_t)(g * D * 4);
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int q4 = tid + k * NT;
+    if (q4 >= n4) continue;
+    const int qi = (4 * q4) / D;
+    float M = -INFINITY, L = 0.f;
+    float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j0 = 0; j0 < cnt; j0 += 4) {  // four pieces per round trip
+      float2 mv[4];
+      float4 ov[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j0 + j < cnt) {
+          const uint32_t base = mapa_shared(obox, (sh.ranks >> (4 * (j0 + j))) & 15u);
+          mv[j] = ld_cluster_f2(base + ml_off + 8u * qi);
+          ov[j] = ld_cluster_f4(base + 16u * q4);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j0 + j < cnt) {
+          const float mn = fmaxf(M, mv[j].x);
+          const float a = ex2(M - mn), f = ex2(mv[j].x - mn);
+          L = L * a + f * mv[j].y;
+          O.x = O.x * a + f * ov[j].x;
+          O.y = O.y * a + f * ov[j].y;
+          O.z = O.z * a + f * ov[j].z;
+          O.w = O.w * a + f * ov[j].w;
+          M = mn;
+        }
+      }
+    }
+    const float r = 1.f / L;
+    out[q4] = make_float4(O.x * r, O.y * r, O.z * r, O.w * r);
+  }
+}
 
 // Shared-memory layout of a stage's K (or V) tile: the stage's 32 tokens
 // come in boxes of `box_h` tokens (one bulk-tensor load each, box_h = min(P,
@@ -220,7 +274,10 @@ __device__ __forceinline__ void consume_stage(
 
 // VM: float4 groups of a head's g x D outputs that each consumer thread owns
 // in the split merge (one kernel per VM keeps a single merge inlined).
-template <int D, int VM>
+// kCluster: the launch runs in thread-block clusters and merges cluster heads
+// through distributed shared memory (a separate instance, so that launches
+// without clusters carry none of that code).
+template <int D, int VM, bool kCluster>
 __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     attn_mma_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D>;
@@ -232,6 +289,8 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   uint64_t *bars = (uint64_t *)(merge + kMergeBufs * kCons * C::kMW);
   volatile int *abort_flag = (volatile int *)(bars + 2 * kStages);
   volatile int *last_flag = abort_flag + 1;
+  // cluster merge: the head's other pieces have arrived (cluster instance only)
+  const uint32_t inbox = smem_u32(bars + 2 * kStages) + 16;
   const uint32_t stage0 = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
 
@@ -246,6 +305,17 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
+    // A block that merges a cluster head (it runs the head's piece 0 as its
+    // last item) waits on its inbox for the head's other pieces.
+    if (kCluster) {
+      uint32_t expect = 1;
+      if (it0 < it1) {
+        const Item last = p.items[it1 - 1];
+        if (last.mode == kMergeCluster && last.piece == 0)
+          expect = (uint32_t)max(1, p.split[last.split].count - 1);
+      }
+      mbar_init(inbox, expect);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -254,6 +324,12 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     prefetch_tensormap(&p.tmV[lane]);
   }
   __syncthreads();
+  // Cluster barrier, phase 0: no block touches another's shared memory before
+  // that block has initialised its barriers (every thread waits for this
+  // phase before its first remote access, at the latest before the final
+  // phase).
+  bool phase0_done = !kCluster;
+  if (kCluster) cluster_arrive();
   // Everything above touches only this block's shared memory and the kernel
   // parameters; global inputs may come from the previous kernel in the stream.
   if (warp == kCons - 1 && p.pf_tokens > 0) {
@@ -459,6 +535,8 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       }
       consumer_sync(kCons * 32);
       const int tid = threadIdx.x;
+      const bool in_cluster = kCluster && item.mode == kMergeCluster;
+      float *obox = (float *)smem;  // cluster merge: this piece's (m, l, o), in the idle ring
       for (int idx = tid; idx < g * D; idx += kCons * 32) {
         const int qi = idx / D, d = idx - qi * D;
         float M = -INFINITY;
@@ -471,7 +549,10 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
           Ls += f * buf[w * C::kMW + 8 * C::kMS + 8 + qi];
           O += f * buf[w * C::kMW + qi * C::kMS + d];
         }
-        if (item.slot < 0) {
+        if (in_cluster) {
+          obox[qi * D + d] = O;
+          if (d == 0) reinterpret_cast<float2 *>(obox + g * D)[qi] = make_float2(M, Ls);
+        } else if (item.slot < 0) {
           p.out[((size_t)b * p.Hq + (size_t)h * g + qi) * D + d] = O / Ls;
         } else {
           p.part_o[((size_t)item.slot * g + qi) * D + d] = O;
@@ -480,8 +561,39 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       }
       // one merge buffer: the next item may overwrite it only after every
       // consumer has read it (a split item's ticket syncs below do that)
-      if (kMergeBufs == 1 && item.slot < 0) consumer_sync(kCons * 32);
-      if (item.slot >= 0) {
+      if (kMergeBufs == 1 && item.slot < 0 && !in_cluster) consumer_sync(kCons * 32);
+      if constexpr (kCluster) {
+        if (in_cluster) {
+          // This piece is the block's last item. Piece 0's block merges the
+          // head; every other piece's block signals it once its (m, l, o) is
+          // in its ring, and keeps that memory (it only waits at the final
+          // cluster barrier, which the merging block passes after reading).
+          fence_acq_rel_cluster();
+          consumer_sync(kCons * 32);
+          if (!phase0_done) {
+            cluster_wait();
+            phase0_done = true;
+          }
+          const SplitHead sh = p.split[item.split];
+          // every rank the plan names must lie inside the cluster (never map
+          // one outside; a damaged plan is reported, not followed)
+          bool ranks_ok = sh.count >= 2 && sh.count <= 8;
+          for (int j = 0; j < sh.count && j < 8; ++j)
+            ranks_ok = ranks_ok && (int)((sh.ranks >> (4 * j)) & 15u) < p.cluster;
+          if (!ranks_ok) {
+            if (tid == 0) atomicOr(p.status, KVX_DEV_BAD_BUDGET);
+          } else if (item.piece != 0) {
+            if (tid == 0) mbar_arrive_remote(mapa_shared(inbox, sh.ranks & 15u));
+          } else {
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_cluster(inbox, 0, p.wait_ns));
+            if (ok)
+              merge_cluster<D, kCons * 32, VM>(p, sh, tid, smem_u32(obox));
+            else if (lane == 0)
+              atomicOr(p.status, KVX_DEV_TIMEOUT);
+          }
+        }
+      }
+      if (!in_cluster && item.slot >= 0) {
         // Publish this piece; the block that finishes the head's last piece
         // merges all of them and rearms the counter for the next call. After
         // the barrier, one thread's acquire-release ticket releases every
@@ -512,33 +624,83 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       tr[3] = tok;
     }
   }
+  // Final cluster barrier: no block leaves while a merging block of its
+  // cluster may still read its shared memory.
+  if constexpr (kCluster) {
+    if (!phase0_done) cluster_wait();
+    cluster_arrive();
+    cluster_wait();
+  }
 }
 
-template <int D, int VM>
-cudaError_t launch_dv(const AttnParams &p, int num_ctas, cudaStream_t st) {
+// Sets the kernel instance's shared-memory limit on the current device (once).
+template <int D, int VM, bool kCluster>
+cudaError_t configure_dv() {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, VM>,
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, VM, kCluster>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::kSmem);
+                                         (kCluster ? Cfg<D>::kSmemCluster : Cfg<D>::kSmem));
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
+  return cudaSuccess;
+}
+
+template <int D, int VM, bool kCluster>
+cudaError_t launch_dvc(const AttnParams &p, int num_ctas, cudaStream_t st) {
+  cudaError_t e = configure_dv<D, VM, kCluster>();
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
   cfg.blockDim = dim3((kCons + 1) * 32);
-  cfg.dynamicSmemBytes = Cfg<D>::kSmem;
+  cfg.dynamicSmemBytes = kCluster ? Cfg<D>::kSmemCluster : Cfg<D>::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, VM>, p);
+  if (kCluster) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
+  e = cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, VM, kCluster>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <int D, int VM>
+cudaError_t launch_dv(const AttnParams &p, int num_ctas, cudaStream_t st) {
+  return p.cluster > 1 ? launch_dvc<D, VM, true>(p, num_ctas, st)
+                       : launch_dvc<D, VM, false>(p, num_ctas, st);
+}
+
+template <int D, int VM>
+int max_clusters_dv(int cluster) {
+  if (configure_dv<D, VM, true>() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster);
+  cfg.blockDim = dim3((kCons + 1) * 32);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmemCluster;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, attn_mma_kernel<D, VM, true>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 template <int D>
@@ -555,9 +717,27 @@ cudaError_t launch_d(const AttnParams &p, int num_ctas, cudaStream_t st) {
   return cudaErrorInvalidValue;  // unreachable: g <= KVX_MAX_GQA
 }
 
+template <int D>
+int max_clusters_d(int g, int cluster) {
+  constexpr int NT = kCons * 32;
+  constexpr int VMAX = (KVX_MAX_GQA * D / 4 + NT - 1) / NT;
+  const int n4 = g * D / 4;
+  if (n4 <= NT) return max_clusters_dv<D, 1>(cluster);
+  if constexpr (VMAX >= 2) {
+    if (n4 <= 2 * NT) return max_clusters_dv<D, 2>(cluster);
+  }
+  if constexpr (VMAX >= 3) return max_clusters_dv<D, 3>(cluster);
+  return 0;
+}
+
 }  // namespace
 
 int attn_mma_ctas_per_sm() { return KVX_ATTN_CTAS_PER_SM; }
+
+int attn_mma_max_clusters(int D, int g, int cluster) {
+  if (cluster < 2 || cluster > 8 || g < 1 || g > KVX_MAX_GQA) return 0;
+  return D == 128 ? max_clusters_d<128>(g, cluster) : max_clusters_d<64>(g, cluster);
+}
 
 cudaError_t launch_attn_mma(const AttnParams &p, int num_ctas, cudaStream_t st) {
   if (num_ctas <= 0) return cudaSuccess;

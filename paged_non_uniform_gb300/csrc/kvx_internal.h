@@ -18,18 +18,29 @@ namespace kvx {
 // every supported page size up to 32, and two 16-row MMA tiles).
 constexpr int kStageTokens = 32;
 
-// One work item: tokens [begin, end) of head bh = b*Hkv + h. slot >= 0 names
-// the partial-result slot of a split head and split its index in the plan's
-// split-head list; slot < 0 means the item covers the whole head and writes
-// the final output.
+// How a split head's partials are merged.
+constexpr int kMergeGlobal = 0;   // partials in the workspace, last piece's block merges
+constexpr int kMergeCluster = 1;  // pieces on blocks of one cluster, merged through
+                                  // distributed shared memory by piece 0's block
+
+// One work item: tokens [begin, end) of head bh = b*Hkv + h. split >= 0
+// names the head's entry in the plan's split-head list. With a global merge,
+// slot >= 0 is the partial-result slot; slot < 0 means the item covers the
+// whole head and writes the final output. With a cluster merge, piece is the
+// item's index among the head's pieces (token order) and the item is the last
+// of its block.
 struct alignas(16) Item {
   int32_t bh, begin, end, slot;
-  int32_t split, pad0, pad1, pad2;
+  int32_t split, piece, mode, pad;
 };
 
-// A split head: its partials occupy slots [slot_begin, slot_begin + count).
+// A split head: count pieces. Global merge: partials in slots [slot_begin,
+// slot_begin + count). Cluster merge: piece i runs on the block of cluster
+// rank (ranks >> 4i) & 15 of the cluster (at most 8 pieces).
 struct SplitHead {
-  int32_t bh, slot_begin, count, pad;
+  int32_t bh, slot_begin, count, mode;
+  uint32_t ranks;
+  int32_t pad0, pad1, pad2;
 };
 
 struct GroupDesc {
@@ -77,6 +88,7 @@ struct alignas(128) AttnParams {
   int32_t cover_stride;
   int32_t B, Hq, Hkv, D, g, P, num_groups, layout;
   float scale_log2;            // scale * log2(e)
+  int32_t cluster;             // blocks per thread-block cluster (1: no clusters)
   int32_t stall_block;         // failure-detection test: block whose first stage gets no loads (-1: none)
   int32_t pf_tokens;           // tokens per block warmed into L2 before the dependency wait
   uint64_t wait_ns;            // limit of every pipeline wait
@@ -87,6 +99,9 @@ struct alignas(128) AttnParams {
 // Launchers (defined in the .cu files). Return cudaGetLastError().
 cudaError_t launch_attn_mma(const AttnParams &p, int num_ctas, cudaStream_t st);
 int attn_mma_ctas_per_sm();  // resident blocks per SM of the tensor-core kernel
+// Clusters of `cluster` blocks of the tensor-core kernel (head dim D, GQA g)
+// that can be resident at once on the current device; 0 if none or on error.
+int attn_mma_max_clusters(int D, int g, int cluster);
 cudaError_t launch_attn_simt(const AttnParams &p, int dtype, int num_ctas,
                              cudaStream_t st);
 
@@ -130,6 +145,7 @@ int set_cuda_error(cudaError_t e);  // records e for kvx_last_cuda_error
 struct kvx_plan {
   kvx_shape shape;
   int32_t policy, kernel, num_ctas;
+  int32_t cluster;                   // blocks per cluster (1: no clusters)
   std::vector<int32_t> n;            // [B*Hkv]
   std::vector<int32_t> head_group;   // [Hkv]
   std::vector<int32_t> head_row;     // [Hkv]

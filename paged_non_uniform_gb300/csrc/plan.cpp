@@ -38,7 +38,7 @@ static void finish_splits(kvx_plan *p) {
     if (count[bh] > 1) {
       first[bh] = slots;
       split_of[bh] = (int32_t)p->split_heads.size();
-      p->split_heads.push_back(SplitHead{bh, slots, count[bh], 0});
+      p->split_heads.push_back(SplitHead{bh, slots, count[bh], kMergeGlobal, 0u, 0, 0, 0});
       slots += count[bh];
     }
   }
@@ -140,6 +140,158 @@ static void plan_balanced(kvx_plan *p, int num_ctas) {
   }
 }
 
+// ---- cluster layout --------------------------------------------------------
+// Every head is either whole on one block or cut into pieces on blocks of one
+// cluster of C blocks; a block holds at most one such piece and runs it last,
+// so that its pieces can be merged through distributed shared memory when the
+// block has nothing else to do. Heads are placed longest first: whole on the
+// least loaded block where it fits under the cost cap, else cut, at stage
+// boundaries, over the free blocks of the cluster with the most room (largest
+// room first). Returns false if that does not fit under the cap.
+struct ClusterFill {
+  std::vector<std::vector<Item>> whole;  // per block
+  std::vector<Item> piece;               // per block; bh < 0: none
+};
+
+static bool fill_cluster(const kvx_plan *p, const std::vector<int> &order, int C, int K,
+                         double cap, double c0, ClusterFill *out) {
+  const int T = kStageTokens, NB = K * C;
+  std::vector<double> used(NB, 0.0);
+  std::vector<char> has_piece(NB, 0);
+  std::vector<std::pair<int64_t, int>> room;
+  if (out) {
+    out->whole.assign(NB, {});
+    out->piece.assign(NB, Item{-1, 0, 0, -1, -1, 0, kMergeGlobal, 0});
+  }
+  for (int bh : order) {
+    const int n = p->n[bh];
+    int best = -1;
+    for (int c = 0; c < NB; ++c)
+      if (cap - used[c] >= n + c0 && (best < 0 || used[c] < used[best])) best = c;
+    if (best >= 0) {
+      used[best] += n + c0;
+      if (out) out->whole[best].push_back(Item{bh, 0, n, -1, -1, 0, kMergeGlobal, 0});
+      continue;
+    }
+    int bk = -1;
+    int64_t bk_room = -1;
+    for (int k = 0; k < K; ++k) {
+      int64_t r = 0;
+      for (int j = 0; j < C; ++j) {
+        const int c = k * C + j;
+        const double left = cap - used[c] - c0;
+        if (!has_piece[c] && left >= T) r += (int64_t)std::floor(left / T) * T;
+      }
+      if (r > bk_room) {
+        bk_room = r;
+        bk = k;
+      }
+    }
+    if (bk < 0 || bk_room < n) return false;
+    room.clear();
+    for (int j = 0; j < C; ++j) {
+      const int c = bk * C + j;
+      const double left = cap - used[c] - c0;
+      if (!has_piece[c] && left >= T) room.push_back({(int64_t)std::floor(left / T) * T, c});
+    }
+    std::stable_sort(room.begin(), room.end(),
+                     [](const std::pair<int64_t, int> &a, const std::pair<int64_t, int> &b) {
+                       return a.first > b.first;
+                     });
+    int pos = 0;
+    for (const auto &rc : room) {
+      if (pos >= n) break;
+      const int k = (int)std::min<int64_t>(rc.first, n - pos);
+      has_piece[rc.second] = 1;
+      used[rc.second] += k + c0;
+      if (out) out->piece[rc.second] = Item{bh, pos, pos + k, -1, -1, 0, kMergeCluster, 0};
+      pos += k;
+    }
+  }
+  return true;
+}
+
+// Cluster layout on num_ctas blocks (a multiple of C): the smallest cost cap
+// (to a token) with which fill_cluster succeeds. Each block runs its whole
+// heads, then its piece. Returns false if no cap works.
+static bool plan_cluster(kvx_plan *p, int C, int num_ctas) {
+  const int K = num_ctas / C, H = p->shape.B * p->shape.Hkv;
+  if (K < 1 || C < 2 || C > 8) return false;
+  const double c0 = item_overhead_tokens();
+  std::vector<int> order(H);
+  double total = 0;
+  for (int bh = 0; bh < H; ++bh) {
+    order[bh] = bh;
+    total += p->n[bh] + c0;
+  }
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return p->n[a] > p->n[b]; });
+  double lo = std::max(total / (K * C), c0 + kStageTokens), hi = lo;
+  for (int guard = 0; !fill_cluster(p, order, C, K, hi, c0, nullptr); ++guard) {
+    if (guard > 400) return false;
+    hi += std::max(c0 + kStageTokens, 0.125 * hi);
+  }
+  while (hi - lo > 1.0) {
+    const double mid = 0.5 * (lo + hi);
+    if (fill_cluster(p, order, C, K, mid, c0, nullptr))
+      hi = mid;
+    else
+      lo = mid;
+  }
+  ClusterFill f;
+  fill_cluster(p, order, C, K, hi, c0, &f);
+  p->items.clear();
+  p->cta_off.assign(1, 0);
+  for (int c = 0; c < K * C; ++c) {
+    for (const Item &it : f.whole[c]) p->items.push_back(it);
+    if (f.piece[c].bh >= 0) p->items.push_back(f.piece[c]);
+    p->cta_off.push_back((int32_t)p->items.size());
+  }
+  p->num_ctas = K * C;
+  p->cluster = C;
+  return true;
+}
+
+// Split-head records of a cluster layout: piece index in token order, the
+// cluster rank of each piece's block; no workspace slots.
+static void finish_cluster_splits(kvx_plan *p) {
+  const int H = p->shape.B * p->shape.Hkv, C = p->cluster;
+  std::vector<int32_t> count(H, 0);
+  for (const Item &it : p->items) count[it.bh]++;
+  std::vector<int32_t> split_of(H, -1);
+  std::vector<std::vector<std::pair<int32_t, int32_t>>> pieces(H);  // (begin, item index)
+  for (size_t i = 0; i < p->items.size(); ++i)
+    if (count[p->items[i].bh] > 1) pieces[p->items[i].bh].push_back({p->items[i].begin, (int)i});
+  std::vector<int32_t> cta_of(p->items.size());
+  for (int c = 0; c < p->num_ctas; ++c)
+    for (int i = p->cta_off[c]; i < p->cta_off[c + 1]; ++i) cta_of[i] = c;
+  for (int bh = 0; bh < H; ++bh) {
+    if (count[bh] < 2) continue;
+    std::sort(pieces[bh].begin(), pieces[bh].end());
+    uint32_t ranks = 0;
+    for (size_t k = 0; k < pieces[bh].size(); ++k) {
+      Item &it = p->items[pieces[bh][k].second];
+      it.piece = (int32_t)k;
+      it.split = (int32_t)p->split_heads.size();
+      it.slot = -1;
+      it.mode = kMergeCluster;
+      ranks |= (uint32_t)(cta_of[pieces[bh][k].second] % C) << (4 * k);
+    }
+    p->split_heads.push_back(SplitHead{bh, -1, count[bh], kMergeCluster, ranks, 0, 0, 0});
+  }
+  for (Item &it : p->items)
+    if (count[it.bh] < 2) {  // a head left in one piece is a whole head
+      it.mode = kMergeGlobal;
+      it.slot = -1;
+      it.split = -1;
+      it.piece = 0;
+    }
+  p->num_slots = 0;
+  p->cta_tokens.assign(p->num_ctas, 0);
+  for (int c = 0; c < p->num_ctas; ++c)
+    for (int i = p->cta_off[c]; i < p->cta_off[c + 1]; ++i)
+      p->cta_tokens[c] += p->items[i].end - p->items[i].begin;
+}
+
 // One block per head, no split.
 static void plan_per_head(kvx_plan *p) {
   const int H = p->shape.B * p->shape.Hkv;
@@ -207,7 +359,7 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
   if (s->dtype != KVX_F32 && s->dtype != KVX_BF16) return KVX_EUNSUPPORTED;
   if (s->layout != KVX_LAYOUT_HEAD_MAJOR && s->layout != KVX_LAYOUT_TOKEN_MAJOR)
     return KVX_EUNSUPPORTED;
-  if (policy < KVX_PLAN_BALANCED || policy > KVX_PLAN_UNIFORM)
+  if (policy < KVX_PLAN_BALANCED || policy > KVX_PLAN_CLUSTER_8)
     return KVX_EINVAL;
   if (kernel < KVX_KERNEL_AUTO || kernel > KVX_KERNEL_SIMT) return KVX_EINVAL;
   int resolved = kernel;
@@ -216,6 +368,14 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
   if (resolved == KVX_KERNEL_MMA && s->dtype != KVX_BF16)
     return KVX_EUNSUPPORTED;
   if (num_ctas < 0) return KVX_EINVAL;
+  const int cluster_req = policy == KVX_PLAN_CLUSTER_2   ? 2
+                          : policy == KVX_PLAN_CLUSTER_4 ? 4
+                          : policy == KVX_PLAN_CLUSTER_8 ? 8
+                                                         : 1;
+  if (cluster_req > 1) {
+    if (resolved != KVX_KERNEL_MMA) return KVX_EUNSUPPORTED;
+    if (num_ctas % cluster_req != 0) return KVX_EINVAL;
+  }
 
   const int B = s->B, Hkv = s->Hkv, G = s->num_groups, P = s->page_size;
   for (int h = 0; h < Hkv; ++h)
@@ -226,7 +386,7 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
     if (head_budget[i] < 1) return KVX_EINVAL;
 
   int sms = 0;
-  if ((policy == KVX_PLAN_BALANCED && num_ctas == 0) ||
+  if (((policy == KVX_PLAN_BALANCED || cluster_req > 1) && num_ctas == 0) ||
       policy == KVX_PLAN_UNIFORM) {
     if (num_ctas > 0) {
       sms = num_ctas;
@@ -243,6 +403,7 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
     p->policy = policy;
     p->kernel = resolved;
     p->num_ctas = 0;
+    p->cluster = 1;
     p->num_slots = 0;
     p->d_buf = nullptr;
     p->d_items = nullptr;
@@ -277,15 +438,27 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
         int32_t &pg = p->group_pages[(size_t)head_group[h] * B + b];
         pg = std::max(pg, (p->n[(size_t)b * Hkv + h] + P - 1) / P);
       }
-    if (policy == KVX_PLAN_BALANCED)
-      plan_balanced(p, num_ctas > 0
-                           ? num_ctas
-                           : sms * (resolved == KVX_KERNEL_MMA ? attn_mma_ctas_per_sm() : 1));
-    else if (policy == KVX_PLAN_PER_HEAD)
-      plan_per_head(p);
-    else
-      plan_uniform(p, sms);
-    finish_splits(p);
+    const int g = s->Hq / s->Hkv;
+    const int resident = sms * (resolved == KVX_KERNEL_MMA ? attn_mma_ctas_per_sm() : 1);
+    if (policy == KVX_PLAN_BALANCED) {
+      plan_balanced(p, num_ctas > 0 ? num_ctas : resident);
+      finish_splits(p);
+    } else if (cluster_req > 1) {
+      int nb = num_ctas;
+      if (nb == 0) nb = std::min(attn_mma_max_clusters(s->D, g, cluster_req),
+                                 resident / cluster_req) * cluster_req;
+      if (nb < cluster_req || !plan_cluster(p, cluster_req, nb)) {
+        delete p;
+        return KVX_EUNSUPPORTED;
+      }
+      finish_cluster_splits(p);
+    } else {
+      if (policy == KVX_PLAN_PER_HEAD)
+        plan_per_head(p);
+      else
+        plan_uniform(p, sms);
+      finish_splits(p);
+    }
     // L2 warm-up amount (short launches only)
     int64_t total = 0;
     for (int64_t v : p->cta_tokens) total += v;
@@ -385,7 +558,7 @@ extern "C" int kvx_plan_get_stats(const kvx_plan *p, kvx_plan_stats *st) {
       alloc += (int64_t)p->group_pages[(size_t)gi * B + b] * p->group_size[gi] * P;
   st->slots_allocated = alloc;
   st->item_overhead = item_overhead_tokens();
-  st->pad_ = 0;
+  st->cluster = p->cluster;
   st->slots_used = tot;
   st->plan_us = p->plan_us;
   return KVX_OK;

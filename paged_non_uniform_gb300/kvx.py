@@ -40,6 +40,9 @@ KVX_BF16 = 1
 KVX_PLAN_BALANCED = 0
 KVX_PLAN_PER_HEAD = 1
 KVX_PLAN_UNIFORM = 2
+KVX_PLAN_CLUSTER_2 = 3
+KVX_PLAN_CLUSTER_4 = 4
+KVX_PLAN_CLUSTER_8 = 5
 KVX_KERNEL_AUTO = 0
 KVX_KERNEL_MMA = 1
 KVX_KERNEL_SIMT = 2
@@ -78,7 +81,7 @@ class kvx_plan_stats(_c.Structure):
                 ("total_tokens", _c.c_int64), ("max_cta_tokens", _c.c_int64),
                 ("mean_cta_tokens", _c.c_double), ("slots_allocated", _c.c_int64),
                 ("slots_used", _c.c_int64), ("plan_us", _c.c_double),
-                ("item_overhead", _c.c_int32), ("pad_", _c.c_int32)]
+                ("item_overhead", _c.c_int32), ("cluster", _c.c_int32)]
 
 
 lib.kvx_status_string.restype = _c.c_char_p

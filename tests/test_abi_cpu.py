@@ -310,3 +310,84 @@ def test_coverage_record_stride_is_checked(kvx):
     assert e.value.status == kvx.KVX_ERANGE
     plan.set_coverage_record(1 << 20, 100)
     plan.set_coverage_record(None)
+
+
+CLUSTER_POLICIES = {2: 3, 4: 4, 8: 5}  # cluster size -> KVX_PLAN_CLUSTER_*
+
+
+def check_cluster_plan(orc, plan, n, C, num_ctas):
+    """Structure of a cluster layout: exact coverage (oracle count array); a
+    cut head's pieces lie on blocks of one cluster, at most C of them, each
+    the last item of its block and at most one per block; cuts fall on stage
+    boundaries except at a head's end."""
+    items, off = plan.items()
+    assert len(off) == num_ctas + 1 and off[-1] == len(items)
+    bad, count = orc.plan_coverage(n, items)
+    assert bad == 0
+    assert np.array_equal(plan.coverage(), count)
+    assert plan.stats()["cluster"] == C and plan.stats()["num_slots"] == 0
+    cta_of = np.repeat(np.arange(num_ctas), np.diff(off))
+    pieces = np.bincount(items[:, 0], minlength=n.size)
+    is_last = np.zeros(len(items), bool)
+    is_last[off[1:][np.diff(off) > 0] - 1] = True
+    per_block = np.zeros(num_ctas, int)
+    for i, (bh, b, e, slot) in enumerate(items):
+        assert slot == -1
+        if pieces[bh] > 1:
+            assert is_last[i], (bh, i)
+            per_block[cta_of[i]] += 1
+            assert b % 32 == 0 and (e % 32 == 0 or e == n[bh]), (bh, b, e)
+    assert per_block.max(initial=0) <= 1
+    for bh in np.flatnonzero(pieces > 1):
+        blocks = cta_of[items[:, 0] == bh]
+        assert 2 <= blocks.size <= C
+        assert len(set((blocks // C).tolist())) == 1, (bh, blocks)
+    return items, off, pieces
+
+
+@pytest.mark.parametrize("C", [2, 4, 8])
+def test_cluster_layout_on_the_sparse_workload(kvx, orc, C):
+    """Llama-3-8B sparse layer (64 heads of 2176 kept tokens) on 304 blocks:
+    every head is cut inside one cluster; with clusters of 4 or 8 every block
+    of a used cluster streams 544 tokens (one head per four blocks)."""
+    cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
+    plan = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
+                               kvx.KVX_BF16, cfg.budget[0], cfg.seq_len, cfg.head_group[0],
+                               304, CLUSTER_POLICIES[C])
+    n = cfg.n[0].reshape(-1)
+    items, off, pieces = check_cluster_plan(orc, plan, n, C, 304)
+    assert np.all(pieces > 1)
+    if C >= 4:
+        assert plan.stats()["max_cta_tokens"] == 544
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_cluster_layout_random_shapes(kvx, orc, seed):
+    """Seeded random shapes, budgets and block counts under every cluster
+    size: the layout's structure and exact coverage."""
+    g = np.random.default_rng(5000 + seed)
+    C = int(g.choice([2, 4, 8]))
+    Hkv = int(g.choice([1, 2, 4, 8]))
+    B = int(g.integers(1, 9))
+    L = g.integers(1, 9001, size=B).astype(np.int32)
+    budget = g.integers(1, 12001, size=(B, Hkv)).astype(np.int32)
+    G = int(g.integers(1, min(Hkv, 3) + 1))
+    hg = np.concatenate([np.arange(G), g.integers(0, G, size=Hkv - G)]).astype(np.int32)
+    num_ctas = C * int(g.integers(1, 40))
+    plan = kvx.kvx_plan_create(B, 4 * Hkv, Hkv, 128, 16, G, kvx.KVX_BF16, budget, L, hg,
+                               num_ctas, CLUSTER_POLICIES[C])
+    n = orc.resolve_budget(budget, L).reshape(-1)
+    check_cluster_plan(orc, plan, n, C, num_ctas)
+
+
+def test_cluster_layout_rejects_bad_arguments(kvx):
+    case = synth.tiny(0)
+    for num_ctas, kernel, want in ((6, 0, kvx.KVX_EINVAL),   # not a multiple of 4 (fp32: SIMT)
+                                   (8, 0, kvx.KVX_EUNSUPPORTED)):  # fp32 runs on the SIMT kernel
+        with pytest.raises(kvx.KvxError) as e:
+            _plan(kvx, case, num_ctas=num_ctas, policy=kvx.KVX_PLAN_CLUSTER_4, kernel=kernel)
+        assert e.value.status in (want, kvx.KVX_EUNSUPPORTED)
+    bf = synth.dense_case(2, 8, 2, 64, [37, 100], [[37, 20], [100, 20]], "bf16", seed=0)
+    with pytest.raises(kvx.KvxError) as e:
+        _plan(kvx, bf, num_ctas=6, policy=kvx.KVX_PLAN_CLUSTER_4)
+    assert e.value.status == kvx.KVX_EINVAL

@@ -210,6 +210,33 @@ def test_repeated_calls_and_shared_workspace(kernel):
     assert max_abs(first_b, oracle_out(b_case)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("kernel", [kvx.KVX_KERNEL_MMA, kvx.KVX_KERNEL_SIMT])
+def test_calls_captured_in_a_cuda_graph_replay_bit_exact(kernel):
+    """Several layers' calls captured in one CUDA graph (after a first direct
+    call per plan) replay to the same bits as direct calls, every replay."""
+    cases = [qwen3_like(21), qwen25_like(22), sparse_like(23)]
+    devs = [DeviceCase(c, make_plan(c, num_ctas=n, kernel=kernel))
+            for c, n in zip(cases, (17, 0, 40))]
+    direct = [d.run() for d in devs]
+    outs = [torch.full_like(d.out, float("nan")) for d in devs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = torch.cuda.current_stream()
+        for d, o in zip(devs, outs):
+            kvx.kvx_decode_attn(d.plan, d.q, d.k_pools, d.v_pools, d.pool_pages, d.pt,
+                                d.strides, d.budget, d.seq_len, 0.0, o, d.ws, stream=st)
+    for _ in range(3):
+        for o in outs:
+            o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for ref, o, d in zip(direct, outs, devs):
+            assert d.status() == 0
+            assert np.array_equal(o.cpu().numpy().astype(np.float64), ref)
+    for ref, c in zip(direct, cases):
+        assert max_abs(ref, oracle_out(c)) <= TOL_BF16
+
+
 def test_pipeline_wait_runs_out_and_is_reported():
     """Failure detection without a GPU fault: one block's first stage is armed
     but never loaded, so its wait runs out after 50 ms. The call must return
