@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--no-group-sweep", action="store_true")
     ap.add_argument("--no-sparse", action="store_true")
     ap.add_argument("--no-workloads", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="decode only the first N layers of the workload (profiling "
+                         "captures); 0 = all")
     ap.add_argument("--cpu-seconds", type=float, default=3.0,
                     help="oracle time per workload in the CPU baseline")
     return ap.parse_args()
@@ -564,7 +567,7 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
     peak, peak_kind = peaks()
 
-    cfg = synth.decode_config(args.workload, seed=rank_seed(rank))
+    cfg = synth.decode_config(args.workload, seed=rank_seed(rank), layers=args.layers or None)
     tables = {}
 
     def table_for(c):

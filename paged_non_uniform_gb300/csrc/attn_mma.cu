@@ -67,6 +67,7 @@ static_assert(kMergeBufs == 1 || kMergeBufs == 2, "one or two merge buffers");
 // k of a slot while another warp's phase k-1 is still loading; a parity wait
 // cannot tell those phases apart and would pass early.
 static_assert(kStages % kCons == 0, "each ring slot must belong to one consumer warp");
+static_assert(kCons <= 3, "the cross-warp merge keeps one weight per warp in a row's 4 padding floats");
 
 template <int D>
 struct Cfg {
@@ -537,26 +538,51 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       const int tid = threadIdx.x;
       const bool in_cluster = kCluster && item.mode == kMergeCluster;
       float *obox = (float *)smem;  // cluster merge: this piece's (m, l, o), in the idle ring
-      for (int idx = tid; idx < g * D; idx += kCons * 32) {
-        const int qi = idx / D, d = idx - qi * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kCons; ++w) M = fmaxf(M, buf[w * C::kMW + 8 * C::kMS + qi]);
-        float Ls = 0.f, O = 0.f;
+      // Per query row, once: each warp's weight 2^(m_w - M) and the row's
+      // 1 / sum, kept in the padding columns of warp 0's row.
+      if (tid < g) {
+        const int qi = tid;
+        float M = -INFINITY, mw_[kCons];
 #pragma unroll
         for (int w = 0; w < kCons; ++w) {
-          const float f = ex2(buf[w * C::kMW + 8 * C::kMS + qi] - M);
+          mw_[w] = buf[w * C::kMW + 8 * C::kMS + qi];
+          M = fmaxf(M, mw_[w]);
+        }
+        float Ls = 0.f;
+        float *rf = buf + qi * C::kMS + D;
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) {
+          const float f = ex2(mw_[w] - M);
+          rf[w] = f;
           Ls += f * buf[w * C::kMW + 8 * C::kMS + 8 + qi];
-          O += f * buf[w * C::kMW + qi * C::kMS + d];
+        }
+        rf[3] = 1.f / Ls;
+        if (in_cluster)
+          reinterpret_cast<float2 *>(obox + g * D)[qi] = make_float2(M, Ls);
+        else if (item.slot >= 0)
+          p.part_ml[(size_t)item.slot * g + qi] = make_float2(M, Ls);
+      }
+      consumer_sync(kCons * 32);
+      for (int q4 = tid; q4 < g * D / 4; q4 += kCons * 32) {
+        const int qi = (4 * q4) / D, d4 = 4 * q4 - qi * D;
+        const float4 rf = *reinterpret_cast<const float4 *>(buf + qi * C::kMS + D);
+        const float fw[3] = {rf.x, rf.y, rf.z};
+        float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < kCons; ++w) {
+          const float4 v = *reinterpret_cast<const float4 *>(buf + w * C::kMW + qi * C::kMS + d4);
+          O.x = fmaf(fw[w], v.x, O.x);
+          O.y = fmaf(fw[w], v.y, O.y);
+          O.z = fmaf(fw[w], v.z, O.z);
+          O.w = fmaf(fw[w], v.w, O.w);
         }
         if (in_cluster) {
-          obox[qi * D + d] = O;
-          if (d == 0) reinterpret_cast<float2 *>(obox + g * D)[qi] = make_float2(M, Ls);
+          *reinterpret_cast<float4 *>(obox + qi * D + d4) = O;
         } else if (item.slot < 0) {
-          p.out[((size_t)b * p.Hq + (size_t)h * g + qi) * D + d] = O / Ls;
+          *reinterpret_cast<float4 *>(p.out + ((size_t)b * p.Hq + (size_t)h * g + qi) * D + d4) =
+              make_float4(O.x * rf.w, O.y * rf.w, O.z * rf.w, O.w * rf.w);
         } else {
-          p.part_o[((size_t)item.slot * g + qi) * D + d] = O;
-          if (d == 0) p.part_ml[(size_t)item.slot * g + qi] = make_float2(M, Ls);
+          *reinterpret_cast<float4 *>(p.part_o + ((size_t)item.slot * g + qi) * D + d4) = O;
         }
       }
       // one merge buffer: the next item may overwrite it only after every

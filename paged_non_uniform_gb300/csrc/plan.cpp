@@ -22,11 +22,16 @@ int set_cuda_error(cudaError_t e);  // abi.cpp
 // load, the cross-warp merge and the partial write of an item take about as
 // long as streaming this many tokens.
 #ifndef KVX_ITEM_OVERHEAD_TOKENS
-#define KVX_ITEM_OVERHEAD_TOKENS 160
+#define KVX_ITEM_OVERHEAD_TOKENS 128
 #endif
 static int item_overhead_tokens() { return KVX_ITEM_OVERHEAD_TOKENS; }
 
 static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// Granularity of the balanced plan's cuts: a piece of a head may start at
+// any multiple of min(P, stage) tokens, because the attention kernels fetch a
+// stage as boxes of min(P, stage) rows that never cross a page.
+static int cut_tokens(const kvx_plan *p) { return std::min(p->shape.page_size, kStageTokens); }
 
 static void finish_splits(kvx_plan *p) {
   const int H = p->shape.B * p->shape.Hkv;
@@ -69,12 +74,12 @@ static void finish_splits(kvx_plan *p) {
 }
 
 // Greedy fill of `heads` (in order) into blocks of cost at most `cap` each
-// (tokens + c0 per item; a head's last sliver under one stage may pass the
-// cap), cutting at stage boundaries; returns the number of blocks used, or
+// (tokens + c0 per item; a head's last sliver under one cut may pass the
+// cap), cutting at multiples of cut_tokens; returns the number of blocks used, or
 // max_ctas + 1 if they do not suffice (out is then partial).
 static int fill_blocks(const kvx_plan *p, const std::vector<int> &heads, double cap, double c0,
                        int max_ctas, std::vector<std::vector<Item>> *out) {
-  const int T = kStageTokens;
+  const int T = cut_tokens(p);
   int c = 0;
   double used = 0;
   if (out) out->assign(max_ctas, {});
@@ -110,7 +115,7 @@ static int fill_blocks(const kvx_plan *p, const std::vector<int> &heads, double 
 
 // Balanced: lay the heads' kept tokens end to end, charge each item its
 // tokens plus a fixed overhead, and cut the stream into at most num_ctas
-// blocks whose cost is at most a common cap, at stage boundaries; the cap is
+// blocks whose cost is at most a common cap, at multiples of cut_tokens; the cap is
 // the smallest (to a token) with which the stream fits.
 static void plan_balanced(kvx_plan *p, int num_ctas) {
   const int H = p->shape.B * p->shape.Hkv;
@@ -121,7 +126,7 @@ static void plan_balanced(kvx_plan *p, int num_ctas) {
     heads[bh] = bh;
     total += p->n[bh] + c0;
   }
-  double lo = std::max(total / num_ctas, c0 + kStageTokens), hi = lo;
+  double lo = std::max(total / num_ctas, c0 + cut_tokens(p)), hi = lo;
   while (fill_blocks(p, heads, hi, c0, num_ctas, nullptr) > num_ctas) hi += c0 + kStageTokens;
   while (hi - lo > 1.0) {
     const double mid = 0.5 * (lo + hi);

@@ -87,8 +87,8 @@ def test_plan_coverage_matches_oracle(kvx, orc, name, policy, num_ctas):
     assert np.all(items[~split, 3] == -1)
     slots = items[split, 3]
     assert sorted(slots.tolist()) == list(range(st["num_slots"]))
-    # items start on stage boundaries (32 tokens)
-    assert np.all(items[:, 1] % 32 == 0)
+    # items start at multiples of the cut granularity, min(P, 32) tokens
+    assert np.all(items[:, 1] % min(case.P, 32) == 0)
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
@@ -221,11 +221,11 @@ def test_select_and_pack_reject_bad_arguments(kvx):
 @pytest.mark.parametrize("num_ctas", [152, 304, 1000])
 def test_balanced_plan_cap(kvx, name, num_ctas):
     """Every block of the balanced plan costs (tokens + item charge per item)
-    at most one item charge plus two stages above the ideal share (stage
-    rounding and the no-sliver rule leave less than a stage each, and a block
-    may close one item short); pieces are
-    whole stages except a head's last piece; at most one head is cut at each
-    block boundary."""
+    at most one item charge plus two stages above the ideal share (cut
+    rounding and the no-sliver rule leave less than a cut each, and a block
+    may close one item short); pieces are whole multiples of the cut
+    granularity min(P, 32) except a head's last piece; at most one head is
+    cut at each block boundary."""
     cfg = synth.decode_config(name, seed=0, layers=1)
     plan = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups,
                                kvx.KVX_BF16, cfg.budget[0], cfg.seq_len, cfg.head_group[0],
@@ -240,8 +240,9 @@ def test_balanced_plan_cap(kvx, name, num_ctas):
     # boundary (where a head can be cut)
     ideal = (int(n.sum()) + c0 * n.size + c0 * (num_ctas - 1)) / num_ctas
     assert max(cost) <= ideal + c0 + 2 * 32 + 1, (max(cost), ideal)
+    T = min(cfg.P, 32)  # cut granularity
     for bh, b, e in items[:, :3]:
-        assert b % 32 == 0 and (e % 32 == 0 or e == n[bh]), (bh, b, e)
+        assert b % T == 0 and (e % T == 0 or e == n[bh]), (bh, b, e)
     # a head cut across blocks: its pieces sit in consecutive blocks
     cta_of = np.repeat(np.arange(num_ctas), np.diff(off))
     for bh in np.unique(items[:, 0]):
@@ -254,10 +255,11 @@ def test_balanced_plan_random_shapes(kvx, orc, seed):
     """Seeded random shapes, budgets, groupings and block counts, down to
     heads shorter than a stage and more blocks than stages. The balanced plan
     covers every kept token once (oracle count array) and resolves budgets as
-    the oracle does. Pieces are whole stages except a head's last. A cut
-    head's pieces sit in consecutive blocks and run before the block's whole
-    heads. No block costs more than one item charge plus two stages above
-    the ideal share. Every piece of a cut head holds at least one stage.
+    the oracle does. Pieces are whole cuts (min(P, 32) tokens) except a head's
+    last. A cut head's pieces sit in consecutive blocks and run before the
+    block's whole heads. No block costs more than one item charge plus two
+    stages above the ideal share. Every piece of a cut head holds at least
+    one cut.
     """
     g = np.random.default_rng(1000 + seed)
     Hkv = int(g.choice([1, 2, 3, 4, 8]))
@@ -279,7 +281,7 @@ def test_balanced_plan_random_shapes(kvx, orc, seed):
     bad, count = orc.plan_coverage(n, items)
     assert bad == 0
     assert np.array_equal(plan.coverage(), count)
-    T, c0 = 32, plan.stats()["item_overhead"]
+    T, c0 = min(P, 32), plan.stats()["item_overhead"]  # cut granularity, item charge
     for bh, b, e in items[:, :3]:
         assert b % T == 0 and (e % T == 0 or e == n[bh]), (bh, b, e)
     pieces = np.bincount(items[:, 0], minlength=n.size)
@@ -287,7 +289,7 @@ def test_balanced_plan_random_shapes(kvx, orc, seed):
     for bh in np.flatnonzero(pieces > 1):
         mine = items[:, 0] == bh
         assert np.all(np.diff(np.sort(cta_of[mine])) == 1), bh
-        # no sliver: every piece of a cut head holds at least one stage
+        # no sliver: every piece of a cut head holds at least one cut
         assert np.all(items[mine, 2] - items[mine, 1] >= T), (bh, items[mine])
     cost = []
     for c in range(num_ctas):
