@@ -484,15 +484,18 @@ int kvx_frame_get_stats(const kvx_frame *frame, kvx_frame_stats *out);
  *               are set to -1.
  *   kept_count  device int32 [B*Hkv].
  *   workspace   device, >= kvx_select_workspace_bytes(B, Hkv, Lmax), 256-byte
- *               aligned (holds the scores, a per-head histogram and bucket
- *               count, which the call clears on `stream` first, and per head a
- *               list of up to 8192 candidates near the cut and a bitmask).
+ *               aligned (holds the scores, the first digit of the largest
+ *               score of every 8 positions and a per-head histogram, which
+ *               the call clears on `stream` first).
  * The cut is decided on fp32 scores: positions whose scores lie within fp32
  * rounding of the cut may be exchanged with respect to an exact selection.
- * Launch: a memset of the workspace's counters, the score pass, then the
- * bucket and top-k passes. The last two are programmatic dependents of the
- * pass before them, which they wait for on the device before reading its
- * results.
+ * Launch: a kernel that clears the histograms; the score pass, a
+ * programmatic dependent of it that waits only before adding its counts;
+ * then the cut pass, a programmatic dependent of the score pass that waits
+ * for it on the device: one thread-block cluster of 4 blocks per head (this
+ * GPU only). Each block reads only the score groups whose largest first digit
+ * reaches the cut's bucket, and sends the bucket's keys to the cluster's
+ * first block through distributed shared memory, which finds the cut there.
  * ------------------------------------------------------------------------- */
 int kvx_select_workspace_bytes(int32_t B, int32_t Hkv, int32_t Lmax, size_t *bytes);
 

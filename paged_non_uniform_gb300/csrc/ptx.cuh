@@ -219,6 +219,22 @@ __device__ __forceinline__ float2 ld_cluster_f2(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Arrival on the cluster barrier that publishes nothing (a block's first
+// arrival, which only says that it has started).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+
 // One arrival on an mbarrier of another block of the cluster (`remote` from
 // mapa_shared), releasing this thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote) {

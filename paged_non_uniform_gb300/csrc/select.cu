@@ -14,13 +14,15 @@
 // Kernels, in stream order:
 //   score   streams every candidate key row once (HBM-bound), fp32 dot with Q,
 //           and counts the first radix digit (top 11 key bits) per head;
-//   bucket  many blocks per head: each reads a span of scores once, sets the
-//           positions whose first radix digit is above the cut's in a
-//           bitmask and appends those in the cut's bucket to a list;
-//   topk    one block per head: the other two radix digits (11/11/10 bits
-//           on order-preserving keys) over the bucket list in shared
-//           memory, then bitmasks of the kept positions and an ordered
-//           write, ascending;
+//   cut     one thread-block cluster per head (this GPU only): every block
+//           reads its span of the head's scores once, sets the positions
+//           whose first digit is above the cut's in a bitmask and keeps
+//           those in the cut's bucket in its shared memory; the leader block
+//           finds the other two radix digits (11/11/10 bits on
+//           order-preserving keys) over the blocks' buckets through
+//           distributed shared memory; every block then marks its positions
+//           against the cut and writes its kept positions, ascending, at an
+//           offset counted over the cluster;
 //   pack    copies kept row i of each head into token i of its pages.
 #include <cuda_bf16.h>
 
@@ -34,8 +36,7 @@ namespace kvx {
 namespace {
 
 constexpr int kScoreThreads = 256;
-constexpr int kScoreTokensPerBlock = 2048;
-constexpr int kTopkThreads = 1024;
+constexpr int kScoreTokensPerBlock = 1024;  // a multiple of 8: groups stay in one block
 constexpr int kPackThreads = 256;
 
 // Order-preserving map of an fp32 score to uint32 (larger score, larger key);
@@ -61,19 +62,32 @@ struct SelectParams {
   const __nv_bfloat16 *keys;  // [B][Hkv][Lmax][D]
   const __nv_bfloat16 *q;     // [B][Hq][D]
   const int32_t *seq_len;     // [B]
-  float *scores;              // [B*Hkv][Lmax]
+  float *scores;              // [B*Hkv][ldsc]
   int32_t *hist0;             // [B*Hkv][2048] counts of the top 11 key bits (zeroed per call)
+  uint16_t *gmax;             // [B*Hkv][ldg] top 11 key bits of the largest score of 8 positions
   int32_t *kept_idx;          // [B*Hkv][stride]
   int32_t *kept_count;        // [B*Hkv]
   uint32_t *status;
-  uint2 *blist;               // [B*Hkv][kBucketCap] (key, position) of the cut's first-digit bucket
-  int32_t *bcnt;              // [B*Hkv] bucket sizes (zeroed per call with hist0)
-  uint32_t *bgt;              // [B*Hkv][wstride] bitmask: first digit above the cut's
   int32_t B, Hq, Hkv, D, Lmax, top, recent, stride;
-  int32_t ldsc;               // score row stride: Lmax rounded up to a multiple of 4
-  int32_t wstride;            // bitmask row stride in words
+  int32_t ldsc;               // score row stride: Lmax rounded up to a multiple of 8
+  int32_t ldg;                // group row stride: Lmax / 8 rounded up to a multiple of 8
 };
 
+// Clears the first-digit histograms; the score pass may start at once.
+constexpr int kZeroThreads = 256;
+__global__ void __launch_bounds__(kZeroThreads) select_zero_kernel(int4 *h, int n4) {
+  pdl_launch_dependents();
+  const int i = blockIdx.x * kZeroThreads + threadIdx.x;
+  if (i < n4) h[i] = make_int4(0, 0, 0, 0);
+}
+
+// Score pass: block (x, bh) takes candidates [x * kScoreTokensPerBlock, ...)
+// of head bh. It sums the g query vectors, streams the key rows (LPT lanes per
+// row, U rows in flight per lane), writes the fp32 scores, then counts their
+// first radix digit (top 11 key bits) and adds the counts to the head's
+// histogram. The same post-pass writes, for every group of 8 positions, the
+// first digit of the group's largest score, so that the cut pass can skip
+// groups below its bucket without reading their scores.
 template <int D>
 __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const SelectParams p) {
   constexpr int LPT = D / 8;          // lanes per token row (16 bytes each)
@@ -82,7 +96,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
   __shared__ float Q[D];
   __shared__ int hist[2048];
   __shared__ float s_sc[kScoreTokensPerBlock];
-  pdl_launch_dependents();  // the bucket pass may launch; it waits for this grid
+  pdl_launch_dependents();  // the cut pass may launch; it waits for this grid
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, h = bh - b * p.Hkv;
   const int g = p.Hq / p.Hkv;
@@ -133,86 +147,82 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
     }
   }
   __syncthreads();
-  // first radix digit of the selection (top 11 key bits), counted per block
-  // with warp-aggregated shared-memory atomics, then added to the head's
-  // global histogram
+  // first radix digit of every score, counted per block with warp-aggregated
+  // shared-memory atomics; the largest digit of each group of 8 positions
   const int cnt_here = t_end - t_begin;
+  uint16_t *gm = p.gmax + (size_t)bh * p.ldg + t_begin / 8;
   for (int i0 = warp * 32; i0 < cnt_here; i0 += kScoreThreads) {
     const int i = i0 + lane;
     const int bin = i < cnt_here ? (int)(order_key(s_sc[i]) >> 21) : -1;
     const unsigned grp = __match_any_sync(0xffffffffu, bin);
     if (bin >= 0 && (__ffs(grp) - 1) == lane) atomicAdd(&hist[bin], __popc(grp));
+    int mx = bin;
+#pragma unroll
+    for (int sh = 1; sh < 8; sh <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
+    if ((lane & 7) == 0 && i < cnt_here) gm[i >> 3] = (uint16_t)mx;
   }
   __syncthreads();
+  pdl_wait();  // the histograms have been zeroed
   int32_t *gh = p.hist0 + (size_t)bh * 2048;
   for (int i = threadIdx.x; i < 2048; i += kScoreThreads)
     if (hist[i]) atomicAdd(gh + i, hist[i]);
 }
 
-constexpr int kTopkWarps = kTopkThreads / 32;
-static_assert(2048 % kTopkThreads == 0, "top-k: the first-digit histogram splits evenly");
-constexpr int kBucketCap = 8192;       // (key, position) pairs kept per head
-constexpr int kBucketThreads = 512;
-static_assert(2048 % kBucketThreads == 0, "bucket: the first-digit histogram splits evenly");
-constexpr int kBucketSpan = 32768;     // positions per bucket block
-constexpr int kBucketUC = 4;           // float4 per thread in each of its sub-spans
-constexpr int kBlockBucketCap = 4096;  // bucket entries one bucket block stages in shared memory
 constexpr int kMaxSelectLmax = 1 << 18;
 
-size_t select_wstride(int Lmax) { return (((size_t)Lmax + 31) / 32 + 3) & ~size_t(3); }
-
-// Dynamic shared memory of the top-k kernel: the bucket list, then the
-// above-cut and at-cut bitmasks of all candidate positions.
-size_t topk_smem_bytes(int Lmax) {
-  return (size_t)kBucketCap * sizeof(uint2) + 2 * select_wstride(Lmax) * sizeof(uint32_t);
-}
-
-// Finds, from a histogram of nb bins, the bin (counted from the top) that
-// holds the k-th largest key and the rank of that key inside the bin. All NT
-// threads of the block call it:
-// thread t owns nb / NT consecutive bins from the top, a two-level scan gives
-// each thread the count above its bins, and the thread whose bins hold the
-// k-th key resolves it. wsum: NT / 32 ints of shared scratch.
-template <int NT>
-__device__ __forceinline__ void find_digit_block(const int *hist, int nb, int k,
-                                                 uint32_t *s_digit, int *s_k, int *wsum) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = nb / NT;
+// Finds, with one warp, the bin (counted from the top) of a histogram of NB
+// bins that holds the k-th largest key, and the rank of that key inside the
+// bin (1 = the bin's largest). Lane i owns the NB / 32 bins below the top
+// i * NB / 32; a warp scan of the lanes' sums finds the lane that reaches k,
+// and a second scan over that lane's bins, spread over the warp, finds the
+// bin. Every lane returns the same result; with 1 <= k <= the histogram's
+// total. Bins are read as int4 (hist 16-byte aligned).
+template <int NB>
+__device__ __forceinline__ void find_digit_warp(const int *hist, int k, uint32_t &digit, int &rank) {
+  constexpr int PER = NB / 32;   // bins per lane
+  constexpr int P2 = PER / 32;   // bins per lane in the second scan
+  static_assert(PER % 4 == 0 && P2 >= 1 && PER % 32 == 0, "histogram size");
+  const int lane = threadIdx.x & 31;
+  const int4 *h4 = reinterpret_cast<const int4 *>(hist + NB - PER * (lane + 1));
   int sum = 0;
-  for (int e = 0; e < per; ++e) sum += hist[nb - 1 - tid * per - e];
+#pragma unroll
+  for (int q = 0; q < PER / 4; ++q) {
+    const int4 h = h4[q];
+    sum += h.x + h.y + h.z + h.w;
+  }
   int incl = sum;
 #pragma unroll
   for (int sh = 1; sh < 32; sh <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, incl, sh);
     if (lane >= sh) incl += y;
   }
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int v = lane < NT / 32 ? wsum[lane] : 0;
-    int x = v;
+  const unsigned hit = __ballot_sync(0xffffffffu, incl >= k);
+  const int L = hit ? __ffs(hit) - 1 : 31;
+  const int kk = k - __shfl_sync(0xffffffffu, incl - sum, L);
+  const int top = NB - 1 - PER * L;  // the highest bin of lane L
+  int c[P2], s2 = 0;
 #pragma unroll
-    for (int sh = 1; sh < 32; sh <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, sh);
-      if (lane >= sh) x += y;
-    }
-    if (lane < NT / 32) wsum[lane] = x - v;
+  for (int e = 0; e < P2; ++e) {
+    c[e] = hist[top - lane * P2 - e];
+    s2 += c[e];
   }
-  __syncthreads();
-  const int before = wsum[warp] + incl - sum;
-  if (before < k && k <= before + sum) {
-    int acc = before;
-    for (int e = 0; e < per; ++e) {
-      const int c = hist[nb - 1 - tid * per - e];
-      if (acc + c >= k) {
-        *s_digit = (uint32_t)(nb - 1 - tid * per - e);
-        *s_k = k - acc;
-        break;
-      }
-      acc += c;
-    }
+  int incl2 = s2;
+#pragma unroll
+  for (int sh = 1; sh < 32; sh <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl2, sh);
+    if (lane >= sh) incl2 += y;
   }
-  __syncthreads();
+  const unsigned hit2 = __ballot_sync(0xffffffffu, incl2 >= kk);
+  const int J = hit2 ? __ffs(hit2) - 1 : 31;
+  int dg = top - lane * P2, rk = kk - (incl2 - s2);
+#pragma unroll
+  for (int e = 0; e + 1 < P2; ++e) {
+    if (rk <= c[e]) break;
+    rk -= c[e];
+    --dg;
+  }
+  digit = (uint32_t)__shfl_sync(0xffffffffu, dg, J);
+  rank = __shfl_sync(0xffffffffu, rk, J);
 }
 
 // Cut search shared by both kernels: the candidate count of a head and
@@ -230,296 +240,481 @@ __device__ __forceinline__ HeadSel head_sel(const SelectParams &p, int bh) {
   return h;
 }
 
-// Bucket pass, grid (position spans, heads). Every block finds the cut's
-// first digit d0 from the score kernel's histogram, then reads its span of
-// scores once (float4 per lane, the next sub-span loading while the current
-// one is sorted): positions whose first digit is above d0 go
-// into the above-cut bitmask (word j of a warp's 128 positions is collected
-// from lanes 8j..8j+7), positions in the bucket d0 are appended to the head's
-// (key, position) list: staged in shared memory (one shared atomic per warp)
-// and copied out after one global atomic per block (many atomics on one
-// global counter would serialise).
-__global__ void __launch_bounds__(kBucketThreads, 2) select_bucket_kernel(const SelectParams p) {
-  __shared__ int hist[2048];
-  __shared__ uint2 sl[kBlockBucketCap];
-  __shared__ uint32_t s_digit;
-  __shared__ int s_k, s_cnt, s_base;
-  __shared__ int wsum[kBucketThreads / 32];
-  pdl_launch_dependents();
-  pdl_wait();  // scores and histograms of the score pass
-  const int bh = blockIdx.y;
-  const HeadSel hs = head_sel(p, bh);
-  const int t_begin = blockIdx.x * kBucketSpan;
-  if (!hs.search || t_begin >= hs.n) return;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int n = hs.n, nwords = (n + 31) >> 5;
-  const float4 *sc4 = reinterpret_cast<const float4 *>(p.scores + (size_t)bh * p.ldsc);
-  uint32_t *gtw = p.bgt + (size_t)bh * p.wstride;
-  uint2 *list = p.blist + (size_t)bh * kBucketCap;
-  constexpr int SUB4 = kBucketThreads * kBucketUC;  // float4 per sub-span
-  constexpr int NSUB = kBucketSpan / 4 / SUB4;
-  const int i0 = t_begin / 4, n4 = (n + 3) >> 2;
-  // the first sub-span's scores are loaded while the cut's first digit is
-  // found; each later sub-span is loaded while the previous one is sorted
-  float4 v[kBucketUC];
-#pragma unroll
-  for (int j = 0; j < kBucketUC; ++j) {
-    const int i4 = i0 + j * kBucketThreads + tid;
-    v[j] = i4 < n4 ? __ldcg(sc4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  {
-    // the histogram's loads are all issued before the first store
-    constexpr int CH = 2048 / kBucketThreads;
-    int hv[CH];
-#pragma unroll
-    for (int j = 0; j < CH; ++j) hv[j] = __ldcg(p.hist0 + (size_t)bh * 2048 + tid + j * kBucketThreads);
-#pragma unroll
-    for (int j = 0; j < CH; ++j) hist[tid + j * kBucketThreads] = hv[j];
-  }
-  if (tid == 0) s_cnt = 0;
-  __syncthreads();
-  find_digit_block<kBucketThreads>(hist, 2048, hs.ksel, &s_digit, &s_k, wsum);
-  const uint32_t d0 = s_digit;
-  // Away from NaN, infinities and the two zeros (digits 0..3, 1023, 1024 and
-  // 2044 up), the bucket d0 is the float interval [lo, hi) of its keys, so
-  // two float compares classify a score; the key is computed only for the
-  // few scores in the bucket. Elsewhere every score's key is compared.
-  const bool fast = d0 >= 4 && d0 <= 2043 && d0 != 1023 && d0 != 1024;
-  const float lo = key_float(d0 << 21), hi = key_float((d0 + 1) << 21);
-#pragma unroll 1
-  for (int c = 0; c < NSUB; ++c) {
-    const int b4 = i0 + c * SUB4;
-    if (4 * b4 >= n) break;  // block-uniform
-    float4 nx[kBucketUC];
-#pragma unroll
-    for (int j = 0; j < kBucketUC; ++j) {
-      const int i4 = b4 + SUB4 + j * kBucketThreads + tid;
-      nx[j] = (c + 1 < NSUB && i4 < n4) ? __ldcg(sc4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int j = 0; j < kBucketUC; ++j) {
-      const int t = 4 * (b4 + j * kBucketThreads + tid);
-      if (t - 4 * lane >= n) break;  // warp-uniform: the warp's 128 positions start past n
-      const float f[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-      uint32_t ng = 0, nb = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool in = t + e < n;
-        bool above, inb;
-        if (fast) {
-          above = f[e] >= hi;
-          inb = f[e] >= lo && !above;
-        } else {
-          const uint32_t dg = order_key(f[e]) >> 21;
-          above = dg > d0;
-          inb = dg == d0;
-        }
-        ng |= (uint32_t)(in && above) << e;
-        nb |= (uint32_t)(in && inb) << e;
-      }
-      uint32_t wg = ng << (4 * (lane & 7));
-#pragma unroll
-      for (int sh = 1; sh < 8; sh <<= 1) wg |= __shfl_xor_sync(0xffffffffu, wg, sh);
-      if ((lane & 7) == 0 && (t >> 5) < nwords) gtw[t >> 5] = wg;
-      if (nb) {
-        int off = atomicAdd(&s_cnt, __popc(nb));
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if ((nb >> e) & 1u) {
-            if (off < kBlockBucketCap) sl[off] = make_uint2(order_key(f[e]), (uint32_t)(t + e));
-            ++off;
-          }
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kBucketUC; ++j) v[j] = nx[j];
-  }
-  __syncthreads();
-  const int c = s_cnt;
-  // a block whose bucket share does not fit marks the whole head as
-  // overflowed (its count alone exceeds the list)
-  if (tid == 0) s_base = atomicAdd(p.bcnt + bh, c > kBlockBucketCap ? kBucketCap + 1 : c);
-  __syncthreads();
-  if (c <= kBlockBucketCap)
-    for (int i = tid; i < c && s_base + i < kBucketCap; i += kBucketThreads)
-      list[s_base + i] = sl[i];
-}
+// ---- cut and ordered write: one cluster of kCutCluster blocks per head -----
+constexpr int kCutCluster = 4;                 // blocks per head
+constexpr int kCutThreads = 512;
+constexpr int kCutWarps = kCutThreads / 32;
+constexpr int kCutLocalCap = 2048;             // bucket entries a block keeps
+constexpr int kCutMaxWords = (kMaxSelectLmax / 32 + kCutCluster - 1) / kCutCluster;
+constexpr int kCutPassC = 4;                   // chunks of 32 groups per warp and pass
+constexpr int kCutWarpCap = 128;               // bucket entries a warp keeps
+constexpr int kCutRB = 8;                      // rounds (of 4 groups) whose scores load together
+static_assert(kCutWarps * kCutWarpCap == kCutLocalCap, "cut: the warps' lists fill the block's");
+constexpr int kCutCand = 32;                   // final-digit candidates one warp resolves
+static_assert(2048 == 4 * kCutThreads, "cut: one int4 of the first-digit histogram per thread");
 
-// One block per head. The cut (the key of the ksel-th largest candidate) is
-// found by a radix select over 11, 11 and 10 bits, MSB first: the first digit
-// from the score kernel's histogram, the other two over the bucket list that
-// the bucket pass gathered (loaded into shared memory). List entries above
-// the cut join the above-cut bitmask, entries equal to it the at-cut
-// bitmask; each warp then writes the selected positions of its words in
-// ascending order, keys equal to the cut lowest position first. If the bucket
-// overflowed the list, the two digits and the bitmasks come from scans of
-// the scores in global memory instead.
-__global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectParams p) {
-  extern __shared__ __align__(16) uint8_t dsm[];
-  uint2 *list = reinterpret_cast<uint2 *>(dsm);
-  uint32_t *gtw = reinterpret_cast<uint32_t *>(list + kBucketCap);
-  uint32_t *eqw = gtw + p.wstride;
-  __shared__ int hist[2048];
-  __shared__ int wcnt[2][kTopkWarps];
-  __shared__ int wsum[kTopkWarps];
-  __shared__ uint32_t s_digit;
-  __shared__ int s_k;
-  pdl_wait();  // bucket lists and bitmasks of the bucket pass
-  const int bh = blockIdx.x;
-  const HeadSel hs = head_sel(p, bh);
-  const int L = hs.L, n = hs.n, ksel = hs.ksel;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0 && L != p.seq_len[bh / p.Hkv]) atomicOr(p.status, KVX_DEV_BAD_LENGTH);
-  const int nwords = (n + 31) >> 5;
-  const float *sc = p.scores + (size_t)bh * p.ldsc;
-  int32_t *out = p.kept_idx + (size_t)bh * p.stride;
-  const bool take_all = ksel >= n;
-  // The first chunk of every input (bucket size, above-cut bitmask words,
-  // bucket list, histogram) is loaded before any of it is stored, so that
-  // the loads share one L2 round trip; list entries past the bucket's size
-  // are read (inside the list's capacity) and dropped. Longer inputs finish
-  // in plain loops.
-  constexpr int CW = 4, CL = 4, CH = 2048 / kTopkThreads;
-  const uint32_t *ggt = p.bgt + (size_t)bh * p.wstride;
-  const uint2 *glist = p.blist + (size_t)bh * kBucketCap;
-  const int32_t *ghist = p.hist0 + (size_t)bh * 2048;
-  const int cnt_raw = hs.search ? __ldcg(p.bcnt + bh) : 0;
-  uint32_t wv[CW];
-  uint2 lv[CL];
-  int hv[CH];
+// Shared memory of a cut block; the same layout in every block, so that a
+// field's address maps to the same field of another block of the cluster.
+struct CutSmem {
+  int hist[2048];
+  uint2 list[kCutWarps][kCutWarpCap];          // (key, position) of the block's bucket, per warp
+  int slot[kCutWarps][kCutPassC * 32];         // a warp's active groups of a pass
+  int wcount[kCutWarps];                       // entries of each warp (may pass the cap)
+  uint32_t keys[kCutCluster][kCutLocalCap];    // leader: every block's bucket keys
+  uint32_t gtw[kCutMaxWords];                  // the block's words: positions above the cut
+  uint32_t eqw[kCutMaxWords];                  // positions whose key equals the cut
+  uint32_t ckey[kCutCand];                     // leader: keys sharing the cut's top 22 bits
+  int creg[kCutCand];                          //   and the block each came from
+  int wcnt[2][kCutWarps];
+  int rcnt[kCutCluster];                       // leader: every block's bucket size
+  int rgt[kCutCluster];                        // leader: every block's count above the bucket
+  int rG[kCutCluster], rE[kCutCluster];        // leader: above / equal to the cut, per block
+  int ncand;
+  int lcount;                                  // this block's bucket size (may pass the cap)
+  int cgt;                                     // this block's positions above the bucket
+  uint32_t s_digit;
+  int s_k;
+  uint32_t s_cut;
+  int s_keq;
+  // from the leader, for this block
+  uint32_t cut;
+  int keq;                                     // keys equal to the cut that this block keeps
+  int base;                                    // kept positions in the blocks before this one
+  int mode;                                    // 0 none, 1 all, 2 from the buckets, 3 from scans
+  int written;                                 // leader: kept candidates of the head
+};
+constexpr size_t kCutSmemBytes = sizeof(CutSmem);
+
+// Leader helper: adds, for every block r, the keys of block r above and equal
+// to the cut (from the blocks' bucket keys, or, from_scores, from the scores
+// in global memory over block r's positions) to rG[r] and rE[r].
+__device__ __forceinline__ void count_against_cut(CutSmem &S, const float *sc, int n, int nwords,
+                                                  int per, uint32_t cut, bool from_scores) {
+  const int tid = threadIdx.x, lane = tid & 31;
 #pragma unroll
-  for (int j = 0; j < CW; ++j) {
-    const int w = tid + j * kTopkThreads;
-    wv[j] = hs.search && w < nwords ? __ldcg(ggt + w) : 0u;
-  }
-#pragma unroll
-  for (int j = 0; j < CL; ++j) {
-    const int i = tid + j * kTopkThreads;
-    lv[j] = hs.search && i < kBucketCap ? __ldcg(glist + i) : make_uint2(0u, 0u);
-  }
-#pragma unroll
-  for (int j = 0; j < CH; ++j) hv[j] = hs.search ? __ldcg(ghist + tid + j * kTopkThreads) : 0;
-  const int cnt = hs.search ? min(cnt_raw, kBucketCap + 1) : 0;
-  const bool in_smem = cnt <= kBucketCap;
-  // bitmasks: above-cut from the bucket pass (or all / none), at-cut empty
-  auto word0 = [&](int w, uint32_t loaded) {
-    const int rem = n - 32 * w;
-    return hs.search ? (in_smem ? loaded : 0u)
-                     : (take_all ? (rem >= 32 ? 0xffffffffu : (1u << rem) - 1u) : 0u);
-  };
-#pragma unroll
-  for (int j = 0; j < CW; ++j) {
-    const int w = tid + j * kTopkThreads;
-    if (w < nwords) {
-      gtw[w] = word0(w, wv[j]);
-      eqw[w] = 0u;
-    }
-  }
-  for (int w = tid + CW * kTopkThreads; w < nwords; w += kTopkThreads) {
-    gtw[w] = word0(w, hs.search && in_smem ? __ldcg(ggt + w) : 0u);
-    eqw[w] = 0u;
-  }
-  if (hs.search) {
-    if (in_smem) {
-#pragma unroll
-      for (int j = 0; j < CL; ++j) {
-        const int i = tid + j * kTopkThreads;
-        if (i < cnt) list[i] = lv[j];
-      }
-      for (int i = tid + CL * kTopkThreads; i < cnt; i += kTopkThreads) list[i] = __ldcg(glist + i);
-    }
-#pragma unroll
-    for (int j = 0; j < CH; ++j) hist[tid + j * kTopkThreads] = hv[j];
-  }
-  __syncthreads();
-  uint32_t prefix = 0;
-  int k = ksel;
-  if (hs.search) {
-    find_digit_block<kTopkThreads>(hist, 2048, k, &s_digit, &s_k, wsum);
-    prefix = s_digit << 21;
-    uint32_t mask = 0x7FFu << 21;
-    k = s_k;
-    __syncthreads();
-    for (int pass = 1; pass < 3; ++pass) {
-      const int bits = pass == 1 ? 11 : 10;
-      const int shift = pass == 1 ? 10 : 0;
-      const int nbins = 1 << bits;
-      for (int i = tid; i < nbins; i += kTopkThreads) hist[i] = 0;
-      __syncthreads();
-      if (in_smem) {
-        for (int i = tid; i < cnt; i += kTopkThreads) {
-          const uint32_t uu = list[i].x;
-          if ((uu & mask) == prefix) atomicAdd(&hist[(uu >> shift) & (uint32_t)(nbins - 1)], 1);
-        }
-      } else {
-        for (int tt = tid; tt < n; tt += kTopkThreads) {
-          const uint32_t uu = order_key(__ldcg(sc + tt));
-          if ((uu & mask) == prefix) atomicAdd(&hist[(uu >> shift) & (uint32_t)(nbins - 1)], 1);
-        }
-      }
-      __syncthreads();
-      find_digit_block<kTopkThreads>(hist, nbins, k, &s_digit, &s_k, wsum);
-      prefix |= s_digit << shift;
-      mask |= (uint32_t)(nbins - 1) << shift;
-      k = s_k;
-      __syncthreads();
-    }
-    const uint32_t cut = prefix;
-    if (in_smem) {
-      for (int i = tid; i < cnt; i += kTopkThreads) {
-        const uint2 e = list[i];
-        if (e.x > cut) atomicOr(&gtw[e.y >> 5], 1u << (e.y & 31));
-        else if (e.x == cut) atomicOr(&eqw[e.y >> 5], 1u << (e.y & 31));
+  for (int r = 0; r < kCutCluster; ++r) {
+    int gt = 0, eq = 0;
+    if (!from_scores) {
+      for (int i = tid; i < S.rcnt[r]; i += kCutThreads) {
+        const uint32_t uu = S.keys[r][i];
+        gt += uu > cut;
+        eq += uu == cut;
       }
     } else {
-      for (int w = warp; w < nwords; w += kTopkWarps) {
-        const int tt = 32 * w + lane;
-        const uint32_t uu = tt < n ? order_key(__ldcg(sc + tt)) : 0u;
-        const unsigned bg = __ballot_sync(0xffffffffu, tt < n && uu > cut);
-        const unsigned be = __ballot_sync(0xffffffffu, tt < n && uu == cut);
-        if (lane == 0) {
-          gtw[w] = bg;
-          eqw[w] = be;
-        }
+      const int a = 32 * min(nwords, r * per), e = min(n, 32 * min(nwords, r * per + per));
+      for (int tt = a + tid; tt < e; tt += kCutThreads) {
+        const uint32_t uu = order_key(__ldcg(sc + tt));
+        gt += uu > cut;
+        eq += uu == cut;
+      }
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, sh);
+      eq += __shfl_xor_sync(0xffffffffu, eq, sh);
+    }
+    if (lane == 0 && (gt | eq)) {
+      atomicAdd(&S.rG[r], gt);
+      atomicAdd(&S.rE[r], eq);
+    }
+  }
+}
+
+// Cluster (rank r of kCutCluster) per head bh. Rank r owns the head's
+// candidate words [w0, w1) (32 positions each). The cut is the key of the
+// ksel-th largest candidate, found by a radix select over 11, 11 and 10 bits,
+// MSB first: every block takes the first digit from the score kernel's
+// histogram, marks its positions above that digit's bucket and keeps the
+// bucket's entries; the blocks send their bucket keys to the leader (rank 0),
+// which finds the other two digits in its own shared memory (or by scans of
+// the scores in global memory when a bucket does not fit), counts each block's
+// positions above and equal to the cut, and sends every block its offset.
+// Positions above the cut are kept; of the positions equal to it, the lowest.
+// Each block then writes its kept positions in ascending order from its
+// offset; rank 0 also writes the recent window, the padding and the count.
+// Shared memory of another block is touched only between the first and the
+// last cluster barrier, so that no block leaves while it may be accessed.
+__global__ void __launch_bounds__(kCutThreads, 2) select_cut_kernel(const SelectParams p) {
+  extern __shared__ __align__(16) unsigned char cut_smem[];
+  CutSmem &S = *reinterpret_cast<CutSmem *>(cut_smem);
+  pdl_launch_dependents();
+  cluster_arrive_relaxed();  // this block has started
+  const int rank = (int)cluster_ctarank();
+  const int bh = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const HeadSel hs = head_sel(p, bh);
+  const int L = hs.L, n = hs.n, ksel = hs.ksel;
+  const int nwords = (n + 31) >> 5;
+  const int per = (nwords + kCutCluster - 1) / kCutCluster;
+  const int w0 = min(nwords, rank * per), w1 = min(nwords, w0 + per), nw = w1 - w0;
+  const float *sc = p.scores + (size_t)bh * p.ldsc;
+  for (int i = tid; i < nw; i += kCutThreads) {
+    S.gtw[i] = 0u;
+    S.eqw[i] = 0u;
+  }
+  if (tid == 0) {
+    S.lcount = 0;
+    S.cgt = 0;
+  }
+  pdl_wait();  // scores and histogram of the score pass
+  // ---- first digit, and this block's span against it
+  if (hs.search) {
+    // Groups of 8 positions; the block's groups that hold candidates are
+    // [gb, gend). Warp w takes chunks of 32 consecutive groups, w, w + 16, ...,
+    // kCutPassC per pass. From the first digit of each group's largest score
+    // it lists the groups that reach the bucket in its slots, then reads and
+    // classifies them four at a time, eight lanes (one position each) per
+    // group: one ballot gives the four groups' positions above the bucket,
+    // another those in it.
+    const uint16_t *gm = p.gmax + (size_t)bh * p.ldg;
+    const int glast = (n + 7) >> 3;
+    const int gb = 4 * w0, gend = min(4 * w1, glast);
+    const int nch = (max(0, gend - gb) + 31) >> 5;
+    auto load_max = [&](uint32_t (&md)[kCutPassC], int c0) {
+#pragma unroll
+      for (int i = 0; i < kCutPassC; ++i) {
+        const int c = c0 + warp + kCutWarps * i;
+        const int g = gb + 32 * c + lane;
+        md[i] = c < nch && g < gend ? (uint32_t)__ldcg(gm + g) : 0xFFFFFFFFu;
+      }
+    };
+    const int4 h4 = __ldcg(reinterpret_cast<const int4 *>(p.hist0 + (size_t)bh * 2048) + tid);
+    uint32_t md[kCutPassC];
+    load_max(md, 0);  // in flight while the first digit is found
+    reinterpret_cast<int4 *>(S.hist)[tid] = h4;
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t dg;
+      int rk;
+      find_digit_warp<2048>(S.hist, ksel, dg, rk);
+      if (lane == 0) {
+        S.s_digit = dg;
+        S.s_k = rk;
       }
     }
     __syncthreads();
-  }
-  // k = how many keys equal to the cut are kept. Warp w owns words
-  // [w*segw, (w+1)*segw).
-  const int segw = (nwords + kTopkWarps - 1) / kTopkWarps;
-  const int w_lo = min(nwords, warp * segw), w_hi = min(nwords, w_lo + segw);
-  int cg = 0, ce = 0;
-  for (int w = w_lo + lane; w < w_hi; w += 32) {
-    cg += __popc(gtw[w]);
-    ce += __popc(eqw[w]);
-  }
+    const uint32_t d0 = S.s_digit;
+    // Away from NaN, infinities and the two zeros (digits 0..3, 1023, 1024
+    // and 2044 up), the bucket d0 is the float interval [lo, hi) of its keys,
+    // so two float compares classify a score. Elsewhere its key is compared.
+    const bool fast = d0 >= 4 && d0 <= 2043 && d0 != 1023 && d0 != 1024;
+    const float lo = key_float(d0 << 21), hi = key_float((d0 + 1) << 21);
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    const int tq = lane >> 3, e = lane & 7;  // group of the round, position in it
+    int *slot = S.slot[warp];
+    uint2 *wl = S.list[warp];
+    int wcnt = 0, cg = 0;  // the warp's bucket entries and positions above (warp-uniform)
+    for (int c0 = 0; c0 < nch; c0 += kCutWarps * kCutPassC) {
+      if (c0 > 0) load_max(md, c0);
+      int na = 0;
 #pragma unroll
-  for (int sh = 16; sh > 0; sh >>= 1) {
-    cg += __shfl_xor_sync(0xffffffffu, cg, sh);
-    ce += __shfl_xor_sync(0xffffffffu, ce, sh);
-  }
-  if (lane == 0) {
-    wcnt[0][warp] = cg;
-    wcnt[1][warp] = ce;
+      for (int i = 0; i < kCutPassC; ++i) {
+        const bool act = md[i] <= 2047u && md[i] >= d0;
+        const unsigned A = __ballot_sync(0xffffffffu, act);
+        if (act) slot[na + __popc(A & lt_mask)] = 32 * (c0 + warp + kCutWarps * i) + lane;
+        na += __popc(A);
+      }
+      __syncwarp();
+      for (int r0 = 0; r0 < na; r0 += 4 * kCutRB) {
+        float f[kCutRB];
+        int grp[kCutRB];
+#pragma unroll
+        for (int q = 0; q < kCutRB; ++q) {
+          const int k = r0 + 4 * q + tq;
+          grp[q] = k < na ? slot[k] : -1;
+          f[q] = grp[q] >= 0 ? __ldcg(sc + 8 * (gb + grp[q]) + e) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kCutRB; ++q) {
+          if (r0 + 4 * q >= na) break;  // warp-uniform
+          const int pos = 8 * (gb + grp[q]) + e;
+          const bool in = grp[q] >= 0 && pos < n;
+          bool above, inb;
+          if (fast) {
+            above = f[q] >= hi;
+            inb = f[q] >= lo && !above;
+          } else {
+            const uint32_t dg = order_key(f[q]) >> 21;
+            above = dg > d0;
+            inb = dg == d0;
+          }
+          const unsigned ab = __ballot_sync(0xffffffffu, in && above);
+          const unsigned bb = __ballot_sync(0xffffffffu, in && inb);
+          if (e == 0 && grp[q] >= 0) {
+            const uint32_t byte = (ab >> (8 * tq)) & 0xFFu;
+            if (byte) atomicOr(&S.gtw[grp[q] >> 2], byte << (8 * (grp[q] & 3)));
+          }
+          cg += __popc(ab);
+          if (bb) {  // warp-uniform
+            if (in && inb) {
+              const int o = wcnt + __popc(bb & lt_mask);
+              if (o < kCutWarpCap) wl[o] = make_uint2(order_key(f[q]), (uint32_t)pos);
+            }
+            wcnt += __popc(bb);
+          }
+        }
+      }
+      __syncwarp();  // the slots are rewritten by the next pass
+    }
+    if (lane == 0) {
+      S.wcount[warp] = wcnt;
+      if (cg) atomicAdd(&S.cgt, cg);
+    }
   }
   __syncthreads();
-  int selp = 0, eqp = 0, total = 0, eqtot = 0;
-  for (int w = 0; w < kTopkWarps; ++w) {
-    if (w < warp) {
-      selp += wcnt[0][w] + max(0, min(wcnt[1][w], k - eqp));
-      eqp += wcnt[1][w];
+  cluster_wait();  // every block of the cluster has started: its shared memory is there
+  // ---- every block sends its bucket keys and counts to the leader: warp w's
+  // entries after those of the warps before it; a block whose bucket does not
+  // fit reports more than the cap and sends none
+  if (hs.search) {
+    int pre = 0, total = 0;
+    bool ovf = false;
+#pragma unroll
+    for (int w = 0; w < kCutWarps; ++w) {
+      const int c = S.wcount[w];
+      pre += w < warp ? c : 0;
+      total += c;
+      ovf = ovf || c > kCutWarpCap;
     }
-    total += wcnt[0][w];
-    eqtot += wcnt[1][w];
+    if (ovf) total = kCutLocalCap + 1;
+    if (total <= kCutLocalCap) {
+      const uint32_t dst = mapa_shared(smem_u32(&S.keys[rank][pre]), 0u);
+      for (int i = lane; i < S.wcount[warp]; i += 32)
+        st_cluster_u32(dst + 4u * (uint32_t)i, S.list[warp][i].x);
+    }
+    if (tid == 0) {
+      S.lcount = total;
+      st_cluster_u32(mapa_shared(smem_u32(&S.rcnt[rank]), 0u), (uint32_t)total);
+      st_cluster_u32(mapa_shared(smem_u32(&S.rgt[rank]), 0u), (uint32_t)S.cgt);
+    }
   }
-  const int written = total + min(eqtot, k);
+  cluster_arrive();
+  cluster_wait();  // the leader holds every block's keys and counts
+  // ---- the leader finds the cut and every block's offset
+  if (rank == 0) {
+    if (tid < kCutCluster) {
+      S.rG[tid] = 0;
+      S.rE[tid] = 0;
+    }
+    if (tid == 0) S.ncand = 0;
+    int mode = 0;
+    if (!hs.search) {
+      mode = ksel >= n && n > 0 ? 1 : 0;
+      if (tid == 0) {
+        S.s_cut = 0u;
+        S.s_keq = 0;
+      }
+    } else {
+      bool overflow = false;
+#pragma unroll
+      for (int r = 0; r < kCutCluster; ++r) overflow = overflow || S.rcnt[r] > kCutLocalCap;
+      mode = overflow ? 3 : 2;
+      const uint32_t d0 = S.s_digit;
+      const int k0 = S.s_k;
+      // second digit (key bits 20..10) over the bucket keys, or over a scan
+      for (int i = tid; i < 2048; i += kCutThreads) S.hist[i] = 0;
+      __syncthreads();
+      if (!overflow) {
+#pragma unroll
+        for (int r = 0; r < kCutCluster; ++r)
+          for (int i = tid; i < S.rcnt[r]; i += kCutThreads)
+            atomicAdd(&S.hist[(S.keys[r][i] >> 10) & 2047u], 1);
+      } else {
+        for (int tt = tid; tt < n; tt += kCutThreads) {
+          const uint32_t uu = order_key(__ldcg(sc + tt));
+          if ((uu >> 21) == d0) atomicAdd(&S.hist[(uu >> 10) & 2047u], 1);
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        uint32_t dg;
+        int rk;
+        find_digit_warp<2048>(S.hist, k0, dg, rk);
+        if (lane == 0) {
+          S.s_digit = dg;
+          S.s_k = rk;
+        }
+      }
+      __syncthreads();
+      const uint32_t p22 = (d0 << 11) | S.s_digit;  // the cut's top 22 bits
+      const int k1 = S.s_k;
+      bool resolved = false;
+      if (!overflow) {
+        // keys above the top 22 bits, per block; the keys sharing them
+        // collected for one warp
+#pragma unroll
+        for (int r = 0; r < kCutCluster; ++r) {
+          int gt = 0;
+          for (int i = tid; i < S.rcnt[r]; i += kCutThreads) {
+            const uint32_t uu = S.keys[r][i];
+            gt += (uu >> 10) > p22;
+            if ((uu >> 10) == p22) {
+              const int o = atomicAdd(&S.ncand, 1);
+              if (o < kCutCand) {
+                S.ckey[o] = uu;
+                S.creg[o] = r;
+              }
+            }
+          }
+#pragma unroll
+          for (int sh = 16; sh > 0; sh >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, sh);
+          if (lane == 0 && gt) atomicAdd(&S.rG[r], gt);
+        }
+        __syncthreads();
+        resolved = S.ncand <= kCutCand;
+        if (resolved && warp == 0) {
+          // the k1-th largest of the m candidates: a lane's key is the cut
+          // when fewer than k1 keys are above it and at least k1 are not below
+          const int m = S.ncand;
+          const bool own = lane < m;
+          const uint32_t key = own ? S.ckey[lane] : 0u;
+          const int reg = own ? S.creg[lane] : -1;
+          int above = 0, notbelow = 0;
+          for (int j = 0; j < m; ++j) {
+            const uint32_t kj = __shfl_sync(0xffffffffu, key, j);
+            above += kj > key;
+            notbelow += kj >= key;
+          }
+          const unsigned hit = __ballot_sync(0xffffffffu, own && above < k1 && k1 <= notbelow);
+          const int src = hit ? __ffs(hit) - 1 : 0;
+          const uint32_t cut = __shfl_sync(0xffffffffu, key, src);
+          const int keq = k1 - __shfl_sync(0xffffffffu, above, src);
+#pragma unroll
+          for (int r = 0; r < kCutCluster; ++r) {
+            const int gtx = __popc(__ballot_sync(0xffffffffu, own && reg == r && key > cut));
+            const int eqx = __popc(__ballot_sync(0xffffffffu, own && reg == r && key == cut));
+            if (lane == r) {
+              S.rG[r] += gtx;
+              S.rE[r] = eqx;
+            }
+          }
+          if (lane == 0) {
+            S.s_cut = cut;
+            S.s_keq = keq;
+          }
+        }
+      }
+      if (!resolved) {
+        // third digit (key bits 9..0) by a histogram, then every block's
+        // counts against the cut
+        for (int i = tid; i < 1024; i += kCutThreads) S.hist[i] = 0;
+        if (tid < kCutCluster) S.rG[tid] = 0;
+        __syncthreads();
+        if (!overflow) {
+#pragma unroll
+          for (int r = 0; r < kCutCluster; ++r)
+            for (int i = tid; i < S.rcnt[r]; i += kCutThreads) {
+              const uint32_t uu = S.keys[r][i];
+              if ((uu >> 10) == p22) atomicAdd(&S.hist[uu & 1023u], 1);
+            }
+        } else {
+          for (int tt = tid; tt < n; tt += kCutThreads) {
+            const uint32_t uu = order_key(__ldcg(sc + tt));
+            if ((uu >> 10) == p22) atomicAdd(&S.hist[uu & 1023u], 1);
+          }
+        }
+        __syncthreads();
+        if (warp == 0) {
+          uint32_t dg;
+          int rk;
+          find_digit_warp<1024>(S.hist, k1, dg, rk);
+          if (lane == 0) {
+            S.s_cut = (p22 << 10) | dg;
+            S.s_keq = rk;
+          }
+        }
+        __syncthreads();
+        count_against_cut(S, sc, n, nwords, per, S.s_cut, overflow);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t cut = S.s_cut;
+      const int keq = S.s_keq;
+      int base = 0, eqseen = 0;
+      for (int r = 0; r < kCutCluster; ++r) {
+        int G = 0, E = 0;
+        const int a = 32 * min(nwords, r * per), e = min(n, 32 * min(nwords, r * per + per));
+        if (mode == 1) G = max(0, e - a);
+        if (mode == 2) G = S.rgt[r] + S.rG[r], E = S.rE[r];
+        if (mode == 3) G = S.rG[r], E = S.rE[r];
+        const int kr = max(0, min(E, keq - eqseen));
+        const uint32_t rr = (uint32_t)r;
+        st_cluster_u32(mapa_shared(smem_u32(&S.cut), rr), cut);
+        st_cluster_u32(mapa_shared(smem_u32(&S.keq), rr), (uint32_t)kr);
+        st_cluster_u32(mapa_shared(smem_u32(&S.base), rr), (uint32_t)base);
+        st_cluster_u32(mapa_shared(smem_u32(&S.mode), rr), (uint32_t)mode);
+        base += G + kr;
+        eqseen += E;
+      }
+      S.written = base;
+    }
+  }
+  cluster_arrive();
+  cluster_wait();  // every block holds its cut, count of equal keys and offset
+  // ---- every block marks its positions against the cut and writes them
+  const uint32_t cut = S.cut;
+  const int keq = S.keq, mode = S.mode;
+  if (mode == 1) {
+    for (int i = tid; i < nw; i += kCutThreads) {
+      const int rem = n - 32 * (w0 + i);
+      S.gtw[i] = rem >= 32 ? 0xffffffffu : (1u << rem) - 1u;
+    }
+  } else if (mode == 2) {
+    // mode 2: every warp's list fits (the leader saw no block over the cap)
+    for (int i = lane; i < S.wcount[warp]; i += 32) {
+      const uint2 e = S.list[warp][i];
+      const int w = (int)(e.y >> 5) - w0;
+      if (e.x > cut) atomicOr(&S.gtw[w], 1u << (e.y & 31));
+      else if (e.x == cut) atomicOr(&S.eqw[w], 1u << (e.y & 31));
+    }
+  } else if (mode == 3) {
+    for (int w = w0 + warp; w < w1; w += kCutWarps) {
+      const int tt = 32 * w + lane;
+      const uint32_t uu = tt < n ? order_key(__ldcg(sc + tt)) : 0u;
+      const unsigned bg = __ballot_sync(0xffffffffu, tt < n && uu > cut);
+      const unsigned be = __ballot_sync(0xffffffffu, tt < n && uu == cut);
+      if (lane == 0) {
+        S.gtw[w - w0] = bg;
+        S.eqw[w - w0] = be;
+      }
+    }
+  }
+  __syncthreads();
+  // warp w of the block owns local words [w*segw, (w+1)*segw)
+  const int segw = (nw + kCutWarps - 1) / kCutWarps;
+  const int v_lo = min(nw, warp * segw), v_hi = min(nw, v_lo + segw);
+  {
+    int cg = 0, ce = 0;
+    for (int v = v_lo + lane; v < v_hi; v += 32) {
+      cg += __popc(S.gtw[v]);
+      ce += __popc(S.eqw[v]);
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) {
+      cg += __shfl_xor_sync(0xffffffffu, cg, sh);
+      ce += __shfl_xor_sync(0xffffffffu, ce, sh);
+    }
+    if (lane == 0) {
+      S.wcnt[0][warp] = cg;
+      S.wcnt[1][warp] = ce;
+    }
+  }
+  __syncthreads();
+  // kept positions before this warp; the block keeps its keq lowest
+  // positions equal to the cut
+  int selp = S.base, eqp = 0;
+  for (int w = 0; w < warp; ++w) {
+    selp += S.wcnt[0][w] + max(0, min(S.wcnt[1][w], keq - eqp));
+    eqp += S.wcnt[1][w];
+  }
+  int32_t *out = p.kept_idx + (size_t)bh * p.stride;
   // ascending write of the warp's words: one word per lane and step
   int wpos = selp, erank = eqp;
-  for (int w0 = w_lo; w0 < w_hi; w0 += 32) {
-    const int w = w0 + lane;
-    const uint32_t g = w < w_hi ? gtw[w] : 0u;
-    uint32_t e = w < w_hi ? eqw[w] : 0u;
+  for (int v0 = v_lo; v0 < v_hi; v0 += 32) {
+    const int v = v0 + lane;
+    const uint32_t gw = v < v_hi ? S.gtw[v] : 0u;
+    uint32_t e = v < v_hi ? S.eqw[v] : 0u;
     const int ne = __popc(e);
     int ie = ne;
 #pragma unroll
@@ -527,15 +722,15 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectP
       const int y = __shfl_up_sync(0xffffffffu, ie, sh);
       if (lane >= sh) ie += y;
     }
-    // keep the first max(0, k - rank) equal keys of this word
-    int take = min(ne, max(0, k - (erank + ie - ne)));
+    // keep the first max(0, keq - rank) equal keys of this word
+    int take = min(ne, max(0, keq - (erank + ie - ne)));
     uint32_t et = 0;
     while (take-- > 0) {
       const uint32_t low = e & (0u - e);
       et |= low;
       e ^= low;
     }
-    uint32_t sel = g | et;
+    uint32_t sel = gw | et;
     const int ns = __popc(sel);
     int is = ns;
 #pragma unroll
@@ -546,19 +741,23 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const SelectP
     int o = wpos + is - ns;
     while (sel) {
       const int bit = __ffs(sel) - 1;
-      if (o < p.stride) out[o] = w * 32 + bit;
+      if (o < p.stride) out[o] = (w0 + v) * 32 + bit;
       ++o;
       sel &= sel - 1;
     }
     wpos += __shfl_sync(0xffffffffu, is, 31);
     erank += __shfl_sync(0xffffffffu, ie, 31);
   }
-  // recent window, then padding
-  for (int t = n + tid; t < L; t += kTopkThreads)
-    if (written + (t - n) < p.stride) out[written + (t - n)] = t;
-  const int cntk = written + (L - n);
-  for (int i = cntk + tid; i < p.stride; i += kTopkThreads) out[i] = -1;
-  if (tid == 0) p.kept_count[bh] = cntk;
+  if (rank == 0) {
+    if (tid == 0 && L != p.seq_len[bh / p.Hkv]) atomicOr(p.status, KVX_DEV_BAD_LENGTH);
+    // recent window, then padding
+    const int written = S.written;
+    for (int t = n + tid; t < L; t += kCutThreads)
+      if (written + (t - n) < p.stride) out[written + (t - n)] = t;
+    const int cntk = written + (L - n);
+    for (int i = cntk + tid; i < p.stride; i += kCutThreads) out[i] = -1;
+    if (tid == 0) p.kept_count[bh] = cntk;
+  }
 }
 
 struct PackParams {
@@ -629,28 +828,27 @@ __global__ void __launch_bounds__(kPackThreads) pack_kept_kernel(const __grid_co
 
 using namespace kvx;
 
-// Workspace: header | hist0 int32 [BH][2048] | bcnt int32 [BH] | scores f32
-// [BH][ldsc] | blist uint2 [BH][kBucketCap] | bgt uint32 [BH][wstride], each
-// section 256-byte aligned; hist0 and bcnt are cleared by one memset per call.
+// Workspace: header | hist0 int32 [BH][2048] | gmax u16 [BH][ldg] | scores f32 [BH][ldsc], each
+// section 256-byte aligned; hist0 is cleared by a kernel at the start of each call.
 struct SelectWs {
-  size_t hist0, bcnt, scores, blist, bgt, total;
+  size_t hist0, gmax, scores, total;
+  size_t ldsc, ldg;
 };
-SelectWs select_ws_offsets(size_t BH, size_t ldsc, size_t wstride) {
+SelectWs select_ws_offsets(size_t BH, size_t Lmax) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   SelectWs w;
+  w.ldsc = (Lmax + 7) & ~size_t(7);
+  w.ldg = ((Lmax + 7) / 8 + 7) & ~size_t(7);
   w.hist0 = KVX_WS_HEADER_BYTES;
-  w.bcnt = w.hist0 + sizeof(int32_t) * 2048 * BH;
-  w.scores = al(w.bcnt + sizeof(int32_t) * BH);
-  w.blist = al(w.scores + sizeof(float) * BH * ldsc);
-  w.bgt = al(w.blist + sizeof(uint2) * BH * kBucketCap);
-  w.total = al(w.bgt + sizeof(uint32_t) * BH * wstride);
+  w.gmax = al(w.hist0 + sizeof(int32_t) * 2048 * BH);
+  w.scores = al(w.gmax + sizeof(uint16_t) * BH * w.ldg);
+  w.total = al(w.scores + sizeof(float) * BH * w.ldsc);
   return w;
 }
 
 extern "C" int kvx_select_workspace_bytes(int32_t B, int32_t Hkv, int32_t Lmax, size_t *bytes) {
   if (!bytes || B < 1 || Hkv < 1 || Lmax < 1) return KVX_EINVAL;
-  const size_t BH = (size_t)B * Hkv, ldsc = ((size_t)Lmax + 3) & ~size_t(3);
-  *bytes = select_ws_offsets(BH, ldsc, select_wstride(Lmax)).total;
+  *bytes = select_ws_offsets((size_t)B * Hkv, (size_t)Lmax).total;
   return KVX_OK;
 }
 
@@ -674,14 +872,11 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
   p.q = (const __nv_bfloat16 *)q;
   p.seq_len = seq_len;
   const size_t BH = (size_t)B * Hkv;
-  const SelectWs wl = select_ws_offsets(BH, ((size_t)Lmax + 3) & ~size_t(3), select_wstride(Lmax));
+  const SelectWs wl = select_ws_offsets(BH, (size_t)Lmax);
   char *ws = (char *)workspace;
   p.hist0 = (int32_t *)(ws + wl.hist0);
-  p.bcnt = (int32_t *)(ws + wl.bcnt);
+  p.gmax = (uint16_t *)(ws + wl.gmax);
   p.scores = (float *)(ws + wl.scores);
-  p.blist = (uint2 *)(ws + wl.blist);
-  p.bgt = (uint32_t *)(ws + wl.bgt);
-  p.wstride = (int32_t)select_wstride(Lmax);
   p.kept_idx = kept_idx;
   p.kept_count = kept_count;
   p.status = (uint32_t *)workspace;
@@ -693,44 +888,41 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
   p.top = top;
   p.recent = recent;
   p.stride = top + recent;
-  p.ldsc = (Lmax + 3) & ~3;
+  p.ldsc = (int32_t)wl.ldsc;
+  p.ldg = (int32_t)wl.ldg;
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e0 = cudaMemsetAsync(p.hist0, 0, wl.scores - wl.hist0, st);
-  if (e0 != cudaSuccess) return set_cuda_error(e0);
-  const dim3 sgrid((Lmax + kScoreTokensPerBlock - 1) / kScoreTokensPerBlock, B * Hkv);
-  if (D == 128)
-    select_score_kernel<128><<<sgrid, kScoreThreads, 0, st>>>(p);
-  else
-    select_score_kernel<64><<<sgrid, kScoreThreads, 0, st>>>(p);
-  {
-    static int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-      cudaError_t ea = cudaFuncSetAttribute(select_topk_kernel,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)topk_smem_bytes(kMaxSelectLmax));
-      if (ea != cudaSuccess) return set_cuda_error(ea);
-      configured[dev] = 1;
-    }
-  }
-  // The bucket and top-k passes are launched as programmatic dependents: each
-  // starts while the grid before it drains and waits on the device for it.
-  cudaLaunchAttribute attr[1];
+  // zero the first-digit histograms; the score pass starts as its
+  // programmatic dependent and waits for it only before adding its counts
+  const int hist4 = (int)(BH * 2048 / 4);
+  select_zero_kernel<<<(hist4 + kZeroThreads - 1) / kZeroThreads, kZeroThreads, 0, st>>>(
+      reinterpret_cast<int4 *>(p.hist0), hist4);
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kCutCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3((Lmax + kBucketSpan - 1) / kBucketSpan, B * Hkv);
-  cfg.blockDim = dim3(kBucketThreads);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, select_bucket_kernel, p);
+  cfg.gridDim = dim3((Lmax + kScoreTokensPerBlock - 1) / kScoreTokensPerBlock, B * Hkv);
+  cfg.blockDim = dim3(kScoreThreads);
+  cudaError_t e = D == 128 ? cudaLaunchKernelEx(&cfg, select_score_kernel<128>, p)
+                           : cudaLaunchKernelEx(&cfg, select_score_kernel<64>, p);
   if (e != cudaSuccess) return set_cuda_error(e);
-  cfg.gridDim = dim3(B * Hkv);
-  cfg.blockDim = dim3(kTopkThreads);
-  cfg.dynamicSmemBytes = topk_smem_bytes(Lmax);
-  e = cudaLaunchKernelEx(&cfg, select_topk_kernel, p);
+  // The cut kernel runs one cluster of kCutCluster blocks per head, as a
+  // programmatic dependent of the score pass: it starts while that grid
+  // drains and waits on the device for it.
+  e = cudaFuncSetAttribute(select_cut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kCutSmemBytes);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  cfg.numAttrs = 2;
+  cfg.gridDim = dim3(kCutCluster, B * Hkv);
+  cfg.blockDim = dim3(kCutThreads);
+  cfg.dynamicSmemBytes = kCutSmemBytes;
+  e = cudaLaunchKernelEx(&cfg, select_cut_kernel, p);
   if (e != cudaSuccess) return set_cuda_error(e);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_cuda_error(e);

@@ -195,13 +195,12 @@ def test_group_size_trades_fragmentation_for_tables(kvx, orc):
 
 def test_select_and_pack_reject_bad_arguments(kvx):
     ws = kvx.kvx_select_workspace_bytes(2, 2, 101)
-    # header | histograms [4][2048] + counts [4] | scores [4][104] | bucket lists
-    # [4][8192] (key, position) | bitmasks [4][4 words], each section 256-aligned
+    # header | histograms [4][2048] | group maxima u16 [4][16] | scores [4][104],
+    # each section 256-aligned (13 groups of 8 rounded up to 16; 101 scores to 104)
     al = lambda x: (x + 255) // 256 * 256
-    scores = al(kvx.KVX_WS_HEADER_BYTES + 4 * 2048 * 4 + 4 * 4)
-    lists = al(scores + 4 * 4 * 104)
-    masks = al(lists + 8 * 4 * 8192)
-    assert ws == al(masks + 4 * 4 * 4)
+    gmax = al(kvx.KVX_WS_HEADER_BYTES + 4 * 2048 * 4)
+    scores = al(gmax + 4 * 2 * 16)
+    assert ws == al(scores + 4 * 4 * 104)
     rc = kvx.lib.kvx_select_topk(256, 256, 256, 2, 8, 2, 96, 100, 10, 4, 256, 256, 256, ws, None)
     assert rc == kvx.KVX_EUNSUPPORTED
     rc = kvx.lib.kvx_select_topk(256, 256, 256, 2, 7, 2, 128, 100, 10, 4, 256, 256, 256, ws, None)

@@ -173,9 +173,10 @@ def test_select_pack_attend_end_to_end(layout):
 
 
 def test_selection_bucket_overflow_and_ragged():
-    """All-equal keys put every candidate in the cut's bucket (more than the
-    kernel keeps in shared memory, so its global fallback runs); ragged
-    lengths end inside a float4, a bitmask word and a streamed chunk."""
+    """All-equal keys put every candidate in the cut's bucket (more than a
+    block keeps in shared memory, so the cut comes from scans of the scores
+    in global memory); ragged lengths end inside a float4, a bitmask word
+    and a block's share of the words."""
     orc = oracle.load()
     q, k, v, L = make(5, 1, 8, 2, 128, [20001], const_keys=True)
     kept, cnt = gpu_select(q, k, L, 300, 7)
@@ -196,9 +197,8 @@ def test_selection_bucket_overflow_and_ragged():
 
 def test_selection_longest_rows():
     """Rows at the library's maximum length (262144) and just past 131072:
-    a head's above-cut bitmask then has more words than the top-k kernel
-    loads in its first chunk, so the remainder of the bitmask is read in
-    the kernel's second loop."""
+    each of the four blocks of a head's cut cluster then owns its largest
+    share of bitmask words (2048)."""
     g = synth.rng(9)
     L = np.array([262144, 131200], np.int32)
     q = synth.normal(g, (2, 4, 128), "bf16")
@@ -212,12 +212,12 @@ def test_selection_longest_rows():
 
 
 def test_selection_cut_bucket_beyond_first_chunk():
-    """Every candidate score lies in one first-digit bucket, with more
-    entries (6436) than the top-k kernel loads in its first chunk (4096)
-    but fewer than the list holds (8192), so the rest of the list is read in
-    the kernel's second loop. The scores 4 (1 + m/128) are exact in fp32 and
-    fp64, so the kept set is unique: the top 2048 with ties at the lower
-    position, then the recent window."""
+    """Every candidate score lies in one first-digit bucket (6436 entries),
+    spread over all four blocks of the head's cut cluster, so the last two
+    digits come from every block's bucket through distributed shared memory
+    and the equal keys at the cut cross block boundaries. The scores
+    4 (1 + m/128) are exact in fp32 and fp64, so the kept set is unique: the
+    top 2048 with ties at the lower position, then the recent window."""
     B, Hq, Hkv, D, L = 1, 8, 2, 128, 6500
     top, recent = 2048, 64
     g = synth.rng(12)
