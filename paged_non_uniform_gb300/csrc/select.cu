@@ -187,7 +187,7 @@ __device__ __forceinline__ void find_digit_warp(const int *hist, int k, uint32_t
   int sum = 0;
 #pragma unroll
   for (int q = 0; q < PER / 4; ++q) {
-    const int4 h = h4[q];
+    const int4 h = h4[(q + lane) % (PER / 4)];  // rotated: eight lanes hit eight bank groups
     sum += h.x + h.y + h.z + h.w;
   }
   int incl = sum;

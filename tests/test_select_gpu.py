@@ -213,11 +213,12 @@ def test_selection_longest_rows():
 
 def test_selection_cut_bucket_beyond_first_chunk():
     """Every candidate score lies in one first-digit bucket (6436 entries),
-    spread over all four blocks of the head's cut cluster, so the last two
-    digits come from every block's bucket through distributed shared memory
-    and the equal keys at the cut cross block boundaries. The scores
-    4 (1 + m/128) are exact in fp32 and fp64, so the kept set is unique: the
-    top 2048 with ties at the lower position, then the recent window."""
+    spread over all four blocks of the head's cut cluster: more than the
+    blocks' warp lists hold, so the last two digits come from scans of the
+    scores in global memory, and the equal keys at the cut cross block
+    boundaries. The scores 4 (1 + m/128) are exact in fp32 and fp64, so the
+    kept set is unique: the top 2048 with ties at the lower position, then
+    the recent window."""
     B, Hq, Hkv, D, L = 1, 8, 2, 128, 6500
     top, recent = 2048, 64
     g = synth.rng(12)
@@ -231,6 +232,35 @@ def test_selection_cut_bucket_beyond_first_chunk():
         ref = orc.select_topk(q[0, 4 * h:4 * h + 4], k[0, h], top, recent)
         assert cnt[h] == ref.size == top + recent
         assert np.array_equal(kept[h, :cnt[h]], ref)
+
+
+def test_selection_many_equal_keys_at_the_cut():
+    """About 500 scattered candidates score exactly 4.03125 and about 500
+    score 4.0; the rest score 1.0. The bucket (about 1000 entries) fits the
+    blocks' lists, so the cluster's leader finds the cut from their keys in
+    its shared memory. More than 32 keys share the cut's top 22 bits, so the
+    last digit comes from a histogram rather than one warp. The top 300 are
+    the 300 lowest positions scoring 4.03125, taken across the four blocks.
+    Every score is exact in fp32 and fp64, so the kept set is unique."""
+    B, Hq, Hkv, D, L = 1, 8, 2, 128, 20000
+    top, recent = 300, 16
+    g = synth.rng(14)
+    q = np.zeros((B, Hq, D), np.float32)
+    q[:, :, 0] = 1.0
+    k = np.zeros((B, Hkv, L, D), np.float32)
+    u = g.random((B, Hkv, L))
+    k[..., 0] = np.where(u < 0.025, 1.0078125, np.where(u < 0.05, 1.0, 0.25))
+    kept, cnt = gpu_select(q, k, np.array([L], np.int32), top, recent)
+    orc = oracle.load()
+    for h in range(Hkv):
+        n = L - recent
+        hi = np.flatnonzero(k[0, h, :n, 0] == 1.0078125)
+        assert hi.size > top
+        exp = np.concatenate([hi[:top], np.arange(n, L)])
+        ref = orc.select_topk(q[0, 4 * h:4 * h + 4], k[0, h], top, recent)
+        assert np.array_equal(ref, exp)
+        assert cnt[h] == exp.size
+        assert np.array_equal(kept[h, :cnt[h]], exp)
 
 
 def test_selection_bad_length_flagged():
