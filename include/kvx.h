@@ -489,8 +489,10 @@ int kvx_frame_get_stats(const kvx_frame *frame, kvx_frame_stats *out);
  *               the call clears on `stream` first).
  * The cut is decided on fp32 scores: positions whose scores lie within fp32
  * rounding of the cut may be exchanged with respect to an exact selection.
- * Launch: a kernel that clears the histograms; the score pass, a
- * programmatic dependent of it that waits only before adding its counts;
+ * Launch: a kernel that clears the histograms, a programmatic dependent of
+ * the work before it on `stream` that waits for that work on the device
+ * before it writes; the score pass, a programmatic dependent of it that
+ * waits only before adding its counts;
  * then the cut pass, a programmatic dependent of the score pass that waits
  * for it on the device: one thread-block cluster of 4 blocks per head (this
  * GPU only). Each block reads only the score groups whose largest first digit

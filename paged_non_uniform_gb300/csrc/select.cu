@@ -73,9 +73,13 @@ struct SelectParams {
   int32_t ldg;                // group row stride: Lmax / 8 rounded up to a multiple of 8
 };
 
-// Clears the first-digit histograms; the score pass may start at once.
+// Clears the first-digit histograms. Launched as a programmatic dependent of
+// whatever precedes the call: it waits for that work to complete (the cut pass
+// of an earlier call may still read the histograms and scores) before it
+// writes or lets the score pass start, which then runs as its dependent.
 constexpr int kZeroThreads = 256;
 __global__ void __launch_bounds__(kZeroThreads) select_zero_kernel(int4 *h, int n4) {
+  pdl_wait();
   pdl_launch_dependents();
   const int i = blockIdx.x * kZeroThreads + threadIdx.x;
   if (i < n4) h[i] = make_int4(0, 0, 0, 0);
@@ -891,11 +895,6 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
   p.ldsc = (int32_t)wl.ldsc;
   p.ldg = (int32_t)wl.ldg;
   cudaStream_t st = (cudaStream_t)stream;
-  // zero the first-digit histograms; the score pass starts as its
-  // programmatic dependent and waits for it only before adding its counts
-  const int hist4 = (int)(BH * 2048 / 4);
-  select_zero_kernel<<<(hist4 + kZeroThreads - 1) / kZeroThreads, kZeroThreads, 0, st>>>(
-      reinterpret_cast<int4 *>(p.hist0), hist4);
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -907,6 +906,16 @@ extern "C" int kvx_select_topk(const void *keys, const void *q, const int32_t *s
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // zero the first-digit histograms; the score pass starts as its
+  // programmatic dependent and waits for it only before adding its counts
+  const int hist4 = (int)(BH * 2048 / 4);
+  cfg.gridDim = dim3((hist4 + kZeroThreads - 1) / kZeroThreads);
+  cfg.blockDim = dim3(kZeroThreads);
+  {
+    const cudaError_t ez = cudaLaunchKernelEx(&cfg, select_zero_kernel,
+                                              reinterpret_cast<int4 *>(p.hist0), hist4);
+    if (ez != cudaSuccess) return set_cuda_error(ez);
+  }
   cfg.gridDim = dim3((Lmax + kScoreTokensPerBlock - 1) / kScoreTokensPerBlock, B * Hkv);
   cfg.blockDim = dim3(kScoreThreads);
   cudaError_t e = D == 128 ? cudaLaunchKernelEx(&cfg, select_score_kernel<128>, p)
