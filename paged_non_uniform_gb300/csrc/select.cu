@@ -86,8 +86,9 @@ __global__ void __launch_bounds__(kZeroThreads) select_zero_kernel(int4 *h, int 
 }
 
 // Score pass: block (x, bh) takes candidates [x * kScoreTokensPerBlock, ...)
-// of head bh. It sums the g query vectors, streams the key rows (LPT lanes per
-// row, U rows in flight per lane), writes the fp32 scores, then counts their
+// of head bh. It issues the loads of each warp's first step of key rows, sums
+// the g query vectors meanwhile, streams the rest (LPT lanes per row, U rows
+// in flight per lane), writes the fp32 scores, then counts their
 // first radix digit (top 11 key bits) and adds the counts to the head's
 // histogram. The same post-pass writes, for every group of 8 positions, the
 // first digit of the group's largest score, so that the cut pass can skip
@@ -108,6 +109,24 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
   const int n = L - p.recent;
   const int t_begin = blockIdx.x * kScoreTokensPerBlock;
   if (t_begin >= n) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = lane / LPT, part = lane % LPT;
+  const uint4 *rows = reinterpret_cast<const uint4 *>(p.keys + (size_t)bh * p.Lmax * D);
+  const int t_end = min(n, t_begin + kScoreTokensPerBlock);
+  constexpr int WARPS = kScoreThreads / 32;
+  constexpr int STEP = WARPS * TPW * U;
+  // the rows of this warp's first step: their loads are in flight while Q is
+  // summed and the counts are cleared
+  auto issue = [&](uint4 (&v)[U], int t0) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = t0 + u * TPW + sub;
+      if (t < t_end) v[u] = __ldcs(rows + (size_t)t * LPT + part);
+    }
+  };
+  uint4 v[U];
+  const int t_first = t_begin + warp * TPW * U;
+  issue(v, t_first);
   for (int d = threadIdx.x; d < D; d += kScoreThreads) {
     float s = 0.f;
     for (int j = 0; j < g; ++j)
@@ -116,21 +135,10 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
   }
   for (int i = threadIdx.x; i < 2048; i += kScoreThreads) hist[i] = 0;
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane / LPT, part = lane % LPT;
   float qv[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) qv[e] = Q[part * 8 + e];
-  const uint4 *rows = reinterpret_cast<const uint4 *>(p.keys + (size_t)bh * p.Lmax * D);
-  const int t_end = min(n, t_begin + kScoreTokensPerBlock);
-  constexpr int WARPS = kScoreThreads / 32;
-  for (int t0 = t_begin + warp * TPW * U; t0 < t_end; t0 += WARPS * TPW * U) {
-    uint4 v[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = t0 + u * TPW + sub;
-      if (t < t_end) v[u] = __ldcs(rows + (size_t)t * LPT + part);
-    }
+  for (int t0 = t_first; t0 < t_end; t0 += STEP) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int t = t0 + u * TPW + sub;
@@ -149,6 +157,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
         s_sc[t - t_begin] = s;
       }
     }
+    if (t0 + STEP < t_end) issue(v, t0 + STEP);
   }
   __syncthreads();
   // first radix digit of every score, counted per block with warp-aggregated

@@ -263,6 +263,42 @@ def test_selection_many_equal_keys_at_the_cut():
         assert np.array_equal(kept[h, :cnt[h]], exp)
 
 
+def test_selection_back_to_back_calls_share_a_workspace():
+    """Two calls on one stream with one workspace and no synchronisation in
+    between, on different keys and into different outputs. The second call's
+    histogram clearing and score pass start as programmatic dependents while
+    the first call's cut may still run; both kept sets must match the
+    oracle."""
+    orc = oracle.load()
+    B, Hq, Hkv, D = 2, 8, 2, 128
+    L = np.array([5000, 3100], np.int32)
+    top, recent = 700, 20
+    runs = []
+    for seed in (21, 22):
+        q, k, v, _ = make(seed, B, Hq, Hkv, D, L)
+        runs.append((q, k))
+    Lmax = int(L.max())
+    ws = torch.zeros(kvx.kvx_select_workspace_bytes(B, Hkv, Lmax) // 4 + 64, dtype=torch.int32,
+                     device="cuda")
+    dev = [(_bf16(k), _bf16(q)) for q, k in runs]
+    sl = torch.from_numpy(L).cuda()
+    outs = [(torch.full((B * Hkv, top + recent), -7, dtype=torch.int32, device="cuda"),
+             torch.zeros(B * Hkv, dtype=torch.int32, device="cuda")) for _ in runs]
+    torch.cuda.synchronize()
+    for (kd, qd), (kept, cnt) in zip(dev, outs):
+        kvx.kvx_select_topk(kd, qd, sl, B, Hq, Hkv, D, Lmax, top, recent, kept, cnt, ws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == 0
+    for (q, k), (kept, cnt) in zip(runs, outs):
+        kept, cnt = kept.cpu().numpy(), cnt.cpu().numpy()
+        for bh in range(B * Hkv):
+            b, h = bh // Hkv, bh % Hkv
+            ref = orc.select_topk(q[b, 4 * h:4 * h + 4], k[b, h, :L[b]], top, recent)
+            assert cnt[bh] == ref.size
+            check_head(orc, q[b, 4 * h:4 * h + 4], k[b, h, :L[b]], top, recent,
+                       kept[bh, :cnt[bh]])
+
+
 def test_selection_bad_length_flagged():
     """A length above Lmax selects nothing for its sequence and sets the
     status bit; the other sequences are unaffected."""
