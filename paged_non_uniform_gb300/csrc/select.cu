@@ -87,20 +87,21 @@ __global__ void __launch_bounds__(kZeroThreads) select_zero_kernel(int4 *h, int 
 
 // Score pass: block (x, bh) takes candidates [x * kScoreTokensPerBlock, ...)
 // of head bh. It issues the loads of each warp's first step of key rows, sums
-// the g query vectors meanwhile, streams the rest (LPT lanes per row, U rows
-// in flight per lane), writes the fp32 scores, then counts their
-// first radix digit (top 11 key bits) and adds the counts to the head's
-// histogram. The same post-pass writes, for every group of 8 positions, the
-// first digit of the group's largest score, so that the cut pass can skip
-// groups below its bucket without reading their scores.
+// the g query vectors meanwhile, then streams the rest (LPT lanes per row, U
+// rows in flight per lane) and writes the fp32 scores. After a step's scores,
+// once the next step's loads are issued, a warp counts their first radix
+// digit (top 11 key bits) in shared memory and writes, for each group of 8
+// positions, the first digit of the group's largest score, so that the cut
+// pass can skip groups below its bucket without reading their scores. At the
+// end the block adds its counts to the head's histogram.
 template <int D>
 __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const SelectParams p) {
   constexpr int LPT = D / 8;          // lanes per token row (16 bytes each)
   constexpr int TPW = 32 / LPT;       // token rows per warp and step
   constexpr int U = 8;                // steps in flight per lane
+  static_assert((U * TPW) % 8 == 0, "score: a warp step covers whole groups of 8 positions");
   __shared__ float Q[D];
   __shared__ int hist[2048];
-  __shared__ float s_sc[kScoreTokensPerBlock];
   pdl_launch_dependents();  // the cut pass may launch; it waits for this grid
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, h = bh - b * p.Hkv;
@@ -138,7 +139,9 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
   float qv[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) qv[e] = Q[part * 8 + e];
+  uint16_t *gm = p.gmax + (size_t)bh * p.ldg;
   for (int t0 = t_first; t0 < t_end; t0 += STEP) {
+    float sv[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int t = t0 + u * TPW + sub;
@@ -152,27 +155,33 @@ __global__ void __launch_bounds__(kScoreThreads, 3) select_score_kernel(const Se
       }
 #pragma unroll
       for (int sh = LPT / 2; sh > 0; sh >>= 1) s += __shfl_xor_sync(0xffffffffu, s, sh);
-      if (part == 0 && t < t_end) {
-        p.scores[(size_t)bh * p.ldsc + t] = s;
-        s_sc[t - t_begin] = s;
-      }
+      sv[u] = s;
+      if (part == 0 && t < t_end) p.scores[(size_t)bh * p.ldsc + t] = s;
     }
     if (t0 + STEP < t_end) issue(v, t0 + STEP);
-  }
-  __syncthreads();
-  // first radix digit of every score, counted per block with warp-aggregated
-  // shared-memory atomics; the largest digit of each group of 8 positions
-  const int cnt_here = t_end - t_begin;
-  uint16_t *gm = p.gmax + (size_t)bh * p.ldg + t_begin / 8;
-  for (int i0 = warp * 32; i0 < cnt_here; i0 += kScoreThreads) {
-    const int i = i0 + lane;
-    const int bin = i < cnt_here ? (int)(order_key(s_sc[i]) >> 21) : -1;
-    const unsigned grp = __match_any_sync(0xffffffffu, bin);
-    if (bin >= 0 && (__ffs(grp) - 1) == lane) atomicAdd(&hist[bin], __popc(grp));
-    int mx = bin;
+    // while those loads are in flight: the step's first digits, and the
+    // largest digit of its groups of 8 positions
+    constexpr int NG = U * TPW / 8;  // groups of 8 positions in a warp step
+    int gmx[NG];
 #pragma unroll
-    for (int sh = 1; sh < 8; sh <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, sh));
-    if ((lane & 7) == 0 && i < cnt_here) gm[i >> 3] = (uint16_t)mx;
+    for (int q = 0; q < NG; ++q) gmx[q] = -1;
+    if (part == 0) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = t0 + u * TPW + sub;
+        if (t < t_end) {
+          const int bin = (int)(order_key(sv[u]) >> 21);
+          atomicAdd(&hist[bin], 1);
+          gmx[(u * TPW) / 8] = max(gmx[(u * TPW) / 8], bin);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+#pragma unroll
+      for (int sh = LPT; sh < 32; sh <<= 1) gmx[q] = max(gmx[q], __shfl_xor_sync(0xffffffffu, gmx[q], sh));
+      if (lane == 0 && t0 + 8 * q < t_end) gm[(t0 + 8 * q) >> 3] = (uint16_t)gmx[q];
+    }
   }
   __syncthreads();
   pdl_wait();  // the histograms have been zeroed
