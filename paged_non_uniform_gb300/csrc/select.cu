@@ -796,7 +796,7 @@ struct PackParams {
 // Kept row i of head (b, h) -> token i of its pages. LPT lanes move one row
 // (16 bytes each of K and V); a thread group handles kPackRows rows spaced
 // rows_per_block apart, with every load issued before the stores.
-constexpr int kPackRows = 4;
+constexpr int kPackRows = 2;
 __global__ void __launch_bounds__(kPackThreads) pack_kept_kernel(const __grid_constant__ PackParams p) {
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, h = bh - b * p.Hkv;
