@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) gather_emit_kernel(const GatherParam
 
 __device__ __forceinline__ void copy_span(const uint8_t *src, uint8_t *dst,
                                           int64_t bytes) {
-  constexpr int U = 4;
+  constexpr int U = 8;
   const int64_t nv = bytes >> 4;
   const uint4 *s = reinterpret_cast<const uint4 *>(src);
   uint4 *d = reinterpret_cast<uint4 *>(dst);
@@ -270,7 +270,7 @@ cudaError_t launch_gather(const GatherParams &p, cudaStream_t st) {
   gather_count_kernel<<<p.S, kThreads, 0, st>>>(p);
   gather_scan_kernel<<<1, kThreads, 0, st>>>(p);
   gather_emit_kernel<<<p.S, kThreads, 0, st>>>(p);
-  gather_copy_kernel<<<4 * sm_count_cached(), kThreads, 0, st>>>(p);
+  gather_copy_kernel<<<8 * sm_count_cached(), kThreads, 0, st>>>(p);
   if (p.flags & KVX_ZERO_TAIL) gather_tail_kernel<<<dim3(p.S, 8), kThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
