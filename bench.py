@@ -113,7 +113,9 @@ def config_of(cfg) -> dict:
                   f"{cfg.kv_bytes_step() / 1e9:.1f} GB of distinct KV pages",
             "plan": "balanced ahead-of-time split, two persistent blocks per SM",
             "step": "one replay of a CUDA graph holding the step's kvx_decode_attn launches "
-                    "(one per layer, captured from the C-ABI calls)"}
+                    "(one per layer, captured from the C-ABI calls)",
+            "early_kv": "on: each launch's load warps fill their rings before the previous "
+                        "launch completes, which writes no page or page table"}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -403,6 +405,10 @@ class DecodeSetup:
             p = kvx.kvx_plan_create(cfg.B, cfg.Hq, cfg.Hkv, cfg.D, cfg.P, cfg.num_groups, dtype,
                                     cfg.budget[l], cfg.seq_len, cfg.head_group[l], 0)
             kvx.kvx_plan_upload(p)
+            # the step's kernels are these attention launches, and none of them
+            # writes pages or page tables: the load warps may start before the
+            # previous layer's launch has completed (kvx_plan_set_early_kv)
+            p.set_early_kv(True)
             self.plan_us.append(p.stats()["plan_us"])
             self.plans.append(p)
             self.layers.append(TableLayer(cfg, l, table, p.group_pages(), seed=0, device=dev))

@@ -256,6 +256,23 @@ int kvx_plan_set_trace(kvx_plan *plan, int64_t *dev_trace);
  * off (the limit stays as given). Errors: KVX_EINVAL, KVX_ERANGE. */
 int kvx_plan_inject_stall(kvx_plan *plan, int32_t block, uint64_t wait_limit_ns);
 
+/* Early K/V loads (off by default; tensor-core kernel). The decode call is
+ * launched as a programmatic dependent of the kernel before it on the stream,
+ * and waits for that kernel on the device before it reads its inputs. With
+ * enable = 1, each block's load warp reads page-table entries and K/V pages
+ * before that wait: it fills its empty ring with its first stages, except a
+ * stage that holds a head's newest page (the page of its last kept token),
+ * and waits before anything else. q, seq_len and head_budget are still read
+ * after the wait, and the L2 warm-up of short launches is skipped.
+ * Precondition: if the kernel before the call lets its dependents start early
+ * (programmatic dependent launch), it writes none of the page-table entries
+ * or K/V pages the call reads, except each head's newest page. An ordinary
+ * kernel lets its dependents start only when it has completed, so any kernel
+ * qualifies that does not use programmatic launch; so do the library's own
+ * kernels, none of which write pages or page tables while a dependent may run.
+ * enable: 0 or 1. Errors: KVX_EINVAL. */
+int kvx_plan_set_early_kv(kvx_plan *plan, int32_t enable);
+
 void kvx_plan_destroy(kvx_plan *plan);
 
 /* ---------------------------------------------------------------------------

@@ -175,7 +175,9 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   p.cluster = plan->cluster;
   p.stall_block = plan->stall_block;
   p.wait_ns = plan->wait_ns;
-  p.pf_tokens = plan->pf_tokens;
+  p.early_kv = plan->early_kv;
+  // with early loads into the ring, the L2 warm-up only competes with them
+  p.pf_tokens = plan->early_kv ? 0 : plan->pf_tokens;
   const float sc = scale == 0.f ? 1.0f / std::sqrt((float)D) : scale;
   p.scale_log2 = (float)((double)sc * 1.4426950408889634);
 

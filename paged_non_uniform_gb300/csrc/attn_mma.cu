@@ -365,7 +365,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   // be read before the wait too.
   Item item0{};
   if (it0 < it1) item0 = p.items[it0];
-  pdl_wait();
+  if (!(p.early_kv && warp == kCons)) pdl_wait();  // an early producer waits later
 
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
@@ -374,6 +374,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     const uint32_t box_bytes = (uint32_t)box_h * 128u * C::kHalves;
     int gs = 0;
     bool dead = false;
+    bool waited = !p.early_kv;
     for (int it = it0; it < it1 && !dead; ++it) {
       const Item item = it == it0 ? item0 : p.items[it];
       const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
@@ -383,6 +384,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
       const void *tmk = &p.tmK[gi];
       const void *tmv = &p.tmV[gi];
       const int maxpg = (item.end - 1) / P;
+      const int last_pg = (__ldg(p.n_plan + item.bh) - 1) / P;  // the head's newest page
       int win = -1;
       int32_t my_page = 0;
       for (int t0 = item.begin; t0 < item.end; t0 += kStageTokens, ++gs) {
@@ -390,10 +392,20 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
         const int valid = min(kStageTokens, item.end - t0);
         const int nbox = (valid + box_h - 1) / box_h;
         const int pg_last = (t0 + valid - 1) / P;
+        // Early loads (kvx_plan_set_early_kv): before the preceding kernel has
+        // completed, only stages clear of the head's newest page load, and
+        // only into the empty ring; the page-table window is read again after
+        // the wait.
+        if (!waited && (gs >= kStages || pg_last >= last_pg)) {
+          pdl_wait();
+          waited = true;
+          win = -1;
+        }
         if (win < 0 || pg_last >= win + 32) {
           win = t0 / P;
           const int idx = win + lane;
-          my_page = idx <= maxpg ? __ldg(pt + idx) : 0;
+          // through L2 only: an early read must leave no stale copy in L1
+          my_page = idx <= maxpg ? __ldcg(pt + idx) : 0;
         }
         if (gs >= kStages) {
           bool ok = true;
@@ -443,6 +455,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
         }
       }
     }
+    if (!waited) pdl_wait();
     // Do not leave while a load of ours may still be landing.
     if (lane == 0) {
       const int issued = gs;

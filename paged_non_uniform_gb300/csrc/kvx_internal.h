@@ -91,6 +91,7 @@ struct alignas(128) AttnParams {
   int32_t cluster;             // blocks per thread-block cluster (1: no clusters)
   int32_t stall_block;         // failure-detection test: block whose first stage gets no loads (-1: none)
   int32_t pf_tokens;           // tokens per block warmed into L2 before the dependency wait
+  int32_t early_kv;            // 1: the producer may fill its ring before the dependency wait
   uint64_t wait_ns;            // limit of every pipeline wait
   int8_t head_grp[KVX_MAX_KV_HEADS];
   int8_t head_row[KVX_MAX_KV_HEADS];
@@ -169,4 +170,5 @@ struct kvx_plan {
   int32_t stall_block;  // kvx_plan_inject_stall
   uint64_t wait_ns;
   int32_t pf_tokens;    // tokens per block warmed into L2 before the dependency wait
+  int32_t early_kv;     // kvx_plan_set_early_kv
 };

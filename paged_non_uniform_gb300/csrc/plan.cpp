@@ -420,6 +420,7 @@ extern "C" int kvx_plan_create(const kvx_shape *s, const int32_t *head_budget,
     p->cover_stride = 0;
     p->stall_block = -1;
     p->wait_ns = 2000000000ull;
+    p->early_kv = 0;
     p->pf_tokens = 0;
     // Deterministic Budget Allocation: n = min(L, budget).
     p->n.resize((size_t)B * Hkv);
@@ -640,6 +641,12 @@ extern "C" int kvx_plan_inject_stall(kvx_plan *p, int32_t block, uint64_t wait_l
   if (wait_limit_ns < 1000000ull || wait_limit_ns > 10000000000ull) return KVX_ERANGE;
   p->stall_block = block < 0 ? -1 : block;
   p->wait_ns = wait_limit_ns;
+  return KVX_OK;
+}
+
+extern "C" int kvx_plan_set_early_kv(kvx_plan *p, int32_t enable) {
+  if (!p || enable < 0 || enable > 1) return KVX_EINVAL;
+  p->early_kv = enable;
   return KVX_OK;
 }
 

@@ -101,6 +101,7 @@ lib.kvx_plan_set_trace.argtypes = [_vp, _vp]
 lib.kvx_plan_coverage.argtypes = [_vp, _vp]
 lib.kvx_plan_set_coverage_record.argtypes = [_vp, _vp, _c.c_int32]
 lib.kvx_plan_inject_stall.argtypes = [_vp, _c.c_int32, _c.c_uint64]
+lib.kvx_plan_set_early_kv.argtypes = [_vp, _c.c_int32]
 lib.kvx_plan_destroy.argtypes = [_vp]
 lib.kvx_plan_destroy.restype = None
 lib.kvx_decode_attn.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c.c_float, _vp,
@@ -231,6 +232,11 @@ class Plan:
         t = np.zeros(max(st["num_ctas"], 1), dtype=np.int64)
         _check(lib.kvx_plan_cta_tokens(self.handle, t.ctypes.data), "kvx_plan_cta_tokens")
         return t[:st["num_ctas"]]
+
+    def set_early_kv(self, enable: bool) -> None:
+        """kvx_plan_set_early_kv: let the load warp fill its ring before the
+        dependency wait (see the header for the precondition)."""
+        _check(lib.kvx_plan_set_early_kv(self.handle, 1 if enable else 0), "kvx_plan_set_early_kv")
 
     def set_trace(self, dev_trace) -> None:
         _check(lib.kvx_plan_set_trace(self.handle, _dptr(dev_trace)), "kvx_plan_set_trace")

@@ -193,6 +193,18 @@ def test_group_size_trades_fragmentation_for_tables(kvx, orc):
     assert entries == sorted(entries, reverse=True)
 
 
+def test_early_kv_setter(kvx):
+    """kvx_plan_set_early_kv takes 0 or 1 on a plan; anything else is
+    KVX_EINVAL (a NULL plan too)."""
+    case = synth.tiny(0)
+    plan = _plan(kvx, case, num_ctas=2)
+    assert kvx.lib.kvx_plan_set_early_kv(plan.handle, 1) == kvx.KVX_OK
+    assert kvx.lib.kvx_plan_set_early_kv(plan.handle, 0) == kvx.KVX_OK
+    assert kvx.lib.kvx_plan_set_early_kv(plan.handle, 2) == kvx.KVX_EINVAL
+    assert kvx.lib.kvx_plan_set_early_kv(plan.handle, -1) == kvx.KVX_EINVAL
+    assert kvx.lib.kvx_plan_set_early_kv(None, 1) == kvx.KVX_EINVAL
+
+
 def test_select_and_pack_reject_bad_arguments(kvx):
     ws = kvx.kvx_select_workspace_bytes(2, 2, 101)
     # header | histograms [4][2048] | group maxima u16 [4][16] | scores [4][104],
