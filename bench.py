@@ -193,14 +193,25 @@ def oracle_timing(cfg, seconds):
             f"time, OpenMP over the {heads} (sequence, KV head) pairs")
 
 
+def oracle_layer_step(name, rate_gbs):
+    """The oracle's time for the whole of layer 0 of a workload at the rate
+    it measured on its batch, and the same times the workload's layer count:
+    an extrapolation, not a timed step."""
+    full = synth.decode_config(name, seed=0)
+    layer_s = full.kv_bytes_layer(0) / (rate_gbs * 1e9)
+    return {"layer_s": layer_s, "step_s_extrapolated": layer_s * full.layers,
+            "layers": full.layers}
+
+
 def cpu_baseline(cfg, seconds, extra=()):
     value, cores, sample = oracle_timing(cfg, seconds)
     out = {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
-           "workloads": {}}
+           **oracle_layer_step(cfg.name, value), "workloads": {}}
     for name in extra:
         c = synth.decode_config(name, seed=0, layers=1)
         v, cr, smp = oracle_timing(c, seconds)
-        out["workloads"][name] = {"value": v, "unit": "GB/s", "cores": cr, "sample": smp}
+        out["workloads"][name] = {"value": v, "unit": "GB/s", "cores": cr, "sample": smp,
+                                  **oracle_layer_step(name, v)}
     return out
 
 

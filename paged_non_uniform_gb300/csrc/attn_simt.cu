@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kWarps * 32)
   constexpr int EPL = Vec16<T>::kN;  // elements per lane per 16-byte load
   constexpr int LPT = D / EPL;       // lanes per token row
   constexpr int TPW = 32 / LPT;      // tokens per warp step
+  constexpr int U = EPL == 4 ? 4 : 2;  // warp steps whose rows are in flight together
   static_assert(LPT >= 1 && LPT <= 32 && 32 % LPT == 0, "a row must tile the warp");
   constexpr int MW = 8 * D + 16;     // floats per warp record
   __shared__ float merge[2][kWarps][MW];
@@ -98,42 +99,57 @@ __global__ void __launch_bounds__(kWarps * 32)
       for (int e = 0; e < EPL; ++e) o[j][e] = qv[j][e] = 0.f;
       if (j < g) Vec16<T>::load(qb + (size_t)j * D, qv[j]);
     }
-    for (int t0 = item.begin + warp * TPW; t0 < item.end; t0 += kWarps * TPW) {
-      const int t = t0 + grp;
-      const bool active = t < item.end;
-      float kv[EPL], vv[EPL];
+    // U warp steps per batch: their page ids, then all their K and V rows,
+    // are loaded before any of them is used, so a short item costs one or two
+    // memory round trips instead of two per warp step. Lane group grp still
+    // takes tokens begin + warp*TPW + grp + k*kWarps*TPW in increasing k.
+    for (int tb = item.begin + warp * TPW; tb < item.end; tb += U * kWarps * TPW) {
+      int32_t page[U];
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) kv[e] = vv[e] = 0.f;
-      if (active) {
-        const int32_t page = __ldg(pt + t / P);
-        if (page < 0 || (int64_t)page >= gd.num_pages) {
-          if (gl == 0) atomicOr(p.status, KVX_DEV_BAD_PAGE);
-        } else {
-          const size_t rr = p.layout == KVX_LAYOUT_HEAD_MAJOR
-                                ? ((size_t)page * gd.size + row) * P + (t & (P - 1))
-                                : ((size_t)page * P + (t & (P - 1))) * gd.size + row;
-          Vec16<T>::load(kp + rr * D + gl * EPL, kv);
-          Vec16<T>::load(vp + rr * D + gl * EPL, vv);
+      for (int u = 0; u < U; ++u) {
+        const int t = tb + u * kWarps * TPW + grp;
+        page[u] = t < item.end ? __ldg(pt + t / P) : 0;
+      }
+      float kv[U][EPL], vv[U][EPL];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int t = tb + u * kWarps * TPW + grp;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) kv[u][e] = vv[u][e] = 0.f;
+        if (t < item.end) {
+          if (page[u] < 0 || (int64_t)page[u] >= gd.num_pages) {
+            if (gl == 0) atomicOr(p.status, KVX_DEV_BAD_PAGE);
+          } else {
+            const size_t rr = p.layout == KVX_LAYOUT_HEAD_MAJOR
+                                  ? ((size_t)page[u] * gd.size + row) * P + (t & (P - 1))
+                                  : ((size_t)page[u] * P + (t & (P - 1))) * gd.size + row;
+            Vec16<T>::load(kp + rr * D + gl * EPL, kv[u]);
+            Vec16<T>::load(vp + rr * D + gl * EPL, vv[u]);
+          }
+          // Coverage record (test hook): one count per token fed to the softmax.
+          if (p.cover && gl == 0) atomicAdd(p.cover + (size_t)item.bh * p.cover_stride + t, 1);
         }
-        // Coverage record (test hook): one count per token fed to the softmax.
-        if (p.cover && gl == 0) atomicAdd(p.cover + (size_t)item.bh * p.cover_stride + t, 1);
       }
 #pragma unroll
-      for (int j = 0; j < KVX_MAX_GQA; ++j) {
-        if (j >= g) break;
-        float dot = 0.f;
+      for (int u = 0; u < U; ++u) {
+        const bool active = tb + u * kWarps * TPW + grp < item.end;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) dot = fmaf(qv[j][e], kv[e], dot);
+        for (int j = 0; j < KVX_MAX_GQA; ++j) {
+          if (j >= g) break;
+          float dot = 0.f;
 #pragma unroll
-        for (int sh = LPT / 2; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
-        if (active) {
-          const float x = dot * p.scale_log2;
-          const float mn = fmaxf(m[j], x);
-          const float al = ex2(m[j] - mn), pw = ex2(x - mn);
-          l[j] = l[j] * al + pw;
+          for (int e = 0; e < EPL; ++e) dot = fmaf(qv[j][e], kv[u][e], dot);
 #pragma unroll
-          for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(o[j][e], al, pw * vv[e]);
-          m[j] = mn;
+          for (int sh = LPT / 2; sh > 0; sh >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, sh);
+          if (active) {
+            const float x = dot * p.scale_log2;
+            const float mn = fmaxf(m[j], x);
+            const float al = ex2(m[j] - mn), pw = ex2(x - mn);
+            l[j] = l[j] * al + pw;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(o[j][e], al, pw * vv[u][e]);
+            m[j] = mn;
+          }
         }
       }
     }
