@@ -112,7 +112,6 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
   kvx_plan_workspace_bytes(plan, &need);
   if (workspace_bytes < need || !aligned(workspace, 256)) return KVX_EINVAL;
   if (!std::isfinite(scale) || scale < 0.f) return KVX_EINVAL;
-  const size_t es = s.dtype == KVX_BF16 ? 2 : 4;
   if (!aligned(q, 16) || !aligned(out, 16)) return KVX_EINVAL;
 
   AttnParams p;
@@ -141,7 +140,6 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
         return set_cuda_error(cudaErrorInvalidValue);
     }
   }
-  (void)es;
   for (int h = 0; h < s.Hkv; ++h) {
     p.head_grp[h] = (int8_t)plan->head_group[h];
     p.head_row[h] = (int8_t)plan->head_row[h];
@@ -277,7 +275,9 @@ extern "C" int kvx_gather_read_runs(const void *workspace, int32_t S,
   }
   std::memset(runs, 0, sizeof(int32_t) * 3 * (size_t)S * (size_t)max_blocks);
   for (int s = 0; s < S; ++s) {
-    for (int r = 0; r < run_count[s]; ++r) {
+    // the counts come from the device: never index past either array
+    const int64_t n = std::min<int64_t>({run_count[s], max_blocks, total - off[s]});
+    for (int r = 0; r < n; ++r) {
       const int4 &d = all[(size_t)off[s] + r];
       int32_t *o = runs + ((size_t)s * max_blocks + r) * 3;
       o[0] = d.x;
