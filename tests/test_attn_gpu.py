@@ -237,14 +237,12 @@ def test_calls_captured_in_a_cuda_graph_replay_bit_exact(kernel):
         assert max_abs(ref, oracle_out(c)) <= TOL_BF16
 
 
-def test_early_kv_loads_are_bit_exact_back_to_back():
-    """kvx_plan_set_early_kv: the load warps fill their rings before the
-    preceding launch completes. Layers launched back to back on one stream,
-    each a programmatic dependent of the one before, give the same bits with
-    early loads as without them, in direct calls and in a graph replay; the
-    outputs match the oracle."""
-    cases = [qwen3_like(31), sparse_like(32), qwen25_like(33), g8_p8(34), p64(35)]
-    devs = [DeviceCase(c, make_plan(c, num_ctas=n)) for c, n in zip(cases, (0, 40, 17, 0, 9))]
+def _early_kv_back_to_back(cases, devs):
+    """Runs the layers once without early loads (reference bits, checked
+    against the oracle), then with kvx_plan_set_early_kv on: three rounds of
+    direct calls launched back to back on one stream (each a programmatic
+    dependent of the one before) and three replays of a captured graph of
+    them. Every output must equal the reference bit for bit."""
     ref = [d.run() for d in devs]
     for d, c, r in zip(devs, cases, ref):
         assert max_abs(r, oracle_out(c)) <= TOL_BF16
@@ -276,6 +274,33 @@ def test_early_kv_loads_are_bit_exact_back_to_back():
         torch.cuda.synchronize()
         for o, r in zip(outs, ref):
             assert np.array_equal(o.cpu().numpy(), r)
+    for d in devs:
+        assert d.status() == 0
+
+
+def test_early_kv_loads_are_bit_exact_back_to_back():
+    """kvx_plan_set_early_kv: the load warps fill their rings before the
+    preceding launch completes. Layers launched back to back give the same
+    bits with early loads as without them, in direct calls and in a graph
+    replay; the outputs match the oracle."""
+    cases = [qwen3_like(31), sparse_like(32), qwen25_like(33), g8_p8(34), p64(35)]
+    devs = [DeviceCase(c, make_plan(c, num_ctas=n)) for c, n in zip(cases, (0, 40, 17, 0, 9))]
+    _early_kv_back_to_back(cases, devs)
+
+
+def test_early_kv_loads_with_token_major_pages_and_cluster_layouts():
+    """The same with KV-RM's token-major pages and with thread-block cluster
+    layouts (their merging blocks wait on an inbox as well), mixed in one
+    stream of back-to-back launches."""
+    cases = [qwen3_like(41), sparse_like(42), qwen25_like(43), sparse_like(44), p64(45)]
+    plans = [make_plan(cases[0], num_ctas=11, layout=kvx.KVX_LAYOUT_TOKEN_MAJOR),
+             make_plan(cases[1], num_ctas=16, policy=kvx.KVX_PLAN_CLUSTER_4),
+             make_plan(cases[2], num_ctas=16, policy=kvx.KVX_PLAN_CLUSTER_8),
+             make_plan(cases[3], num_ctas=12, policy=kvx.KVX_PLAN_CLUSTER_2,
+                       layout=kvx.KVX_LAYOUT_TOKEN_MAJOR),
+             make_plan(cases[4], num_ctas=0)]
+    devs = [DeviceCase(c, p) for c, p in zip(cases, plans)]
+    _early_kv_back_to_back(cases, devs)
 
 
 def test_pipeline_wait_runs_out_and_is_reported():

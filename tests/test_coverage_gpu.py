@@ -59,6 +59,17 @@ def test_fp32_coverage_record_is_exact(grouping, policy, num_ctas):
     assert max_abs(got, oracle_out(case)) <= TOL_F32
 
 
+@pytest.mark.parametrize("name", ["qwen3_like", "sparse_like", "p64"])
+def test_coverage_record_is_exact_with_early_kv_loads(name):
+    """Early K/V loads (kvx_plan_set_early_kv) change when the load warp
+    issues a stage, not which tokens the consumers feed to the softmax."""
+    case = BF16_CASES[name](2)
+    plan = make_plan(case, num_ctas=0)
+    plan.set_early_kv(True)
+    got, _ = run_with_record(case, plan)
+    assert max_abs(got, oracle_out(case)) <= TOL_BF16
+
+
 def test_coverage_record_accumulates_and_turns_off():
     """Two calls with the record on count every kept token twice; a call with
     it off adds nothing."""
