@@ -266,7 +266,9 @@ int kvx_plan_inject_stall(kvx_plan *plan, int32_t block, uint64_t wait_limit_ns)
  * after the wait, and the L2 warm-up of short launches is skipped.
  * Precondition: if the kernel before the call lets its dependents start early
  * (programmatic dependent launch), it writes none of the page-table entries
- * or K/V pages the call reads, except each head's newest page. An ordinary
+ * or K/V pages the call reads, except each head's newest page and that page's
+ * page-table entry (the load warp reads the entries again after the wait and
+ * loads the newest page only then). An ordinary
  * kernel lets its dependents start only when it has completed, so any kernel
  * qualifies that does not use programmatic launch; so do the library's own
  * kernels, none of which write pages or page tables while a dependent may run.
