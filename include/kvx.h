@@ -547,6 +547,40 @@ int kvx_pack_kept(const kvx_plan *plan, const void *keys, const void *values,
                   size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * kvx_decode_attn_kept -- decode attention straight over the kept rows of a
+ * dense cache, without packing them into pages first. The result is that of
+ * kvx_decode_attn over the pages kvx_pack_kept would fill from the same kept
+ * lists with the same plan, bit for bit: the same items, the same stages of
+ * 32 kept tokens, the same arithmetic ("KVDrive", Fig. 7: decode attends to
+ * each head's selected critical entries; Tangram, Fig. 13: the plan's split).
+ *   plan        bf16 plan whose kept count n[b][h] is the number of entries of
+ *               head (b, h)'s kept list that it attends to (for example
+ *               kvx_select_topk's kept_count passed as head_budget to
+ *               kvx_plan_create); any page size and work-split policy.
+ *   q, out, head_budget, seq_len, scale, workspace: as for kvx_decode_attn.
+ *   keys, values  device bf16 [B][Hkv][Lmax][D], 16-byte aligned.
+ *   kept_idx    device int32 [B*Hkv][kept_stride]: token i of head
+ *               bh = b*Hkv + h is row kept_idx[bh*kept_stride + i] of that
+ *               head's keys and values, for i < n[b][h]; any order. An index
+ *               outside [0, Lmax) reads as a zero row and sets KVX_DEV_BAD_BLOCK
+ *               in the workspace status word.
+ * Launch: as kvx_decode_attn, except that the load warps read the kept list
+ * only after the dependency wait (it usually comes from the kernel before,
+ * e.g. kvx_select_topk), so kvx_plan_set_early_kv and the L2 warm-up of short
+ * launches do not apply. Each load warp copies a stage's 32 rows of K and V
+ * with 16-byte asynchronous copies (cp.async) that arrive on the stage's
+ * barrier as they land.
+ * Errors: KVX_EINVAL, KVX_ERANGE (kept_stride below the plan's largest kept
+ * count), KVX_ESTATE, KVX_EUNSUPPORTED (fp32 plans, CUDA-core kernel plans),
+ * KVX_ECUDA.
+ * ------------------------------------------------------------------------- */
+int kvx_decode_attn_kept(const kvx_plan *plan, const void *q, const void *keys,
+                         const void *values, int32_t Lmax, const int32_t *kept_idx,
+                         int32_t kept_stride, const int32_t *head_budget,
+                         const int32_t *seq_len, float scale, float *out, void *workspace,
+                         size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * kvx_gather_coalesce_noalloc -- kvx_gather_coalesce without a workspace.
  *
  * The pages have no counterpart of this entry point: it exists for callers

@@ -92,6 +92,61 @@ extern "C" const char *kvx_status_string(int s) {
 
 extern "C" int kvx_last_cuda_error(void) { return g_last_cuda_error; }
 
+namespace kvx {
+
+// Checks and fills what both decode entry points share: the plan, q, out,
+// the per-call device arrays, the workspace and the scale.
+static int attn_common(const kvx_plan *plan, const void *q, const int32_t *head_budget,
+                       const int32_t *seq_len, float scale, float *out, void *workspace,
+                       size_t workspace_bytes, AttnParams &p) {
+  if (!plan || !q || !head_budget || !seq_len || !out || !workspace) return KVX_EINVAL;
+  if (!plan->d_buf) return KVX_ESTATE;
+  const kvx_shape &s = plan->shape;
+  size_t need = 0;
+  kvx_plan_workspace_bytes(plan, &need);
+  if (workspace_bytes < need || !aligned(workspace, 256)) return KVX_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.f) return KVX_EINVAL;
+  if (!aligned(q, 16) || !aligned(out, 16)) return KVX_EINVAL;
+  std::memset(&p, 0, sizeof(p));
+  for (int h = 0; h < s.Hkv; ++h) {
+    p.head_grp[h] = (int8_t)plan->head_group[h];
+    p.head_row[h] = (int8_t)plan->head_row[h];
+  }
+  char *ws = (char *)workspace;
+  const AttnWs lay = attn_ws_layout(plan);
+  p.items = plan->d_items;
+  p.cta_off = plan->d_cta_off;
+  p.split = plan->d_split;
+  p.counters = (int32_t *)(ws + lay.counters);
+  p.n_plan = plan->d_n;
+  p.head_budget = head_budget;
+  p.seq_len = seq_len;
+  p.q = q;
+  p.out = out;
+  p.status = (uint32_t *)ws;
+  p.part_ml = (float2 *)(ws + lay.part_ml);
+  p.part_o = (float *)(ws + lay.part_o);
+  p.trace = plan->d_trace;
+  p.cover = plan->d_cover;
+  p.cover_stride = plan->cover_stride;
+  p.B = s.B;
+  p.Hq = s.Hq;
+  p.Hkv = s.Hkv;
+  p.D = s.D;
+  p.g = s.Hq / s.Hkv;
+  p.P = s.page_size;
+  p.num_groups = s.num_groups;
+  p.layout = s.layout;
+  p.cluster = plan->cluster;
+  p.stall_block = plan->stall_block;
+  p.wait_ns = plan->wait_ns;
+  const float sc = scale == 0.f ? 1.0f / std::sqrt((float)s.D) : scale;
+  p.scale_log2 = (float)((double)sc * 1.4426950408889634);
+  return KVX_OK;
+}
+
+}  // namespace kvx
+
 extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
                                const void *const *k_pools,
                                const void *const *v_pools,
@@ -102,20 +157,14 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
                                const int32_t *seq_len, float scale, float *out,
                                void *workspace, size_t workspace_bytes,
                                void *stream) {
-  if (!plan || !q || !k_pools || !v_pools || !pool_pages || !page_tables ||
-      !page_table_stride || !head_budget || !seq_len || !out || !workspace)
+  if (!k_pools || !v_pools || !pool_pages || !page_tables || !page_table_stride)
     return KVX_EINVAL;
-  if (!plan->d_buf) return KVX_ESTATE;
+  AttnParams p;
+  const int rc = attn_common(plan, q, head_budget, seq_len, scale, out, workspace,
+                             workspace_bytes, p);
+  if (rc != KVX_OK) return rc;
   const kvx_shape &s = plan->shape;
   const int G = s.num_groups, B = s.B, P = s.page_size, D = s.D;
-  size_t need = 0;
-  kvx_plan_workspace_bytes(plan, &need);
-  if (workspace_bytes < need || !aligned(workspace, 256)) return KVX_EINVAL;
-  if (!std::isfinite(scale) || scale < 0.f) return KVX_EINVAL;
-  if (!aligned(q, 16) || !aligned(out, 16)) return KVX_EINVAL;
-
-  AttnParams p;
-  std::memset(&p, 0, sizeof(p));
   for (int gi = 0; gi < G; ++gi) {
     if (!k_pools[gi] || !v_pools[gi] || !page_tables[gi]) return KVX_EINVAL;
     if (!aligned(k_pools[gi], 16) || !aligned(v_pools[gi], 16)) return KVX_EINVAL;
@@ -140,49 +189,45 @@ extern "C" int kvx_decode_attn(const kvx_plan *plan, const void *q,
         return set_cuda_error(cudaErrorInvalidValue);
     }
   }
-  for (int h = 0; h < s.Hkv; ++h) {
-    p.head_grp[h] = (int8_t)plan->head_group[h];
-    p.head_row[h] = (int8_t)plan->head_row[h];
-  }
-  const int g = s.Hq / s.Hkv;
-  char *ws = (char *)workspace;
-  const AttnWs lay = attn_ws_layout(plan);
-  p.items = plan->d_items;
-  p.cta_off = plan->d_cta_off;
-  p.split = plan->d_split;
-  p.counters = (int32_t *)(ws + lay.counters);
-  p.n_plan = plan->d_n;
-  p.head_budget = head_budget;
-  p.seq_len = seq_len;
-  p.q = q;
-  p.out = out;
-  p.status = (uint32_t *)ws;
-  p.part_ml = (float2 *)(ws + lay.part_ml);
-  p.part_o = (float *)(ws + lay.part_o);
-  p.trace = plan->d_trace;
-  p.cover = plan->d_cover;
-  p.cover_stride = plan->cover_stride;
-  p.B = B;
-  p.Hq = s.Hq;
-  p.Hkv = s.Hkv;
-  p.D = D;
-  p.g = g;
-  p.P = P;
-  p.num_groups = G;
-  p.layout = s.layout;
-  p.cluster = plan->cluster;
-  p.stall_block = plan->stall_block;
-  p.wait_ns = plan->wait_ns;
   p.early_kv = plan->early_kv;
   // with early loads into the ring, the L2 warm-up only competes with them
   p.pf_tokens = plan->early_kv ? 0 : plan->pf_tokens;
-  const float sc = scale == 0.f ? 1.0f / std::sqrt((float)D) : scale;
-  p.scale_log2 = (float)((double)sc * 1.4426950408889634);
 
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = plan->kernel == KVX_KERNEL_MMA
                       ? launch_attn_mma(p, plan->num_ctas, st)
                       : launch_attn_simt(p, s.dtype, plan->num_ctas, st);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return KVX_OK;
+}
+
+extern "C" int kvx_decode_attn_kept(const kvx_plan *plan, const void *q, const void *keys,
+                                    const void *values, int32_t Lmax,
+                                    const int32_t *kept_idx, int32_t kept_stride,
+                                    const int32_t *head_budget, const int32_t *seq_len,
+                                    float scale, float *out, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+  if (!keys || !values || !kept_idx) return KVX_EINVAL;
+  AttnParams p;
+  const int rc = attn_common(plan, q, head_budget, seq_len, scale, out, workspace,
+                             workspace_bytes, p);
+  if (rc != KVX_OK) return rc;
+  if (plan->shape.dtype != KVX_BF16 || plan->kernel != KVX_KERNEL_MMA) return KVX_EUNSUPPORTED;
+  if (Lmax < 1 || kept_stride < 1) return KVX_EINVAL;
+  if (!aligned(keys, 16) || !aligned(values, 16)) return KVX_EINVAL;
+  int32_t maxn = 0;
+  for (int32_t v : plan->n) maxn = std::max(maxn, v);
+  if (maxn > kept_stride) return KVX_ERANGE;
+  p.kept = kept_idx;
+  p.kdense = keys;
+  p.vdense = values;
+  p.kept_stride = kept_stride;
+  p.Lmax = Lmax;
+  // the kept list comes from the work before the call: no loads before the
+  // dependency wait, and no L2 warm-up (it walks page tables)
+  p.early_kv = 0;
+  p.pf_tokens = 0;
+  cudaError_t e = launch_attn_mma(p, plan->num_ctas, (cudaStream_t)stream);
   if (e != cudaSuccess) return set_cuda_error(e);
   return KVX_OK;
 }

@@ -83,6 +83,80 @@ struct Cfg {
   static constexpr int kSmemCluster = kSmem + 16;
 };
 
+// Load warp of kept-row attention (kvx_decode_attn_kept). Token i of head bh
+// is row kept[bh * kept_stride + i] of the dense caches. Lane j copies row
+// kept[t0 + j] of K and V into row j of the stage, into the same swizzled
+// [half][row][128 B] tiles that one 32-row bulk-tensor box lands in (16-byte
+// chunk c of row j goes to chunk c ^ (j & 7)), as 16-byte asynchronous
+// copies; every lane's copies arrive on the stage's barrier as they land, and
+// lane 0's plain arrival, made after all lanes have registered theirs, is the
+// one the barrier was initialised to expect. The next stage's kept entries
+// load while the warp waits for the stage's slot. An index outside
+// [0, Lmax) loads a zero row and sets KVX_DEV_BAD_BLOCK.
+template <int D>
+__device__ __forceinline__ void produce_kept(const AttnParams &p, int it0, int it1,
+                                             const Item &item0, uint32_t stage0,
+                                             uint32_t full0, uint32_t empty0,
+                                             volatile int *abort_flag, uint64_t pol, int lane,
+                                             int &gs, bool &dead) {
+  using C = Cfg<D>;
+  for (int it = it0; it < it1 && !dead; ++it) {
+    const Item item = it == it0 ? item0 : p.items[it];
+    const int32_t *kl = p.kept + (size_t)item.bh * p.kept_stride;
+    const size_t head_row0 = (size_t)item.bh * p.Lmax;
+    int pos = item.begin + lane < item.end ? __ldg(kl + item.begin + lane) : 0;
+    for (int t0 = item.begin; t0 < item.end; t0 += kStageTokens, ++gs) {
+      const int slot = gs % kStages;
+      const int valid = min(kStageTokens, item.end - t0);
+      const int tn = t0 + kStageTokens + lane;
+      const int pos_next = tn < item.end ? __ldg(kl + tn) : 0;
+      if (gs >= kStages) {
+        bool ok = true;
+        if (lane == 0)
+          ok = !*abort_flag && mbar_wait(empty0 + 8 * slot, ((gs / kStages) - 1) & 1, p.wait_ns);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          if (lane == 0) {
+            atomicOr(p.status, KVX_DEV_TIMEOUT);
+            *abort_flag = 1;
+          }
+          dead = true;
+          break;
+        }
+      }
+      // Failure-detection test only: the chosen block arms nothing for its
+      // first stage, so that stage's wait runs out.
+      if (gs == 0 && (int)blockIdx.x == p.stall_block) {
+        pos = pos_next;
+        continue;
+      }
+      const uint32_t full = full0 + 8 * slot;
+      if (lane < valid) {
+        const bool in = pos >= 0 && pos < p.Lmax;
+        if (!in) atomicOr(p.status, KVX_DEV_BAD_BLOCK);
+        const size_t off = (head_row0 + (size_t)(in ? pos : 0)) * (size_t)(D * 2);
+        const char *ks = (const char *)p.kdense + off;
+        const char *vs = (const char *)p.vdense + off;
+        const uint32_t nbytes = in ? 16u : 0u;
+        const uint32_t kd = stage0 + slot * C::kStage + (uint32_t)lane * 128u;
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t so =
+                (uint32_t)hf * (kStageTokens * 128) + ((uint32_t)(c ^ (lane & 7)) << 4);
+            cp_async_16(kd + so, ks + hf * 128 + c * 16, nbytes, pol);
+            cp_async_16(kd + C::kTile + so, vs + hf * 128 + c * 16, nbytes, pol);
+          }
+      }
+      cp_async_mbar_arrive(full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full);
+      pos = pos_next;
+    }
+  }
+}
+
 // Merge of a head whose pieces ran on blocks of one thread-block cluster
 // (distributed shared memory, this GPU only). Every piece's block has left
 // its merged (m, l, o) in its own ring, which is idle once its last item is
@@ -278,7 +352,7 @@ __device__ __forceinline__ void consume_stage(
 // kCluster: the launch runs in thread-block clusters and merges cluster heads
 // through distributed shared memory (a separate instance, so that launches
 // without clusters carry none of that code).
-template <int D, int VM, bool kCluster>
+template <int D, int VM, bool kCluster, bool kKept>
 __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     attn_mma_kernel(const __grid_constant__ AttnParams p) {
   using C = Cfg<D>;
@@ -320,7 +394,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kCons && lane < p.num_groups) {
+  if (!kKept && warp == kCons && lane < p.num_groups) {
     prefetch_tensormap(&p.tmK[lane]);
     prefetch_tensormap(&p.tmV[lane]);
   }
@@ -333,7 +407,7 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
   if (kCluster) cluster_arrive();
   // Everything above touches only this block's shared memory and the kernel
   // parameters; global inputs may come from the previous kernel in the stream.
-  if (warp == kCons - 1 && p.pf_tokens > 0) {
+  if (!kKept && warp == kCons - 1 && p.pf_tokens > 0) {
     // While that kernel finishes, warm L2 with the first pf_tokens tokens of
     // this block's items (done by the consumer warp whose first stage comes
     // last, so that the producer's first loads are not held up). A prefetch changes no data, so a page-table entry
@@ -375,7 +449,9 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     int gs = 0;
     bool dead = false;
     bool waited = !p.early_kv;
-    for (int it = it0; it < it1 && !dead; ++it) {
+    if constexpr (kKept)  // kept rows of a dense cache (the host turns early loads off)
+      produce_kept<D>(p, it0, it1, item0, stage0, full0, empty0, abort_flag, pol, lane, gs, dead);
+    for (int it = it0; it < it1 && !dead && !kKept; ++it) {
       const Item item = it == it0 ? item0 : p.items[it];
       const int b = item.bh / p.Hkv, h = item.bh - b * p.Hkv;
       const int gi = p.head_grp[h], row = p.head_row[h];
@@ -471,7 +547,8 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
     const int r = lane >> 2, c = lane & 3;
     const float sl2 = p.scale_log2;
     const int box_h = P < kStageTokens ? P : kStageTokens;
-    const LaneAddr la = lane_addr<D>(lane, 31 - __clz(box_h));
+    // kept rows fill a stage as one 32-row tile
+    const LaneAddr la = lane_addr<D>(lane, kKept ? 5 : 31 - __clz(box_h));
     int gs = 0;
     bool dead = false;
     for (int it = it0; it < it1; ++it) {
@@ -673,13 +750,13 @@ __global__ void __launch_bounds__((kCons + 1) * 32, KVX_ATTN_CTAS_PER_SM)
 }
 
 // Sets the kernel instance's shared-memory limit on the current device (once).
-template <int D, int VM, bool kCluster>
+template <int D, int VM, bool kCluster, bool kKept>
 cudaError_t configure_dv() {
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, VM, kCluster>,
+    cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, VM, kCluster, kKept>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (kCluster ? Cfg<D>::kSmemCluster : Cfg<D>::kSmem));
     if (e != cudaSuccess) return e;
@@ -688,9 +765,9 @@ cudaError_t configure_dv() {
   return cudaSuccess;
 }
 
-template <int D, int VM, bool kCluster>
+template <int D, int VM, bool kCluster, bool kKept>
 cudaError_t launch_dvc(const AttnParams &p, int num_ctas, cudaStream_t st) {
-  cudaError_t e = configure_dv<D, VM, kCluster>();
+  cudaError_t e = configure_dv<D, VM, kCluster, kKept>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_ctas);
@@ -709,20 +786,23 @@ cudaError_t launch_dvc(const AttnParams &p, int num_ctas, cudaStream_t st) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  e = cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, VM, kCluster>, p);
+  e = cudaLaunchKernelEx(&cfg, attn_mma_kernel<D, VM, kCluster, kKept>, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <int D, int VM>
 cudaError_t launch_dv(const AttnParams &p, int num_ctas, cudaStream_t st) {
-  return p.cluster > 1 ? launch_dvc<D, VM, true>(p, num_ctas, st)
-                       : launch_dvc<D, VM, false>(p, num_ctas, st);
+  if (p.kept)
+    return p.cluster > 1 ? launch_dvc<D, VM, true, true>(p, num_ctas, st)
+                         : launch_dvc<D, VM, false, true>(p, num_ctas, st);
+  return p.cluster > 1 ? launch_dvc<D, VM, true, false>(p, num_ctas, st)
+                       : launch_dvc<D, VM, false, false>(p, num_ctas, st);
 }
 
 template <int D, int VM>
 int max_clusters_dv(int cluster) {
-  if (configure_dv<D, VM, true>() != cudaSuccess) return 0;
+  if (configure_dv<D, VM, true, false>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)cluster);
   cfg.blockDim = dim3((kCons + 1) * 32);
@@ -735,7 +815,7 @@ int max_clusters_dv(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, attn_mma_kernel<D, VM, true>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, attn_mma_kernel<D, VM, true, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }

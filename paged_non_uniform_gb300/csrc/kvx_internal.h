@@ -93,6 +93,14 @@ struct alignas(128) AttnParams {
   int32_t pf_tokens;           // tokens per block warmed into L2 before the dependency wait
   int32_t early_kv;            // 1: the producer may fill its ring before the dependency wait
   uint64_t wait_ns;            // limit of every pipeline wait
+  // Kept-row attention (kvx_decode_attn_kept): token i of head bh is row
+  // kept[bh * kept_stride + i] of the dense kdense / vdense [B*Hkv][Lmax][D];
+  // null kept: head-group pages through the tensor maps.
+  const int32_t *kept;
+  const void *kdense;
+  const void *vdense;
+  int32_t kept_stride;
+  int32_t Lmax;
   int8_t head_grp[KVX_MAX_KV_HEADS];
   int8_t head_row[KVX_MAX_KV_HEADS];
 };

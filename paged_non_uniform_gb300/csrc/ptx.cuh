@@ -1,6 +1,6 @@
 // ptx.cuh -- inline-PTX helpers for sm_103a used by the kvx kernels:
-// mbarriers with bounded waits, bulk-tensor (TMA) loads, ldmatrix, the
-// m16n8k16 bf16 warp MMA, movmatrix and ex2.
+// mbarriers with bounded waits, bulk-tensor (TMA) loads, asynchronous 16-byte
+// copies, ldmatrix, the m16n8k16 bf16 warp MMA, movmatrix and ex2.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -70,6 +70,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+
+// ---- asynchronous 16-byte copies, completion tracked by an mbarrier ------
+// Copies 16 bytes from global `src` to shared `dst`, reading the first
+// src_bytes (0 or 16) and zero-filling the rest, under L2 cache policy `pol`
+// (the global side goes through L2 only).
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes,
+                                            uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst),
+               "l"(src), "r"(src_bytes), "l"(pol)
+               : "memory");
+}
+
+// Makes `bar` receive one arrival once every cp.async this thread has issued
+// so far has landed. The barrier's pending count is raised by one when this
+// executes, so the arrival does not use up the count it was initialised with.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ---- bulk tensor (TMA) --------------------------------------------------

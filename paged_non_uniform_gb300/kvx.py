@@ -120,6 +120,8 @@ lib.kvx_select_topk.argtypes = [_vp, _vp, _vp, _c.c_int32, _c.c_int32, _c.c_int3
                                 _vp]
 lib.kvx_pack_kept.argtypes = [_vp, _vp, _vp, _c.c_int32, _vp, _c.c_int32, _vp, _vp, _vp, _vp,
                               _vp, _vp, _c.c_size_t, _vp]
+lib.kvx_decode_attn_kept.argtypes = [_vp, _vp, _vp, _vp, _c.c_int32, _vp, _c.c_int32, _vp,
+                                     _vp, _c.c_float, _vp, _vp, _c.c_size_t, _vp]
 
 class kvx_frame_stats(_c.Structure):
     _fields_ = [("commits", _c.c_int64), ("free_blocks", _c.c_int64),
@@ -382,6 +384,18 @@ def kvx_pack_kept(plan: Plan, keys, values, Lmax, kept_idx, kept_stride, k_pools
                            pp.ctypes.data, _ptr_array(page_tables), ps.ctypes.data,
                            _dptr(workspace), int(workspace_bytes), _stream(stream))
     _check(rc, "kvx_pack_kept")
+
+
+def kvx_decode_attn_kept(plan: Plan, q, keys, values, Lmax, kept_idx, kept_stride, head_budget,
+                         seq_len, scale, out, workspace, workspace_bytes=None,
+                         stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = lib.kvx_decode_attn_kept(plan.handle, _dptr(q), _dptr(keys), _dptr(values), int(Lmax),
+                                  _dptr(kept_idx), int(kept_stride), _dptr(head_budget),
+                                  _dptr(seq_len), float(scale), _dptr(out), _dptr(workspace),
+                                  int(workspace_bytes), _stream(stream))
+    _check(rc, "kvx_decode_attn_kept")
 
 
 def kvx_gather_coalesce_noalloc(block_table, num_blocks, S, max_blocks, pools, num_phys_blocks,

@@ -228,6 +228,21 @@ def test_select_and_pack_reject_bad_arguments(kvx):
     assert rc == kvx.KVX_ESTATE
 
 
+def test_kept_row_attention_rejects_bad_arguments(kvx):
+    case = synth.tiny(0)
+    plan = _plan(kvx, case, num_ctas=2)
+    f = kvx.lib.kvx_decode_attn_kept
+    # null dense caches or kept list, then a plan that was never uploaded
+    assert f(plan.handle, 256, None, 256, 100, 256, 100, 256, 256, 0.0, 256, 256, 1 << 20,
+             None) == kvx.KVX_EINVAL
+    assert f(plan.handle, 256, 256, 256, 100, None, 100, 256, 256, 0.0, 256, 256, 1 << 20,
+             None) == kvx.KVX_EINVAL
+    assert f(None, 256, 256, 256, 100, 256, 100, 256, 256, 0.0, 256, 256, 1 << 20,
+             None) == kvx.KVX_EINVAL
+    assert f(plan.handle, 256, 256, 256, 100, 256, 100, 256, 256, 0.0, 256, 256, 1 << 20,
+             None) == kvx.KVX_ESTATE
+
+
 @pytest.mark.parametrize("name", ["qwen3_4b", "llama3_sparse", "qwen25_32b"])
 @pytest.mark.parametrize("num_ctas", [152, 304, 1000])
 def test_balanced_plan_cap(kvx, name, num_ctas):

@@ -117,7 +117,9 @@ def test_selection_ties_and_edges():
 def test_select_pack_attend_end_to_end(layout):
     """GPU selection -> packing into head-group pages -> attention, against the
     oracle's selection and attention, head by head where the kept sets agree;
-    the packed slots are compared bit for bit with the dense rows."""
+    the packed slots are compared bit for bit with the dense rows, and
+    attention straight over the kept rows (kvx_decode_attn_kept, same plan)
+    with the packed path's output."""
     B, Hq, Hkv, D, P = 2, 32, 8, 128, 16
     top, recent = 512, 64
     q, k, v, L = make(4, B, Hq, Hkv, D, [6000, 4000])
@@ -146,6 +148,15 @@ def test_select_pack_attend_end_to_end(layout):
     torch.cuda.synchronize()
     assert kvx.kvx_workspace_status(ws) == 0
     got = out.cpu().numpy().astype(np.float64)
+    # the same plan straight over the kept rows of the dense cache (no
+    # packing): the same bits
+    out2 = torch.full((B, Hq, D), float("nan"), device="cuda")
+    kvx.kvx_decode_attn_kept(plan, _bf16(q), kd, vd, k.shape[2], torch.from_numpy(kept).cuda(),
+                             top + recent, torch.from_numpy(n.reshape(-1).copy()).cuda(),
+                             torch.from_numpy(L).cuda(), 0.0, out2, ws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == 0
+    assert np.array_equal(out2.cpu().numpy().astype(np.float64), got)
     # packed slots: bit-exact copies of the dense rows the GPU selected
     rows = pages.head_rows(hg)
     kbits = synth.f32_to_bf16_bits(k)
