@@ -164,7 +164,8 @@ def test_full_size_select_pack_attend(table):
     x 122k, one layer): GPU selection, packing of the kept rows into
     head-group pages, attention over them. Every head: packed slots equal the
     dense rows bit for bit, and the output equals the oracle's attention over
-    the same kept set."""
+    the same kept set; attention straight over the kept rows
+    (kvx_decode_attn_kept, same plan) gives the same bits."""
     cfg = synth.decode_config("llama3_sparse", seed=0, layers=1)
     B, Hq, Hkv, D, L, P = cfg.B, cfg.Hq, cfg.Hkv, cfg.D, int(cfg.seq_len[0]), cfg.P
     top, recent = 2048, 128
@@ -200,6 +201,13 @@ def test_full_size_select_pack_attend(table):
     torch.cuda.synchronize()
     assert kvx.kvx_workspace_status(aws) == 0
     got = out.cpu().numpy().astype(np.float64)
+    # the same plan straight over the kept rows of the dense cache: the same bits
+    out2 = torch.full((B, Hq, D), float("nan"), device="cuda")
+    kvx.kvx_decode_attn_kept(plan, qd, keys, vals, L, kept, top + recent,
+                             torch.from_numpy(n.reshape(-1).copy()).cuda(), sl, 0.0, out2, aws)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(aws) == 0
+    assert np.array_equal(out2.cpu().numpy().astype(np.float64), got)
     kept_h = kept.cpu().numpy()
     orc = oracle.load()
     g = Hq // Hkv

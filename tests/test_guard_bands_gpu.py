@@ -46,6 +46,31 @@ def test_attention_output_and_workspace_bands(kernel):
     assert torch.isfinite(out).all()
 
 
+def test_kept_row_attention_output_and_workspace_bands():
+    case = synth.dense_case(2, 16, 4, 128, [700, 333], [[700, 70, 33, 1], [333, 200, 1, 64]],
+                            "bf16", seed=4, P=16, head_group=[0, 1, 1, 0])
+    plan = make_plan(case, num_ctas=7)
+    conv = lambda a: torch.from_numpy(synth.f32_to_bf16_bits(a).view(np.int16)).view(
+        torch.bfloat16).cuda()
+    Lmax = case.k.shape[2]
+    stride = max(len(x) for x in case.kept)
+    kept = np.full((len(case.kept), stride), -1, np.int32)
+    for i, x in enumerate(case.kept):
+        kept[i, :len(x)] = x
+    out, out_w = guarded(case.B * case.Hq * case.D * 4, torch.float32, 0)
+    wsb = (plan.workspace_bytes() + 255) // 256 * 256
+    ws, ws_w = guarded(wsb, torch.int32, 0)
+    kvx.kvx_decode_attn_kept(plan, conv(case.q), conv(case.k), conv(case.v), Lmax,
+                             torch.from_numpy(kept).cuda(), stride,
+                             torch.from_numpy(case.budget.reshape(-1).astype(np.int32)).cuda(),
+                             torch.from_numpy(case.seq_len.astype(np.int32)).cuda(), 0.0,
+                             out.view(case.B, case.Hq, -1), ws, workspace_bytes=wsb)
+    torch.cuda.synchronize()
+    assert kvx.kvx_workspace_status(ws) == 0
+    assert intact(out_w) and intact(ws_w)
+    assert torch.isfinite(out).all()
+
+
 def test_gather_staging_and_workspace_bands():
     cfg = synth.gather_config(seed=4, S=10, Lmin=1, Lmax=640, token_bytes=4, num_phys=2048,
                               extents=True, max_extent=6)
