@@ -555,8 +555,9 @@ int kvx_pack_kept(const kvx_plan *plan, const void *keys, const void *values,
  * each head's selected critical entries; Tangram, Fig. 13: the plan's split).
  *   plan        bf16 plan whose kept count n[b][h] is the number of entries of
  *               head (b, h)'s kept list that it attends to (for example
- *               kvx_select_topk's kept_count passed as head_budget to
- *               kvx_plan_create); any page size and work-split policy.
+ *               kvx_select_topk's kept_count, copied to the host, as the
+ *               head_budget of kvx_plan_create); any page size, layout and
+ *               work-split policy (pages play no part here).
  *   q, out, head_budget, seq_len, scale, workspace: as for kvx_decode_attn.
  *   keys, values  device bf16 [B][Hkv][Lmax][D], 16-byte aligned.
  *   kept_idx    device int32 [B*Hkv][kept_stride]: token i of head
