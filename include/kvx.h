@@ -64,7 +64,9 @@ extern "C" {
 #define KVX_DEV_BAD_PAGE 1u    /* a page-table entry outside [0, pool_pages) */
 #define KVX_DEV_BAD_BUDGET 2u  /* min(seq_len, head_budget) differs from the plan */
 #define KVX_DEV_TIMEOUT 4u     /* a pipeline wait gave up after its time limit */
-#define KVX_DEV_BAD_BLOCK 8u   /* a block-table entry outside [0, num_phys_blocks) */
+#define KVX_DEV_BAD_BLOCK 8u   /* a block-table entry outside [0, num_phys_blocks);
+                                  a kept index outside [0, Lmax) (packing,
+                                  kept-row attention) */
 #define KVX_DEV_BAD_LENGTH 16u /* num_blocks[s] outside [0, max_blocks] or the row;
                                   a selection seq_len outside [0, Lmax] */
 
