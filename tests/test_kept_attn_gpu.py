@@ -11,7 +11,7 @@ import torch
 import oracle
 import synth
 from harness import DeviceCase, make_plan, max_abs, oracle_out
-from test_attn_gpu import BF16_CASES, TOL_BF16
+from test_attn_gpu import BF16_CASES, EXTREME_CASES, TOL_BF16
 from paged_non_uniform_gb300 import kvx
 
 pytestmark = pytest.mark.gpu
@@ -74,6 +74,20 @@ def test_kept_rows_match_oracle_and_packed_pages(name, num_ctas):
     assert max_abs(got, oracle_out(case)) <= TOL_BF16
     paged = DeviceCase(case, plan).run()
     assert np.array_equal(got, paged)
+
+
+@pytest.mark.parametrize("name", sorted(EXTREME_CASES))
+def test_kept_rows_extreme_shapes(name):
+    """64 KV heads without GQA (16 groups, 128-token pages), GQA 7 at D = 64
+    (8-token pages), GQA 3: bit-equal to the packed pages, within tolerance of
+    the oracle."""
+    case = EXTREME_CASES[name]()
+    plan = make_plan(case, num_ctas=0)
+    kc = KeptCase(case, plan)
+    got = kc.run()
+    assert kc.status() == 0
+    assert max_abs(got, oracle_out(case)) <= TOL_BF16
+    assert np.array_equal(got, DeviceCase(case, plan).run())
 
 
 @pytest.mark.parametrize("name", ["qwen3_like", "sparse_like", "p64"])
