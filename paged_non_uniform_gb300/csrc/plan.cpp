@@ -74,23 +74,35 @@ static void finish_splits(kvx_plan *p) {
       p->cta_tokens[c] += p->items[i].end - p->items[i].begin;
 }
 
-// Greedy fill of `heads` (in order) into blocks of cost at most `cap` each
-// (tokens + c0 per item; a head's last sliver under one cut may pass the
-// cap), cutting at multiples of cut_tokens; returns the number of blocks used, or
-// max_ctas + 1 if they do not suffice (out is then partial).
+// Blocks dispatched last. A launch that follows another kernel gets its
+// blocks placed, in index order, into the slots that kernel's blocks free as
+// they leave; the last blocks start latest (up to about 2 us after the median
+// on a short launch) and have had the least time to fill their rings before
+// the dependency wait. The last kLateFrac of the blocks are therefore charged
+// kLateTokens more (measured on back-to-back decode layers: the sparse step
+// 2.3 % faster, the Qwen3-4B and 32k steps 0.2 %, Qwen2.5-32B unchanged).
+constexpr double kLateFrac = 0.3;
+constexpr double kLateTokens = 48.0;
+
+// Greedy fill of `heads` (in order) into blocks of cost at most `cap` each,
+// less kLateTokens for the last kLateFrac of the blocks (tokens + c0 per
+// item; a head's last sliver under one cut may pass the cap), cutting at
+// multiples of cut_tokens; returns the number of blocks used, or max_ctas + 1
+// if they do not suffice (out is then partial).
 static int fill_blocks(const kvx_plan *p, const std::vector<int> &heads, double cap, double c0,
                        int max_ctas, std::vector<std::vector<Item>> *out) {
   const int T = cut_tokens(p);
   int c = 0;
   double used = 0;
   if (out) out->assign(max_ctas, {});
+  const int late0 = (int)std::ceil((1.0 - kLateFrac) * max_ctas);
   for (int bh : heads) {
     const int n = p->n[bh];
     int pos = 0;
     while (pos < n) {
       if (c >= max_ctas) return max_ctas + 1;
       const int rem = n - pos;
-      const double left = cap - used;
+      const double left = cap - (c >= late0 ? kLateTokens : 0.0) - used;
       if (left >= rem + c0) {
         if (out) (*out)[c].push_back(Item{bh, pos, n, -1, -1, 0, 0, 0});
         used += rem + c0;
@@ -116,8 +128,9 @@ static int fill_blocks(const kvx_plan *p, const std::vector<int> &heads, double 
 
 // Balanced: lay the heads' kept tokens end to end, charge each item its
 // tokens plus a fixed overhead, and cut the stream into at most num_ctas
-// blocks whose cost is at most a common cap, at multiples of cut_tokens; the cap is
-// the smallest (to a token) with which the stream fits.
+// blocks whose cost is at most a common cap (less the late charge for the
+// blocks dispatched last), at multiples of cut_tokens; the cap is the smallest
+// (to a token) with which the stream fits.
 static void plan_balanced(kvx_plan *p, int num_ctas) {
   const int H = p->shape.B * p->shape.Hkv;
   const double c0 = item_overhead_tokens();
